@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Benchmark of the tiled-attention hot path on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole path over one batch: fa_fwd (O, L) followed by
+fa_bwd (Dlt/lse preprocess, the recompute-P backward kernel, dQ conversion) on
+the multi-head LLM-shaped layer B=4, H=32, Nq=Nk=4096, D=128, causal, bf16
+Q/K/V/dO ~ N(0,1)*0.5 from the seeded recipe.  FLOPs per step follow the
+4*B*H*Nq*Nk*D forward convention (halved for causal) plus 2.5x that for the
+backward.  Inputs (4 x 134 MB) exceed the 129 MB L2, so no flush is needed.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-cpu-baseline]
+
+Multi-GPU: one process per GPU (torchrun); every rank runs the same per-GPU
+workload (weak scaling, no collective on the data path); the step time is the
+max over ranks and `value` the work of all ranks over it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s (bf16 causal H=32 N=4096 D=128), % of TC peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+BWD_SOURCES = ["tiled_attention_11_gb300/csrc/bwd_sm103a.cu", "tiled_attention_11_gb300/csrc/ptx_sm103a.cuh"]
+FWD_SOURCES = ["tiled_attention_11_gb300/csrc/fwd_sm103a.cu", "tiled_attention_11_gb300/csrc/ptx_sm103a.cuh"]
+
+
+# ------------------------------------------------------------------ host helpers (CPU-testable)
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's step time."""
+    return flops_per_step_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_sha(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, sources) -> float | None:
+    """DRAM bytes per launch from a committed ncu summary, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(kernel)
+    if not d or d.get("source_sha") != sources_sha(sources):
+        return None
+    return float(d["dram_bytes_per_launch"])
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
+
+    def stop(self, gpu_index: int = 0):
+        if self.proc is None:
+            return {"samples": 0, "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) != 9:
+                    continue
+                try:
+                    if int(parts[0]) != gpu_index:
+                        continue
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0}
+        reasons = sorted({n for r in rows for n, v in zip(self.NAMES, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_sample(p, seconds_target: float, max_heads: int, seed: int = 0):
+    """Time the fp64 oracle (fwd + bwd) on whole heads of the workload until about
+    `seconds_target` of CPU work; returns (TFLOP/s by the path's convention, heads, seconds)."""
+    import oracle
+    from tiled_attention_11_gb300 import inputs as I
+    q, k, v, do = I.draw(p, seed)
+    per_head = (I.flops_fwd(p) + I.flops_bwd(p)) / (p.B * p.H)
+    t_total, n = 0.0, 0
+    while n < max_heads and (n == 0 or t_total < seconds_target):
+        b, h = divmod(n % (p.B * p.H), p.H)
+        qd, kd, vd, dod = (I.as_f64(t[b, h]) for t in (q, k, v, do))
+        t0 = time.perf_counter()
+        oracle.forward_head(qd, kd, vd, p.scale, p.causal)
+        oracle.backward_head(qd, kd, vd, dod, p.scale, p.causal)
+        t_total += time.perf_counter() - t0
+        n += 1
+    return per_head * n / t_total / 1e12, n, t_total
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from tiled_attention_11_gb300 import _lib
+    from tiled_attention_11_gb300 import inputs as I
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not os.path.exists(_lib.LIB_PATH):
+        if local == 0:
+            from tiled_attention_11_gb300.build import build
+            build()
+        if world > 1:
+            dist.barrier()
+    _lib.lib()
+
+    p = I.LAYER
+    flops_fwd, flops_bwd = I.flops_fwd(p), I.flops_bwd(p)
+    flops_step = flops_fwd + flops_bwd
+    q, k, v, do = I.draw(p, seed=rank)
+    pin = [t.pin_memory() for t in (q, k, v, do)]
+    qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qg)
+    lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
+    ws = torch.empty(_lib.fa_bwd_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D), dtype=torch.uint8, device=dev)
+
+    def fwd():
+        _lib.fa_fwd(qg, kg, vg, o, lse, p.causal, p.scale)
+
+    def bwd():
+        _lib.fa_bwd(qg, kg, vg, o, lse, dog, dq, dk, dv, p.causal, p.scale, workspace=ws)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    fb, fe, bb, be, mb, me = ([ev() for _ in range(K)] for _ in range(6))
+    s = torch.cuda.current_stream()
+    for e in fb + fe + bb + be + mb + me:
+        e.record(s)  # create the underlying CUDA events before the timed region
+    start, end = ev(), ev()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler()
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(s)
+    for i in range(K):
+        fb[i].record(s)
+        fwd()
+        fe[i].record(s)
+        _lib.fa_set_bwd_main_events(mb[i], me[i])
+        bb[i].record(s)
+        bwd()
+        be[i].record(s)
+    end.record(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    _lib.fa_set_bwd_main_events(None, None)
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    smi_index = int(visible.split(",")[local]) if visible and visible.split(",")[local].isdigit() else local
+    clk = clocks.stop(smi_index)
+
+    ms_step = max_over_ranks(start.elapsed_time(end) / K, dev)
+    fwd_ms = statistics.mean(fb[i].elapsed_time(fe[i]) for i in range(K))
+    bwd_ms = statistics.mean(bb[i].elapsed_time(be[i]) for i in range(K))
+    main_ms = statistics.mean(mb[i].elapsed_time(me[i]) for i in range(K))
+    rc, site = _lib.fa_device_status()
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} (wait site {site}) after the timed region")
+
+    # ---------------- end to end: pinned host -> device, fwd + bwd, results -> pinned host
+    outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs_host)
+    K2 = max(1, min(K, args.e2e_steps))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e2e_s, e2e_e = ev(), ev()
+    e2e_s.record(s)
+    for _ in range(K2):
+        for dst, src in zip((qg, kg, vg, dog), pin):
+            dst.copy_(src, non_blocking=True)
+        fwd()
+        bwd()
+        for dst, src in zip(outs_host, (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+    e2e_e.record(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e2e_ms = max_over_ranks(e2e_s.elapsed_time(e2e_e) / K2, dev)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    fwd_tf = flops_fwd / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = flops_bwd / (bwd_ms * 1e-3) / 1e12
+    main_tf = flops_bwd / (main_ms * 1e-3) / 1e12
+    if main_ms >= fwd_ms:
+        dom, dom_ms, dom_flops, dom_src = "fa_bwd main kernel (bwd_kernel<128,causal>)", main_ms, flops_bwd, BWD_SOURCES
+        traffic = traffic_for("bwd_main_layer", BWD_SOURCES)
+    else:
+        dom, dom_ms, dom_flops, dom_src = "fa_fwd kernel (fwd_kernel<128,causal>)", fwd_ms, flops_fwd, FWD_SOURCES
+        traffic = traffic_for("fwd_layer", FWD_SOURCES)
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+
+    out = {
+        "metric": METRIC,
+        "value": round(job_throughput(flops_step, world, ms_step), 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V/dO; no dataset)",
+        "config": {"workload": "multi-head LLM-shaped attention layer fwd+bwd: B=4 H=32 Nq=Nk=4096 D=128 causal",
+                   "B": p.B, "H": p.H, "Nq": p.Nq, "Nk": p.Nk, "D": p.D, "causal": True,
+                   "flops_per_step": flops_step, "l2": "inputs larger than L2 (Q,K,V,dO = 537 MB), no flush"},
+        "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tf, 1), "pct_peak_sustained": round(100 * fwd_tf / sustained, 1),
+                "pct_peak_burst": round(100 * fwd_tf / burst, 1)},
+        "bwd": {"ms": round(bwd_ms, 4), "tflops": round(bwd_tf, 1), "pct_peak_sustained": round(100 * bwd_tf / sustained, 1),
+                "pct_peak_burst": round(100 * bwd_tf / burst, 1), "main_kernel_ms": round(main_ms, 4),
+                "main_kernel_tflops": round(main_tf, 1)},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": sustained, "unit": "TFLOP/s", "frac": round(achieved / sustained, 4),
+                     "peak_kind": f"bf16_tflops_sustained ({peak_src}; kernel timed inside a seconds-long loop)",
+                     "frac_of_burst": round(achieved / burst, 4),
+                     "traffic": traffic, "algorithmic_flops_per_launch": dom_flops},
+        "e2e": {"value": round(job_throughput(flops_step, world, e2e_ms), 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "steps": K2, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        val, n, secs = oracle_sample(p, args.cpu_seconds, max_heads=p.B * p.H)
+        out["cpu_baseline"] = {"value": round(val, 6), "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                               "sample": f"fp64 numpy oracle fwd+bwd on {n} whole head(s) of the workload "
+                                         f"({secs:.1f} s of CPU work), FLOPs by the same convention"}
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+def run_reference(args):
+    from tiled_attention_11_gb300 import inputs as I
+    import oracle
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    p = I.LAYER
+    q, k, v, do = I.draw(p, 0)
+    per_head = (I.flops_fwd(p) + I.flops_bwd(p)) / (p.B * p.H)
+
+    def step(i):
+        b, h = divmod(i % (p.B * p.H), p.H)
+        qd, kd, vd, dod = (I.as_f64(t[b, h]) for t in (q, k, v, do))
+        oracle.forward_head(qd, kd, vd, p.scale, p.causal)
+        oracle.backward_head(qd, kd, vd, dod, p.scale, p.causal)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    secs = time.perf_counter() - t0
+    ms = secs * 1e3 / args.steps
+    val = per_head / (ms * 1e-3) / 1e12
+    cores = blas_threads()
+    sample = "fp64 numpy oracle fwd+bwd on one whole head of the workload per step"
+    out = {
+        "metric": METRIC, "value": round(val, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1)*0.5 bf16 Q/K/V/dO; no dataset)",
+        "impl": "reference",
+        "config": {"workload": "multi-head LLM-shaped attention layer fwd+bwd: B=4 H=32 Nq=Nk=4096 D=128 causal",
+                   "B": p.B, "H": p.H, "Nq": p.Nq, "Nk": p.Nk, "D": p.D, "causal": True,
+                   "sample": "one head (1/128 of the layer) per step"},
+        "cpu_baseline": {"value": round(val, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

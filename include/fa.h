@@ -1,0 +1,125 @@
+/*
+ * C ABI of the GB300 (sm_103a) tiled-attention library (libta11_fa.so).
+ *
+ * The library computes exact scaled-dot-product attention tile by tile with an
+ * online softmax, forward and backward, on one GPU.  The method and its notation
+ * follow the pages this library restates:
+ *   [FA2-impl]  "FlashAttention-2实现与优化：高效注意力机制详解"
+ *   [FA-hist]   "FlashAttention技术演进全景图"
+ *   [FA-mem]    "解释FlashAttention的显存优化原理"
+ *
+ * Conventions shared by every call
+ *   - Tensors are dense, contiguous, row-major [B, H, N, D] (D innermost) in
+ *     bf16 (__nv_bfloat16); "void*" arguments are such bf16 device pointers.
+ *     With H = 1 this is the [B, N, D] layout of [FA2-impl] §3.1/§3.2.
+ *   - lse is fp32 [B, H, Nq]: the natural-log row logsumexp of the scaled
+ *     scores, L_i = m_i + log(sum_j exp(S_ij - m_i)) ([FA2-impl] §3.1, L = m + log l).
+ *   - Supported head dims: D in {16, 32, 64, 128}.  B, H, Nq, Nk >= 1;
+ *     ceil(Nq/128) and ceil(Nk/128) <= 65535.  scale must be finite and > 0
+ *     (the usual value is 1/sqrt(D), [FA2-impl] §3.1).
+ *   - causal != 0 keeps key j for query i iff j <= i on absolute indices
+ *     (top-left alignment, [FA2-impl] §4.3), for any Nq, Nk.  Masked keys get
+ *     exactly zero weight (the pages fill with -1e6; this library uses -inf).
+ *   - Every device pointer must be non-null and 16-byte aligned (TMA); lse must
+ *     be 4-byte aligned; the bwd workspace 256-byte aligned.  Output buffers
+ *     may not overlap inputs or each other.
+ *   - Ownership: the caller allocates and frees every buffer.  The library never
+ *     allocates device memory and keeps no state between calls except the
+ *     device status word below and a per-process wait limit.
+ *   - Asynchrony: calls enqueue work on `stream` and return without
+ *     synchronising.  A failed check returns its code and launches nothing.
+ *     Launch errors are reported as FA_ERR_LAUNCH.
+ *   - Thread safety: re-entrant; work on different streams is independent.
+ *   - Device: the current CUDA device must be sm_103 (GB300); otherwise
+ *     FA_ERR_DEVICE.  There is no CPU fallback.
+ */
+#ifndef TA11_FA_H_
+#define TA11_FA_H_
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad scale, overlapping buffers */
+  FA_ERR_UNSUPPORTED_D = 2, /* D not in {16, 32, 64, 128} */
+  FA_ERR_MISALIGNED = 3,    /* pointer alignment below the stated minimum */
+  FA_ERR_WORKSPACE = 4,     /* bwd workspace null, misaligned or too small */
+  FA_ERR_DEVICE = 5,        /* no CUDA device, or the current device is not sm_103 */
+  FA_ERR_LAUNCH = 6,        /* a kernel launch or tensor-map encode failed */
+  FA_ERR_TIMEOUT = 7        /* a kernel gave up a bounded wait (see fa_device_status) */
+} fa_status;
+
+/*
+ * Forward: O = softmax(scale * Q K^T [masked]) V and the row logsumexp L.
+ * [FA2-impl] §3.1 (forward(q, k, v, is_causal) returns o and saves (L, q, k, v, o))
+ * and §3.2 (kernel arguments Q, K, V, O, L, N_QUERIES, N_KEYS, scale, D, IS_CAUSAL).
+ *   q   [B,H,Nq,D] bf16 in      k, v [B,H,Nk,D] bf16 in
+ *   o   [B,H,Nq,D] bf16 out     lse  [B,H,Nq]   fp32 out (natural log)
+ * The N x N score matrix is never written to memory.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
+           float scale, int causal, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes (0 if they are invalid):
+ * dq_accum fp32 [B*H, Nq_pad, D], Dlt fp32 [B*H, Nq_pad] and L*log2(e) fp32
+ * [B*H, Nq_pad], with Nq_pad = 64*ceil(Nq/64), each segment 256-byte aligned.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int D);
+
+/*
+ * Backward: given dO, computes dQ, dK, dV by recomputing P from lse instead of
+ * storing it ([FA-mem] §2(2) recomputation; [FA-hist] §2.2; [FA2-impl] §7 lists the
+ * backward as the next step).  Formulas: dV = P^T dO, dP = dO V^T,
+ * Dlt_i = sum_d dO_id O_id, dS = P o (dP - Dlt), dQ = scale dS K, dK = scale dS^T Q.
+ *   q, o, dO [B,H,Nq,D] bf16 in   k, v [B,H,Nk,D] bf16 in   lse [B,H,Nq] fp32 in
+ *   dq [B,H,Nq,D], dk, dv [B,H,Nk,D] bf16 out
+ *   workspace: >= fa_bwd_workspace_size(...) bytes of device memory, 256-byte
+ *   aligned, owned by the caller, contents on entry ignored (overwritten).
+ * o and lse must be the forward's outputs for the same q, k, v, scale, causal.
+ * dQ accumulates with fp32 atomics, so it is not bitwise deterministic run to run.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+           void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal, void* workspace,
+           size_t workspace_bytes, cudaStream_t stream);
+
+/* Static English description of a status code (never NULL). */
+const char* fa_strerror(int status);
+
+/*
+ * Device status word: FA_OK, or FA_ERR_TIMEOUT once any kernel of this library
+ * gave up a bounded wait on the current device.  Synchronises the device first.
+ * *site (if non-null) receives the internal wait site of the first timeout.
+ * reset != 0 clears the word afterwards.
+ */
+int fa_device_status(unsigned* site, int reset);
+
+/* Per-process limit on every in-kernel wait, in nanoseconds (default 2e9). */
+void fa_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Self-test hook for the timeout path: launches a one-warp kernel that waits,
+ * with the given limit, on a barrier nothing ever arrives on; it then records
+ * FA_ERR_TIMEOUT in the status word and exits normally (no trap, no hang).
+ */
+int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
+
+/*
+ * Timing hook for measurement tools (no counterpart on the pages): while both
+ * events are non-null, every fa_bwd records `begin` on its stream immediately
+ * before launching its main tensor-core kernel and `end` immediately after it,
+ * so cudaEventElapsedTime(begin, end) is that one kernel's duration.  The events
+ * belong to the caller; pass NULL, NULL to stop recording.  Process-wide setting.
+ */
+void fa_set_bwd_main_events(cudaEvent_t begin, cudaEvent_t end);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TA11_FA_H_ */

@@ -120,9 +120,27 @@ def backward_head(q, k, v, do, scale, causal, q_rows=None, k_range=None, row_chu
     full = q_rows is None and k_range is None
     dq = dk = dv = None
 
-    # dQ rows (full or sampled)
-    if full or q_rows is not None:
-        idx = np.arange(nq) if q_rows is None else np.asarray(q_rows)
+    if full:
+        # one pass over row chunks yields every output
+        dq = np.empty_like(q)
+        dk = np.zeros_like(k)
+        dv = np.zeros_like(v)
+        for r0 in range(0, nq, row_chunk):
+            r1 = min(nq, r0 + row_chunk)
+            nkv = _visible_keys(r1, nk, causal)
+            s = _scores(q[r0:r1], k[:nkv], scale, causal, r0)
+            p, _ = _softmax_rows(s)
+            dp = do[r0:r1] @ v[:nkv].T
+            delta = (p * dp).sum(axis=1)
+            ds = p * (dp - delta[:, None])
+            dq[r0:r1] = scale * (ds @ k[:nkv])
+            dv[:nkv] += p.T @ do[r0:r1]
+            dk[:nkv] += scale * (ds.T @ q[r0:r1])
+        return dq, dk, dv
+
+    # dQ rows (sampled)
+    if q_rows is not None:
+        idx = np.asarray(q_rows)
         dq = np.empty((idx.size, q.shape[1]), np.float64)
         for c0 in range(0, idx.size, row_chunk):
             ci = idx[c0:c0 + row_chunk]
@@ -136,9 +154,9 @@ def backward_head(q, k, v, do, scale, causal, q_rows=None, k_range=None, row_chu
             ds = p * (dp - delta[:, None])
             dq[c0:c0 + ci.size] = scale * (ds @ k[:nkv])
 
-    # dK / dV rows (full or a contiguous key range)
-    if full or k_range is not None:
-        k0, k1 = (0, nk) if k_range is None else k_range
+    # dK / dV rows (a contiguous key range)
+    if k_range is not None:
+        k0, k1 = k_range
         dk = np.zeros((k1 - k0, k.shape[1]), np.float64)
         dv = np.zeros((k1 - k0, v.shape[1]), np.float64)
         first_q = k0 if causal else 0  # causal: rows i < k0 never see keys >= k0

@@ -1,0 +1,131 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every symbol
+include/fa.h declares, and rejects bad arguments with the documented codes
+before touching a device.  No compute call is made here.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiled_attention_11_gb300 import _lib
+from tiled_attention_11_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in fa.h but not exported"
+    assert set(declared_functions()) == set(_lib.EXPORTED)
+
+
+def test_strerror_strings(L):
+    for code in range(0, 8):
+        assert len(_lib.strerror(code)) > 3
+    assert "unknown" in _lib.strerror(99)
+
+
+# fake, never-dereferenced device addresses (16-byte aligned, far apart)
+A = 0x10000000
+GAP = 0x10000000
+
+
+def ptrs(n, base=A):
+    return [base + i * GAP for i in range(n)]
+
+
+def fwd_call(L, q, k, v, o, lse, B=2, H=3, Nq=100, Nk=77, D=64, scale=0.125, causal=1):
+    vp = ctypes.c_void_p
+    return L.fa_fwd(vp(q), vp(k), vp(v), vp(o), vp(lse), B, H, Nq, Nk, D, scale, causal, None)
+
+
+def bwd_call(L, p, B=2, H=3, Nq=100, Nk=77, D=64, scale=0.125, causal=1, ws=None, ws_bytes=None):
+    vp = ctypes.c_void_p
+    need = L.fa_bwd_workspace_size(B, H, Nq, Nk, D)
+    ws = p[9] if ws is None else ws
+    ws_bytes = need if ws_bytes is None else ws_bytes
+    return L.fa_bwd(*[vp(x) for x in p[:9]], B, H, Nq, Nk, D, scale, causal, vp(ws), ws_bytes, None)
+
+
+def test_fwd_validation_codes(L):
+    q, k, v, o, lse = ptrs(5)
+    assert fwd_call(L, 0, k, v, o, lse) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, 0) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, lse, D=48) == _lib.FA_ERR_UNSUPPORTED_D
+    assert fwd_call(L, q, k, v, o, lse, D=256) == _lib.FA_ERR_UNSUPPORTED_D
+    assert fwd_call(L, q, k, v, o, lse, Nq=0) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, lse, Nk=-1) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, lse, B=0) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, lse, scale=float("nan")) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, lse, scale=float("inf")) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, lse, scale=-0.1) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, lse, Nq=65536 * 128) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q + 8, k, v, o, lse) == _lib.FA_ERR_MISALIGNED
+    assert fwd_call(L, q, k, v, o + 2, lse) == _lib.FA_ERR_MISALIGNED
+    assert fwd_call(L, q, k, v, o, lse + 2) == _lib.FA_ERR_MISALIGNED
+    # output overlapping an input
+    assert fwd_call(L, q, k, v, q + 1024, lse) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, o + 16) == _lib.FA_ERR_INVALID_ARG
+    # every argument valid: the only failure left is the missing sm_103 device
+    assert fwd_call(L, q, k, v, o, lse) == _lib.FA_ERR_DEVICE
+
+
+def test_bwd_validation_codes(L):
+    p = ptrs(10)
+    assert bwd_call(L, [0] + p[1:]) == _lib.FA_ERR_INVALID_ARG
+    assert bwd_call(L, p, D=8) == _lib.FA_ERR_UNSUPPORTED_D
+    assert bwd_call(L, p[:6] + [p[6] + 4] + p[7:]) == _lib.FA_ERR_MISALIGNED
+    need = L.fa_bwd_workspace_size(2, 3, 100, 77, 64)
+    assert bwd_call(L, p, ws_bytes=need - 1) == _lib.FA_ERR_WORKSPACE
+    assert bwd_call(L, p, ws=0) == _lib.FA_ERR_WORKSPACE
+    assert bwd_call(L, p, ws=p[9] + 128) == _lib.FA_ERR_WORKSPACE
+    # workspace overlapping dq
+    assert bwd_call(L, p[:9] + [p[6] + 256]) == _lib.FA_ERR_INVALID_ARG
+    # dk overlapping an input
+    assert bwd_call(L, p[:7] + [p[0] + 64] + p[8:]) == _lib.FA_ERR_INVALID_ARG
+    assert bwd_call(L, p) == _lib.FA_ERR_DEVICE
+
+
+def test_workspace_size_formula(L):
+    def rnd(x):
+        return (x + 255) // 256 * 256
+    for (B, H, Nq, Nk, D) in [(2, 3, 100, 77, 64), (1, 1, 1, 1, 16), (4, 32, 4096, 4096, 128), (1, 8, 65537, 65537, 128)]:
+        nq_pad = (Nq + 63) // 64 * 64
+        rows = B * H * nq_pad
+        assert L.fa_bwd_workspace_size(B, H, Nq, Nk, D) == rnd(rows * D * 4) + 2 * rnd(rows * 4)
+    assert L.fa_bwd_workspace_size(1, 1, 16, 16, 24) == 0
+    assert L.fa_bwd_workspace_size(0, 1, 16, 16, 64) == 0
+
+
+def test_binding_rejects_missing_gpu():
+    """The Python path has no CPU fallback: without a GPU the call raises."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    q = torch.zeros(1, 1, 8, 16, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        _lib.forward(q, q, q, causal=False)
+
+
+def test_wait_probe_needs_device(L):
+    assert L.fa_wait_probe(1000, None) == _lib.FA_ERR_DEVICE

@@ -263,6 +263,9 @@ MUTATIONS = [
     ("keys reversed in dP", "dp = do[r0:r1] @ v[:nkv].T", "dp = do[r0:r1] @ v[:nkv][::-1].T"),
     ("delta from wrong axis", "delta = (p * dp).sum(axis=1)\n            ds = p * (dp - delta[:, None])\n            hi",
      "delta = (p * dp).sum(axis=1) * 0\n            ds = p * (dp - delta[:, None])\n            hi"),
+    ("dropped scale in full-pass dQ", "dq[r0:r1] = scale * (ds @ k[:nkv])", "dq[r0:r1] = (ds @ k[:nkv])"),
+    ("full-pass dK without scale", "dk[:nkv] += scale * (ds.T @ q[r0:r1])", "dk[:nkv] += (ds.T @ q[r0:r1])"),
+    ("full-pass dV scaled", "dv[:nkv] += p.T @ do[r0:r1]", "dv[:nkv] += 1.01 * (p.T @ do[r0:r1])"),
     ("dV uses dP instead of dO", "dv[:hi - k0] += p[:, k0:hi].T @ do[r0:r1]", "dv[:hi - k0] += p[:, k0:hi].T @ (do[r0:r1] * 1.5)"),
     ("no causal key skipping bound", "return min(nk, row_end) if causal else nk", "return min(nk, row_end - 1) if causal else nk"),
     ("scale applied twice", "s = scale * (q[ci] @ k[:nkv].T)\n        if causal:\n            s = np.where(np.arange(nkv)[None, :] > ci[:, None], NEG_INF, s)\n        p, l",

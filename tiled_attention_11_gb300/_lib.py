@@ -1,0 +1,171 @@
+"""Thin ctypes binding over the C ABI in include/fa.h (argument marshalling only).
+
+Every function here maps torch tensors to device pointers and sizes and calls
+the same-named entry point of ``libta11_fa.so``; all arithmetic runs in the
+library's CUDA kernels.  PyTorch only provides device memory and the current
+stream.  There is no fallback: if the library is missing, or the device is not
+an sm_103 GB300, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libta11_fa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED_D = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_WORKSPACE = 4
+FA_ERR_DEVICE = 5
+FA_ERR_LAUNCH = 6
+FA_ERR_TIMEOUT = 7
+
+EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_device_status",
+            "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events")
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (status {code})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libta11_fa.so (built in-tree by ``build.py``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    L.fa_fwd.restype = i
+    L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+    L.fa_bwd.restype = i
+    L.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    L.fa_bwd_workspace_size.restype = sz
+    L.fa_strerror.argtypes = [i]
+    L.fa_strerror.restype = ctypes.c_char_p
+    L.fa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
+    L.fa_device_status.restype = i
+    L.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    L.fa_set_wait_limit_ns.restype = None
+    L.fa_wait_probe.argtypes = [ctypes.c_ulonglong, vp]
+    L.fa_wait_probe.restype = i
+    L.fa_set_bwd_main_events.argtypes = [vp, vp]
+    L.fa_set_bwd_main_events.restype = None
+    _lib = L
+    return L
+
+
+def strerror(code: int) -> str:
+    return lib().fa_strerror(int(code)).decode()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None, name: str, dtype) -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _check(rc: int, where: str):
+    if rc != FA_OK:
+        raise FAError(rc, where)
+
+
+def fa_bwd_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int) -> int:
+    return int(lib().fa_bwd_workspace_size(B, H, Nq, Nk, D))
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None) -> None:
+    """C ``fa_fwd`` on [B,H,N,D] bf16 tensors; writes o (bf16) and lse (fp32 [B,H,Nq])."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib().fa_fwd(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16), _ptr(v, "v", torch.bfloat16),
+                      _ptr(o, "o", torch.bfloat16), _ptr(lse, "lse", torch.float32),
+                      B, H, Nq, Nk, D, float(scale), int(bool(causal)), _stream(stream))
+    _check(rc, "fa_fwd")
+
+
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None = None, workspace=None,
+           stream=None) -> None:
+    """C ``fa_bwd``; allocates the workspace with torch when none is given."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    need = fa_bwd_workspace_size(B, H, Nq, Nk, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib().fa_bwd(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16), _ptr(v, "v", torch.bfloat16),
+                      _ptr(o, "o", torch.bfloat16), _ptr(lse, "lse", torch.float32),
+                      _ptr(do, "do", torch.bfloat16), _ptr(dq, "dq", torch.bfloat16),
+                      _ptr(dk, "dk", torch.bfloat16), _ptr(dv, "dv", torch.bfloat16),
+                      B, H, Nq, Nk, D, float(scale), int(bool(causal)),
+                      _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(rc, "fa_bwd")
+
+
+def forward(q, k, v, causal: bool, scale: float | None = None, stream=None):
+    """Allocate outputs and run the forward: returns (o, lse)."""
+    B, H, Nq, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, causal: bool, scale: float | None = None, workspace=None, stream=None):
+    """Allocate gradients and run the backward: returns (dq, dk, dv)."""
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal, scale, workspace, stream)
+    return dq, dk, dv
+
+
+def fa_device_status(reset: bool = False):
+    """(code, site) of the device status word; synchronises the device."""
+    site = ctypes.c_uint(0)
+    rc = lib().fa_device_status(ctypes.byref(site), int(bool(reset)))
+    return rc, site.value
+
+
+def fa_set_wait_limit_ns(ns: int) -> None:
+    lib().fa_set_wait_limit_ns(int(ns))
+
+
+def fa_wait_probe(limit_ns: int, stream=None) -> None:
+    _check(lib().fa_wait_probe(int(limit_ns), _stream(stream)), "fa_wait_probe")
+
+
+def fa_set_bwd_main_events(begin=None, end=None) -> None:
+    """Record torch.cuda.Events (already created by one .record()) around the main
+    backward kernel of later fa_bwd calls; None, None turns it off."""
+    b = begin.cuda_event if begin is not None else 0
+    e = end.cuda_event if end is not None else 0
+    lib().fa_set_bwd_main_events(b or None, e or None)

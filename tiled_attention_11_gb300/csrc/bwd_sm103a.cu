@@ -1,0 +1,503 @@
+// Backward pass of exact attention for sm_103a: recompute P from the saved row
+// logsumexp instead of storing it ("解释FlashAttention的显存优化原理" §2(2) 重计算;
+// "FlashAttention技术演进全景图" §2.2 重计算机制; the forward saves (L, q, k, v, o),
+// "FlashAttention-2实现与优化：高效注意力机制详解" §3.1).  The gradient formulas are the
+// softmax Jacobian:  dV = P^T dO,  dP = dO V^T,  Dlt_i = rowsum(dO o O)_i,
+// dS = P o (dP - Dlt),  dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Three kernels, in stream order:
+//   prep     Dlt = rowsum(dO o O) (fp32), lse2 = L*log2(e) (+inf on padded rows),
+//            dq_accum = 0.                                          (HBM-bound)
+//   bwd      one CTA per (batch*head, 128-key tile); K_j, V_j stay in shared memory,
+//            dK_j, dV_j accumulate in TMEM; 64-query tiles Q_i, dO_i stream through
+//            a TMA ring (causal: starting at the diagonal).  Per query tile, all on
+//            tcgen05 (keys on the M=128 axis):
+//              S^T  = K Q_i^T            -> TMEM   P^T = 2^(S^T c - lse2)  (compute WGs)
+//              dP^T = V dO_i^T           -> TMEM   dS^T = P^T o (dP^T - Dlt)
+//              dV  += P^T dO_i   (A = P^T from TMEM)
+//              dK  += dS^T Q_i   (A = dS^T from TMEM)
+//              dQ_i^T = K^T dS^T (both from shared memory) -> TMEM (double-buffered),
+//            then the compute warps add dQ_i into dq_accum with fp32 red.add.
+//   convert  dq = bf16(dq_accum * scale).
+#include "fa_kernels.h"
+#include "ptx_sm103a.cuh"
+
+namespace ta11 {
+namespace bwd {
+
+template <int D>
+struct Cfg {
+  static constexpr int BN = 128;                       // keys per CTA (UMMA M)
+  static constexpr int BM = 64;                        // queries per inner step (UMMA N)
+  static constexpr int CHUNK = D < 64 ? D : 64;
+  static constexpr int NCHUNK = D / CHUNK;
+  static constexpr int ROWB = CHUNK * 2;
+  static constexpr uint32_t LAYOUT = umma_layout_for_swizzle(ROWB);
+  static constexpr int K_CHUNK_BYTES = BN * ROWB;
+  static constexpr int KV_TILE = BN * D * 2;
+  static constexpr int Q_CHUNK_BYTES = BM * ROWB;
+  static constexpr int Q_TILE = BM * D * 2;
+  static constexpr int NS = 2;
+  static constexpr int DS_BYTES = BN * BM * 2;         // dS^T tile, bf16, 128-byte rows
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV_TILE;
+  static constexpr int OFF_Q = 2 * KV_TILE;
+  static constexpr int OFF_DO = OFF_Q + NS * Q_TILE;
+  static constexpr int OFF_DS = OFF_DO + NS * Q_TILE;
+  static constexpr int OFF_LSE = OFF_DS + 2 * DS_BYTES;
+  static constexpr int OFF_DLT = OFF_LSE + NS * BM * 4;
+  static constexpr int OFF_BAR = OFF_DLT + NS * BM * 4;
+  // barriers
+  static constexpr int B_KV = 0;
+  static constexpr int B_QF = 1;             // [NS]
+  static constexpr int B_QE = 1 + NS;        // [NS]
+  static constexpr int B_SF = 1 + 2 * NS;
+  static constexpr int B_DPF = 2 + 2 * NS;
+  static constexpr int B_PF = 3 + 2 * NS;
+  static constexpr int B_DSF = 4 + 2 * NS;
+  static constexpr int B_DQF = 5 + 2 * NS;   // [2]
+  static constexpr int B_DQE = 7 + 2 * NS;   // [2]
+  static constexpr int B_DRAIN = 9 + 2 * NS;
+  static constexpr int NBAR = 10 + 2 * NS;
+  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
+  static constexpr int THREADS = 384;
+  // TMEM columns
+  static constexpr int T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 256 + D;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, BM, false, false);   // S^T, dP^T
+  static constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
+  static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, true, true);    // dQ^T (A, B MN-major)
+  static_assert(Q_TILE % 1024 == 0 && KV_TILE % 1024 == 0, "alignment");
+};
+
+// K-major operand with `rows` rows (chunk = rows * ROWB bytes), kk-th 16-wide K slice.
+template <int D>
+__device__ __forceinline__ uint64_t desc_k(uint32_t tile, uint32_t chunk_bytes, int kk) {
+  using C = Cfg<D>;
+  const int el = kk * 16;
+  return sdesc(tile + (el / C::CHUNK) * chunk_bytes + (el % C::CHUNK) * 2, 16, 8 * C::ROWB, C::LAYOUT);
+}
+
+// MN-major operand stored as rows of D (D contiguous): the K dimension runs over rows.
+template <int D>
+__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, uint32_t lbo, int kk) {
+  using C = Cfg<D>;
+  return sdesc(tile + kk * 16 * C::ROWB, lbo, 8 * C::ROWB, C::LAYOUT);
+}
+
+// TMEM column of the packed bf16 A operand (P^T or dS^T) for the kk-th 16-query slice:
+// queries 0..31 live in columns [0,16), queries 32..63 in [32,48).
+__device__ __forceinline__ uint32_t a_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, site));
+}
+
+__device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
+
+template <int D>
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[16], float mul) {
+  uint4 w0, w1;
+  w0.x = pack_bf16(as_f(v[0]) * mul, as_f(v[1]) * mul);
+  w0.y = pack_bf16(as_f(v[2]) * mul, as_f(v[3]) * mul);
+  w0.z = pack_bf16(as_f(v[4]) * mul, as_f(v[5]) * mul);
+  w0.w = pack_bf16(as_f(v[6]) * mul, as_f(v[7]) * mul);
+  w1.x = pack_bf16(as_f(v[8]) * mul, as_f(v[9]) * mul);
+  w1.y = pack_bf16(as_f(v[10]) * mul, as_f(v[11]) * mul);
+  w1.z = pack_bf16(as_f(v[12]) * mul, as_f(v[13]) * mul);
+  w1.w = pack_bf16(as_f(v[14]) * mul, as_f(v[15]) * mul);
+  reinterpret_cast<uint4*>(dst)[0] = w0;
+  reinterpret_cast<uint4*>(dst)[1] = w1;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const BwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+  const int bh = blockIdx.x;
+  const int kt = blockIdx.y;  // causal: low key tiles see the most queries, launch them first
+  const int k0 = kt * C::BN;
+  const int n_qt = (p.Nq + C::BM - 1) / C::BM;
+  const int i_start = CAUSAL ? min(k0 / C::BM, n_qt) : 0;
+  const int n_it = n_qt - i_start;
+  const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[C::B_KV], 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bars[C::B_QF + s], 1);
+      mbar_init(&bars[C::B_QE + s], 1);
+    }
+    mbar_init(&bars[C::B_SF], 1);
+    mbar_init(&bars[C::B_DPF], 1);
+    mbar_init(&bars[C::B_PF], 256);
+    mbar_init(&bars[C::B_DSF], 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[C::B_DQF + b], 1);
+      mbar_init(&bars[C::B_DQE + b], 256);
+    }
+    mbar_init(&bars[C::B_DRAIN], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && n_it > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&bars[C::B_KV], 2 * C::KV_TILE);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_3d(smem + C::OFF_K + c * C::K_CHUNK_BYTES, &tm_k, &bars[C::B_KV], c * C::CHUNK, k0, bh);
+        tma_load_3d(smem + C::OFF_V + c * C::K_CHUNK_BYTES, &tm_v, &bars[C::B_KV], c * C::CHUNK, k0, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % C::NS;
+        const int i = i_start + it;
+        if (it >= C::NS && !mbar_wait(&bars[C::B_QE + s], ((it / C::NS) - 1) & 1, wc, 31)) break;
+        mbar_arrive_expect_tx(&bars[C::B_QF + s], 2 * C::Q_TILE + 2 * C::BM * 4);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_3d(smem + C::OFF_Q + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_q, &bars[C::B_QF + s],
+                      c * C::CHUNK, i * C::BM, bh);
+          tma_load_3d(smem + C::OFF_DO + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_do, &bars[C::B_QF + s],
+                      c * C::CHUNK, i * C::BM, bh);
+        }
+        const size_t roff = (size_t)bh * p.Nq_pad + (size_t)i * C::BM;
+        bulk_load(smem + C::OFF_LSE + s * C::BM * 4, p.lse2 + roff, C::BM * 4, &bars[C::B_QF + s]);
+        bulk_load(smem + C::OFF_DLT + s * C::BM * 4, p.dlt + roff, C::BM * 4, &bars[C::B_QF + s]);
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+        mbar_wait(&bars[C::B_KV], 0, w2, 40);
+        const int first = issued > C::NS ? issued - C::NS : 0;
+        for (int it = first; it < issued; ++it)
+          mbar_wait(&bars[C::B_QF + it % C::NS], (it / C::NS) & 1, w2, 41);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- UMMA issuer
+    if (lane == 0) {
+      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+      const uint32_t kt_lbo = (D == 128) ? (uint32_t)C::K_CHUNK_BYTES : 0u;  // K^T as A: M = d padded to 128
+      if (n_it > 0 && mbar_wait(&bars[C::B_KV], 0, wc, 32)) {
+        for (int it = 0; it < n_it; ++it) {
+          const int s = it % C::NS;
+          if (!mbar_wait(&bars[C::B_QF + s], (it / C::NS) & 1, wc, 33)) break;
+          tc_fence_after();
+          const uint32_t sQ = sbase + C::OFF_Q + s * C::Q_TILE;
+          const uint32_t sdO = sbase + C::OFF_DO + s * C::Q_TILE;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + C::T_S, desc_k<D>(sK, C::K_CHUNK_BYTES, kk), desc_k<D>(sQ, C::Q_CHUNK_BYTES, kk),
+                    C::IDESC_S, kk > 0 ? 1u : 0u);
+          umma_commit(&bars[C::B_SF]);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + C::T_DP, desc_k<D>(sV, C::K_CHUNK_BYTES, kk), desc_k<D>(sdO, C::Q_CHUNK_BYTES, kk),
+                    C::IDESC_S, kk > 0 ? 1u : 0u);
+          umma_commit(&bars[C::B_DPF]);
+
+          if (!mbar_wait(&bars[C::B_PF], it & 1, wc, 34)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < C::BM / 16; ++kk)
+            umma_ts(tmem + C::T_DV, tmem + C::T_S + a_col(kk), desc_mn<D>(sdO, C::Q_CHUNK_BYTES, kk),
+                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+
+          if (!mbar_wait(&bars[C::B_DSF], it & 1, wc, 35)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < C::BM / 16; ++kk)
+            umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_mn<D>(sQ, C::Q_CHUNK_BYTES, kk),
+                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&bars[C::B_QE + s]);
+
+          const int b = it & 1;
+          if (it >= 2 && !mbar_wait(&bars[C::B_DQE + b], ((it - 2) >> 1) & 1, wc, 36)) break;
+          tc_fence_after();
+          const uint32_t sdS = sbase + C::OFF_DS + b * C::DS_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            umma_ss(tmem + C::T_DQ + b * C::BM, desc_mn<D>(sK, kt_lbo, kk),
+                    sdesc(sdS + kk * 16 * 128, C::DS_BYTES, 1024, 2u), C::IDESC_DQ, kk > 0 ? 1u : 0u);
+          umma_commit(&bars[C::B_DQF + b]);
+        }
+      }
+      umma_commit(&bars[C::B_DRAIN]);
+      volatile int no_abort = 0;
+      const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+      mbar_wait(&bars[C::B_DRAIN], 0, w2, 42);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- compute warpgroups
+    const int wg = (warp - 4) >> 2;  // 0: queries 0..31 of a tile (and dK), 1: queries 32..63 (and dV)
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // key row of the tile (also d for the dQ^T readout)
+    const int key = k0 + row;
+    const int col0 = wg * 32;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = p.scale_log2;
+    uint8_t* sds_row_base = smem + C::OFF_DS + row * 128;
+    bool ok = true;
+
+    auto readout = [&](int t) -> bool {
+      const int b = t & 1;
+      if (!warp_wait(&bars[C::B_DQF + b], (t >> 1) & 1, wc, 37)) return false;
+      tc_fence_after();
+      uint32_t v[32];
+      tmem_ld32(t_lane + C::T_DQ + b * C::BM + col0, v);
+      tmem_wait_ld(v);
+      if (row < D) {
+        float* dst = p.dq_accum + ((size_t)bh * p.Nq_pad + (size_t)(i_start + t) * C::BM + col0) * D + row;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) red_add_f32(dst + (size_t)c * D, as_f(v[c]));
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_DQE + b]);
+      return true;
+    };
+
+    for (int it = 0; it < n_it && ok; ++it) {
+      const int s = it % C::NS;
+      const int i = i_start + it;
+      if (!warp_wait(&bars[C::B_QF + s], (it / C::NS) & 1, wc, 38) || !warp_wait(&bars[C::B_SF], it & 1, wc, 39)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld32(t_lane + C::T_S + col0, sv);
+      tmem_wait_ld(sv);
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * C::BM * 4) + col0;
+      const float* dlt = reinterpret_cast<const float*>(smem + C::OFF_DLT + s * C::BM * 4) + col0;
+      const bool need_mask = (k0 + C::BN > p.Nk) || (CAUSAL && (k0 + C::BN - 1 > i * C::BM + col0));
+      int lim = 1 << 30;  // columns c with q = i*64+col0+c < key are masked (causal)
+      if (CAUSAL) lim = key - (i * C::BM + col0);
+      const bool key_valid = key < p.Nk;
+      float pv[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float x = ex2(fmaf(as_f(sv[c]), sl2, -lse2[c]));
+        if (need_mask && (!key_valid || (CAUSAL && c < lim))) x = 0.f;
+        pv[c] = x;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
+      tmem_st16(t_lane + C::T_S + wg * 32, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_PF]);
+
+      if (!warp_wait(&bars[C::B_DPF], it & 1, wc, 43)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t dv[32];
+      tmem_ld32(t_lane + C::T_DP + col0, dv);
+      tmem_wait_ld(dv);
+      uint32_t dk[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float d0 = pv[2 * c] * (as_f(dv[2 * c]) - dlt[2 * c]);
+        const float d1 = pv[2 * c + 1] * (as_f(dv[2 * c + 1]) - dlt[2 * c + 1]);
+        dk[c] = pack_bf16(d0, d1);
+      }
+      tmem_st16(t_lane + C::T_DP + wg * 32, dk);
+      // dS^T row into shared memory (128-byte rows, 128B swizzle) for the dQ^T MMA.
+      uint8_t* dsrow = sds_row_base + (it & 1) * C::DS_BYTES;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int phys = (4 * wg + t) ^ (row & 7);
+        *reinterpret_cast<uint4*>(dsrow + phys * 16) = make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_DSF]);
+
+      if (it >= 1 && !readout(it - 1)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok && n_it > 0) ok = readout(n_it - 1);
+
+    // epilogue: WG0 writes dK = scale * acc, WG1 writes dV
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) + ((size_t)bh * p.Nk + key) * D;
+    if (n_it == 0) {
+      if (key < p.Nk) {
+        for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(dst + d) = make_uint4(0, 0, 0, 0);
+      }
+    } else if (ok) {
+      tc_fence_after();
+      const float mul = (wg == 0) ? p.scale : 1.f;
+#pragma unroll
+      for (int g = 0; g < D / 16; ++g) {
+        uint32_t v[16];
+        tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + g * 16, v);
+        tmem_wait_ld(v);
+        if (key < p.Nk) store_row_bf16<D>(dst + g * 16, v, mul);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// prep: Dlt = rowsum(dO o O), lse2 = L * log2(e) (+inf past Nq), dq_accum = 0
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
+  constexpr int TPR = D / 8;  // threads per row, 8 bf16 each
+  const long long rows = (long long)p.BH * p.Nq_pad;
+  const long long total = rows * TPR;
+  const int part = threadIdx.x % TPR;
+  for (long long base = (long long)blockIdx.x * blockDim.x; base < total; base += (long long)gridDim.x * blockDim.x) {
+    const long long gid = base + threadIdx.x;
+    const bool active = gid < total;
+    const long long r = gid / TPR;
+    const int bh = (int)(r / p.Nq_pad), q = (int)(r % p.Nq_pad);
+    float acc = 0.f;
+    if (active && q < p.Nq) {
+      const size_t off = ((size_t)bh * p.Nq + q) * D + part * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.o) + off);
+      const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dout) + off);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 fa = __bfloat1622float2(a2[t]);
+        const float2 fb = __bfloat1622float2(b2[t]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+    }
+#pragma unroll
+    for (int w = TPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (active) {
+      float4* z = reinterpret_cast<float4*>(p.dq_accum + (size_t)r * D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (part == 0) {
+        p.dlt[r] = acc;
+        p.lse2[r] = (q < p.Nq) ? p.lse[(size_t)bh * p.Nq + q] * 1.4426950408889634f : INFINITY;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// convert: dq = bf16(dq_accum * scale), rows < Nq only
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) convert_kernel(const ConvParams p) {
+  const long long nvec = (long long)p.BH * p.Nq * (D / 8);
+  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+       v += (long long)gridDim.x * blockDim.x) {
+    const long long e = v * 8;
+    const long long row = e / D;  // bh*Nq + q
+    const int d = (int)(e % D);
+    const int bh = (int)(row / p.Nq), q = (int)(row % p.Nq);
+    const float4* src = reinterpret_cast<const float4*>(p.dq_accum + ((size_t)bh * p.Nq_pad + q) * D + d);
+    const float4 a = src[0], b = src[1];
+    uint4 w;
+    w.x = pack_bf16(a.x * p.scale, a.y * p.scale);
+    w.y = pack_bf16(a.z * p.scale, a.w * p.scale);
+    w.z = pack_bf16(b.x * p.scale, b.y * p.scale);
+    w.w = pack_bf16(b.z * p.scale, b.w * p.scale);
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + e) = w;
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                     const BwdParams& p, int BH, cudaStream_t st) {
+  using C = Cfg<D>;
+  auto kern = bwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)BH, (unsigned)p.n_k_tiles);
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+static int grid_for(long long work_items, int threads) {
+  long long b = (work_items + threads - 1) / threads;
+  const long long cap = 152LL * 16;  // enough resident blocks to saturate HBM on 152 SMs
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return (int)b;
+}
+
+template <int D>
+cudaError_t prep_t(const PrepParams& p, cudaStream_t st) {
+  const long long total = (long long)p.BH * p.Nq_pad * (D / 8);
+  prep_kernel<D><<<grid_for(total, 256), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t conv_t(const ConvParams& p, cudaStream_t st) {
+  const long long total = (long long)p.BH * p.Nq * (D / 8);
+  convert_kernel<D><<<grid_for(total, 256), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+#define TA11_SWITCH_D(D, EXPR_T)       \
+  switch (D) {                         \
+    case 16: { constexpr int DD = 16; return EXPR_T; }   \
+    case 32: { constexpr int DD = 32; return EXPR_T; }   \
+    case 64: { constexpr int DD = 64; return EXPR_T; }   \
+    case 128: { constexpr int DD = 128; return EXPR_T; } \
+    default: return cudaErrorInvalidValue;               \
+  }
+
+cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, int BH, cudaStream_t st) {
+  TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true>(tq, tk, tv, tdo, p, BH, st)
+                           : bwd::launch_t<DD, false>(tq, tk, tv, tdo, p, BH, st)))
+}
+
+cudaError_t launch_bwd_prep(int D, const PrepParams& p, cudaStream_t st) {
+  TA11_SWITCH_D(D, bwd::prep_t<DD>(p, st))
+}
+
+cudaError_t launch_bwd_convert(int D, const ConvParams& p, cudaStream_t st) {
+  TA11_SWITCH_D(D, bwd::conv_t<DD>(p, st))
+}
+
+}  // namespace ta11

@@ -1,0 +1,294 @@
+// Host side of the C ABI declared in include/fa.h: argument validation, TMA
+// tensor-map encoding, kernel launches and the device status word.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_kernels.h"
+
+namespace {
+
+// Device-side status word pair: [0] = FA_OK or FA_ERR_TIMEOUT, [1] = wait site.
+__device__ unsigned g_fa_status[2];
+
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+
+// Optional events recorded around the main backward kernel (timing hook).
+std::mutex g_ev_mu;
+cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int ok = 0;               // 1: sm_103 and status word resolved
+  unsigned* status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+// Resolve the current device: sm_103 check and the status word's device address.
+int current_device(unsigned** status) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return FA_ERR_DEVICE;
+  }
+  DeviceState& s = g_dev[dev];
+  std::call_once(s.once, [&]() {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    if (major != 10 || minor != 3) return;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    s.status = static_cast<unsigned*>(p);
+    s.ok = 1;
+  });
+  if (!s.ok) return FA_ERR_DEVICE;
+  *status = s.status;
+  return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// 3-D bf16 tensor map over [BH][N][D] with a {chunk, box_rows, 1} box and the
+// swizzle that matches a chunk row (32, 64 or 128 bytes).  Loads past N are
+// zero-filled, so heads never read each other's rows.
+bool make_map(CUtensorMap* m, const void* base, int D, int N, int BH, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int chunk = D < 64 ? D : 64;
+  const CUtensorMapSwizzle sw = chunk == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : chunk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)chunk, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+Range rng(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + bytes};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool valid_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
+
+// Shared size checks; returns FA_OK or a code.
+int check_sizes(int B, int H, int Nq, int Nk, int D, float scale) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if ((Nq + 127) / 128 > 65535 || (Nk + 127) / 128 > 65535) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!valid_d(D)) return FA_ERR_UNSUPPORTED_D;
+  return FA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t dq_off, dlt_off, lse2_off, total;
+  int Nq_pad;
+};
+WsLayout ws_layout(int B, int H, int Nq, int D) {
+  WsLayout w;
+  w.Nq_pad = ((Nq + 63) / 64) * 64;
+  const size_t rows = (size_t)B * H * w.Nq_pad;
+  w.dq_off = 0;
+  w.dlt_off = round256(rows * D * 4);
+  w.lse2_off = w.dlt_off + round256(rows * 4);
+  w.total = w.lse2_off + round256(rows * 4);
+  return w;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "success";
+    case FA_ERR_INVALID_ARG: return "invalid argument (null pointer, size, scale or overlapping buffers)";
+    case FA_ERR_UNSUPPORTED_D: return "unsupported head dimension (D must be 16, 32, 64 or 128)";
+    case FA_ERR_MISALIGNED: return "misaligned pointer (bf16 tensors need 16 bytes, lse 4 bytes)";
+    case FA_ERR_WORKSPACE: return "backward workspace null, misaligned (256 bytes) or too small";
+    case FA_ERR_DEVICE: return "no usable device: the current CUDA device must be sm_103 (GB300)";
+    case FA_ERR_LAUNCH: return "kernel launch or TMA descriptor encoding failed";
+    case FA_ERR_TIMEOUT: return "a kernel gave up a bounded wait (device status word)";
+    default: return "unknown status";
+  }
+}
+
+void fa_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns : 1ull); }
+
+size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int D) {
+  if (check_sizes(B, H, Nq, Nk, D, 1.f) != FA_OK) return 0;
+  return ws_layout(B, H, Nq, D).total;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
+           float scale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  int rc = check_sizes(B, H, Nq, Nk, D, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  const size_t BH = (size_t)B * H;
+  const Range rq = rng(q, BH * Nq * D * 2), rk = rng(k, BH * Nk * D * 2), rv = rng(v, BH * Nk * D * 2);
+  const Range ro = rng(o, BH * Nq * D * 2), rl = rng(lse, BH * Nq * 4);
+  for (Range out : {ro, rl})
+    for (Range in : {rq, rk, rv})
+      if (overlap(out, in)) return FA_ERR_INVALID_ARG;
+  if (overlap(ro, rl)) return FA_ERR_INVALID_ARG;
+
+  unsigned* status = nullptr;
+  rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, D, Nq, (int)BH, 128) || !make_map(&tk, k, D, Nk, (int)BH, 128) ||
+      !make_map(&tv, v, D, Nk, (int)BH, 128))
+    return FA_ERR_LAUNCH;
+  ta11::FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_q_tiles = (Nq + 127) / 128;
+  p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.status = status;
+  return ta11::launch_fwd(D, causal != 0, tq, tk, tv, p, (int)BH, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+           void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal, void* workspace,
+           size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int rc = check_sizes(B, H, Nq, Nk, D, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  const WsLayout w = ws_layout(B, H, Nq, D);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+  const size_t BH = (size_t)B * H;
+  const size_t nq_b = BH * Nq * D * 2, nk_b = BH * Nk * D * 2;
+  const Range ins[] = {rng(q, nq_b), rng(k, nk_b), rng(v, nk_b), rng(o, nq_b), rng(lse, BH * Nq * 4), rng(dO, nq_b)};
+  const Range outs[] = {rng(dq, nq_b), rng(dk, nk_b), rng(dv, nk_b), rng(workspace, w.total)};
+  for (int a = 0; a < 4; ++a) {
+    for (const Range& in : ins)
+      if (overlap(outs[a], in)) return FA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlap(outs[a], outs[b])) return FA_ERR_INVALID_ARG;
+  }
+
+  unsigned* status = nullptr;
+  rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, q, D, Nq, (int)BH, 64) || !make_map(&tk, k, D, Nk, (int)BH, 128) ||
+      !make_map(&tv, v, D, Nk, (int)BH, 128) || !make_map(&tdo, dO, D, Nq, (int)BH, 64))
+    return FA_ERR_LAUNCH;
+
+  char* ws = static_cast<char*>(workspace);
+  float* dq_accum = reinterpret_cast<float*>(ws + w.dq_off);
+  float* dlt = reinterpret_cast<float*>(ws + w.dlt_off);
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+
+  ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, (int)BH, Nq, w.Nq_pad};
+  if (ta11::launch_bwd_prep(D, pp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+
+  ta11::BwdParams bp;
+  bp.dk = dk;
+  bp.dv = dv;
+  bp.dq_accum = dq_accum;
+  bp.lse2 = lse2;
+  bp.dlt = dlt;
+  bp.Nq = Nq;
+  bp.Nk = Nk;
+  bp.Nq_pad = w.Nq_pad;
+  bp.n_k_tiles = (Nk + 127) / 128;
+  bp.scale = scale;
+  bp.scale_log2 = scale * kLog2e;
+  bp.wait_limit_ns = g_wait_limit_ns.load();
+  bp.status = status;
+  cudaEvent_t ev_b = nullptr, ev_e = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_ev_mu);
+    ev_b = g_ev_begin;
+    ev_e = g_ev_end;
+  }
+  if (ev_b && ev_e && cudaEventRecord(ev_b, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (ta11::launch_bwd(D, causal != 0, tq, tk, tv, tdo, bp, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (ev_b && ev_e && cudaEventRecord(ev_e, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+
+  ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale};
+  if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
+int fa_device_status(unsigned* site, int reset) {
+  unsigned* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_LAUNCH;
+  unsigned h[2] = {0, 0};
+  if (cudaMemcpyFromSymbol(h, g_fa_status, sizeof(h)) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (site) *site = h[1];
+  if (reset) {
+    const unsigned z[2] = {0, 0};
+    if (cudaMemcpyToSymbol(g_fa_status, z, sizeof(z)) != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return h[0] == 0 ? FA_OK : (int)h[0];
+}
+
+void fa_set_bwd_main_events(cudaEvent_t begin, cudaEvent_t end) {
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  g_ev_begin = (begin && end) ? begin : nullptr;
+  g_ev_end = (begin && end) ? end : nullptr;
+}
+
+int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream) {
+  unsigned* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  return ta11::launch_wait_probe(limit_ns, status, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // extern "C"
