@@ -51,7 +51,8 @@ typedef enum fa_status {
   FA_ERR_WORKSPACE = 4,     /* bwd workspace null, misaligned or too small */
   FA_ERR_DEVICE = 5,        /* no CUDA device, or the current device is not sm_103 */
   FA_ERR_LAUNCH = 6,        /* a kernel launch or tensor-map encode failed */
-  FA_ERR_TIMEOUT = 7        /* a kernel gave up a bounded wait (see fa_device_status) */
+  FA_ERR_TIMEOUT = 7,       /* a kernel gave up a bounded wait (see fa_device_status) */
+  FA_ERR_SCRATCH_LIMIT = 8  /* fa_bwd_noalloc: problem needs more than its fixed scratch */
 } fa_status;
 
 /*
@@ -117,6 +118,33 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
  * belong to the caller; pass NULL, NULL to stop recording.  Process-wide setting.
  */
 void fa_set_bwd_main_events(cudaEvent_t begin, cudaEvent_t end);
+
+/*
+ * Backward without any device allocation, for callers that cannot call
+ * cudaMalloc or hand over a workspace: for example a process that must not
+ * allocate device memory after start-up (its memory budget is fixed), or a
+ * plug-in whose host framework owns the allocator and passes only input and
+ * output buffers.  The pages have no counterpart of this call; it computes
+ * exactly what fa_bwd computes, with the same arguments minus the workspace.
+ *
+ * Its scratch (dq_accum, Dlt, L*log2(e), laid out as fa_bwd's workspace) is a
+ * fixed 32 MiB array in the library's device memory, which every GPU that
+ * loads the library holds until the process exits.  Problems whose
+ * fa_bwd_workspace_size(...) exceeds 32 MiB are rejected with
+ * FA_ERR_SCRATCH_LIMIT before anything is launched (for D = 128 that is about
+ * B*H*Nq <= 64k query rows).
+ *
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up per device, done with that device current); make that first call
+ * before any stream capture.  All calls share the one array and the kernels
+ * re-initialise what must start at zero, so calls that overlap on the GPU
+ * (different streams, or different threads without ordering) race on it and
+ * must be serialised by the caller.  Allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library routine.
+ */
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal,
+                   cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_strerror_strings(L):
-    for code in range(0, 8):
+    for code in range(0, 9):
         assert len(_lib.strerror(code)) > 3
     assert "unknown" in _lib.strerror(99)
 
@@ -129,3 +129,10 @@ def test_binding_rejects_missing_gpu():
 
 def test_wait_probe_needs_device(L):
     assert L.fa_wait_probe(1000, None) == _lib.FA_ERR_DEVICE
+
+
+def test_noalloc_size_limit_checked_on_host(L):
+    vp = ctypes.c_void_p
+    p = [vp(x) for x in ptrs(9)]
+    assert L.fa_bwd_noalloc(*p, 4, 32, 4096, 4096, 128, 0.088, 1, None) == _lib.FA_ERR_SCRATCH_LIMIT
+    assert L.fa_bwd_noalloc(*p, 2, 3, 100, 77, 64, 0.125, 1, None) == _lib.FA_ERR_DEVICE

@@ -25,9 +25,10 @@ FA_ERR_WORKSPACE = 4
 FA_ERR_DEVICE = 5
 FA_ERR_LAUNCH = 6
 FA_ERR_TIMEOUT = 7
+FA_ERR_SCRATCH_LIMIT = 8
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_device_status",
-            "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events")
+            "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc")
 
 _lib = None
 
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
     L.fa_wait_probe.restype = i
     L.fa_set_bwd_main_events.argtypes = [vp, vp]
     L.fa_set_bwd_main_events.restype = None
+    L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    L.fa_bwd_noalloc.restype = i
     _lib = L
     return L
 
@@ -169,3 +172,19 @@ def fa_set_bwd_main_events(begin=None, end=None) -> None:
     b = begin.cuda_event if begin is not None else 0
     e = end.cuda_event if end is not None else 0
     lib().fa_set_bwd_main_events(b or None, e or None)
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None = None, stream=None) -> None:
+    """C ``fa_bwd_noalloc``: the backward for callers that cannot allocate device
+    memory; its scratch is a fixed 32 MiB array inside the library (see fa.h)."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib().fa_bwd_noalloc(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
+                              _ptr(v, "v", torch.bfloat16), _ptr(o, "o", torch.bfloat16),
+                              _ptr(lse, "lse", torch.float32), _ptr(do, "do", torch.bfloat16),
+                              _ptr(dq, "dq", torch.bfloat16), _ptr(dk, "dk", torch.bfloat16),
+                              _ptr(dv, "dv", torch.bfloat16), B, H, Nq, Nk, D, float(scale),
+                              int(bool(causal)), _stream(stream))
+    _check(rc, "fa_bwd_noalloc")

@@ -149,6 +149,7 @@ const char* fa_strerror(int status) {
     case FA_ERR_DEVICE: return "no usable device: the current CUDA device must be sm_103 (GB300)";
     case FA_ERR_LAUNCH: return "kernel launch or TMA descriptor encoding failed";
     case FA_ERR_TIMEOUT: return "a kernel gave up a bounded wait (device status word)";
+    case FA_ERR_SCRATCH_LIMIT: return "problem needs more than the 32 MiB fixed scratch of fa_bwd_noalloc";
     default: return "unknown status";
   }
 }
@@ -292,3 +293,103 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------
+// fa_bwd_noalloc: the backward with its scratch in a fixed device array, for
+// callers that cannot allocate device memory (see include/fa.h).
+// ------------------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB, held by every device that loads the library
+
+// File-scope device scratch.  In host code this name is only a host-side stand-in:
+// its device address must be obtained with cudaGetSymbolAddress on each device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+  std::once_flag once;
+  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+
+// One-time set-up per device, run with that device current.
+void* noalloc_scratch_for_current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  NoAllocDevice& s = g_noalloc_dev[dev];
+  std::call_once(s.once, [&]() {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    s.scratch = ptr;
+  });
+  return s.scratch;
+}
+
+}  // namespace
+
+extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dO, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int D,
+                              float scale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  int rc = check_sizes(B, H, Nq, Nk, D, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  const WsLayout w = ws_layout(B, H, Nq, D);
+  if (w.total > kNoAllocScratchBytes) return FA_ERR_SCRATCH_LIMIT;
+  const size_t BH = (size_t)B * H;
+  const size_t nq_b = BH * Nq * D * 2, nk_b = BH * Nk * D * 2;
+  const Range ins[] = {rng(q, nq_b), rng(k, nk_b), rng(v, nk_b), rng(o, nq_b), rng(lse, BH * Nq * 4), rng(dO, nq_b)};
+  const Range outs[] = {rng(dq, nq_b), rng(dk, nk_b), rng(dv, nk_b)};
+  for (int a = 0; a < 3; ++a) {
+    for (const Range& in : ins)
+      if (overlap(outs[a], in)) return FA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 3; ++b)
+      if (overlap(outs[a], outs[b])) return FA_ERR_INVALID_ARG;
+  }
+
+  unsigned* status = nullptr;
+  rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  char* ws = static_cast<char*>(noalloc_scratch_for_current_device());
+  if (!ws) return FA_ERR_DEVICE;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, q, D, Nq, (int)BH, 64) || !make_map(&tk, k, D, Nk, (int)BH, 128) ||
+      !make_map(&tv, v, D, Nk, (int)BH, 128) || !make_map(&tdo, dO, D, Nq, (int)BH, 64))
+    return FA_ERR_LAUNCH;
+  float* dq_accum = reinterpret_cast<float*>(ws + w.dq_off);
+  float* dlt = reinterpret_cast<float*>(ws + w.dlt_off);
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+
+  // The preprocess kernel rewrites every scratch word this call reads (it zeroes
+  // dq_accum and fills Dlt and L*log2(e)), so the previous call's contents never leak in.
+  ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, (int)BH, Nq, w.Nq_pad};
+  if (ta11::launch_bwd_prep(D, pp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  ta11::BwdParams bp;
+  bp.dk = dk;
+  bp.dv = dv;
+  bp.dq_accum = dq_accum;
+  bp.lse2 = lse2;
+  bp.dlt = dlt;
+  bp.Nq = Nq;
+  bp.Nk = Nk;
+  bp.Nq_pad = w.Nq_pad;
+  bp.n_k_tiles = (Nk + 127) / 128;
+  bp.scale = scale;
+  bp.scale_log2 = scale * kLog2e;
+  bp.wait_limit_ns = g_wait_limit_ns.load();
+  bp.status = status;
+  if (ta11::launch_bwd(D, causal != 0, tq, tk, tv, tdo, bp, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale};
+  if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  return FA_OK;
+}
