@@ -79,7 +79,7 @@ def test_fwd_validation_codes(L):
     assert fwd_call(L, q, k, v, o, lse, scale=float("nan")) == _lib.FA_ERR_INVALID_ARG
     assert fwd_call(L, q, k, v, o, lse, scale=float("inf")) == _lib.FA_ERR_INVALID_ARG
     assert fwd_call(L, q, k, v, o, lse, scale=-0.1) == _lib.FA_ERR_INVALID_ARG
-    assert fwd_call(L, q, k, v, o, lse, Nq=65536 * 128) == _lib.FA_ERR_INVALID_ARG
+    assert fwd_call(L, q, k, v, o, lse, B=256, H=256) == _lib.FA_ERR_INVALID_ARG  # B*H > 65535
     assert fwd_call(L, q + 8, k, v, o, lse) == _lib.FA_ERR_MISALIGNED
     assert fwd_call(L, q, k, v, o + 2, lse) == _lib.FA_ERR_MISALIGNED
     assert fwd_call(L, q, k, v, o, lse + 2) == _lib.FA_ERR_MISALIGNED

@@ -125,8 +125,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = (int)warp_id(), lane = (int)lane_id();
-  const int bh = blockIdx.x;
-  const int kt = blockIdx.y;  // causal: low key tiles see the most queries, launch them first
+  // Key tiles of one head are adjacent in launch order, so resident CTAs share the
+  // Q, dO and dq_accum of a few heads in L2; causal: low key tiles see the most
+  // queries and go first.
+  const int kt = blockIdx.x;
+  const int bh = blockIdx.y;
   const int k0 = kt * C::BN;
   const int n_qt = (p.Nq + C::BM - 1) / C::BM;
   const int i_start = CAUSAL ? min(k0 / C::BM, n_qt) : 0;
@@ -448,7 +451,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   auto kern = bwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)BH, (unsigned)p.n_k_tiles);
+  dim3 grid((unsigned)p.n_k_tiles, (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }

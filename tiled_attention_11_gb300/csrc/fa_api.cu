@@ -109,8 +109,7 @@ bool valid_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
 // Shared size checks; returns FA_OK or a code.
 int check_sizes(int B, int H, int Nq, int Nk, int D, float scale) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
-  if ((long long)B * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  if ((Nq + 127) / 128 > 65535 || (Nk + 127) / 128 > 65535) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H > 65535) return FA_ERR_INVALID_ARG;  // grid.y
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (!valid_d(D)) return FA_ERR_UNSUPPORTED_D;
   return FA_OK;

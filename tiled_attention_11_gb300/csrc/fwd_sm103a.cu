@@ -96,8 +96,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = (int)warp_id(), lane = (int)lane_id();
-  const int bh = blockIdx.x;
-  const int qt = (int)gridDim.y - 1 - (int)blockIdx.y;  // heaviest (causal) query tiles first
+  // Query tiles of one head are adjacent in launch order, so the CTAs resident at
+  // any moment share the K/V of a few heads in L2; within a head the heaviest
+  // (causal) query tiles go first.
+  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;
+  const int bh = blockIdx.y;
   const int q0 = qt * C::BM;
   const int nk_tiles = (p.Nk + C::BN - 1) / C::BN;
   const int n_kv = CAUSAL ? min(nk_tiles, qt + 1) : nk_tiles;
@@ -331,7 +334,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   auto kern = fwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)BH, (unsigned)p.n_q_tiles);
+  dim3 grid((unsigned)p.n_q_tiles, (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
