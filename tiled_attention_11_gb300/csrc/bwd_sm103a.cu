@@ -16,8 +16,11 @@
 //              dP^T = V dO_i^T           -> TMEM   dS^T = P^T o (dP^T - Dlt)
 //              dV  += P^T dO_i   (A = P^T from TMEM)
 //              dK  += dS^T Q_i   (A = dS^T from TMEM)
-//              dQ_i^T = K^T dS^T (both from shared memory) -> TMEM (double-buffered),
-//            then the compute warps add dQ_i into dq_accum with fp32 red.add.
+//              dQ_i^T = K^T dS^T (both from shared memory) -> TMEM (double-buffered)
+//            Issue order S(i+1) after dV(i) and dP(i+1) after dQ(i) keeps the tensor
+//            core busy while the compute warps work on the previous tile; a dQ
+//            warpgroup moves dQ_i^T from TMEM to shared memory and adds it into
+//            dq_accum with one TMA bulk reduce-add per tile.
 //   convert  dq = bf16(dq_accum * scale).
 #include "fa_kernels.h"
 #include "ptx_sm103a.cuh"
@@ -46,7 +49,9 @@ struct Cfg {
   static constexpr int OFF_DS = OFF_DO + NS * Q_TILE;
   static constexpr int OFF_LSE = OFF_DS + 2 * DS_BYTES;
   static constexpr int OFF_DLT = OFF_LSE + NS * BM * 4;
-  static constexpr int OFF_BAR = OFF_DLT + NS * BM * 4;
+  static constexpr int OFF_STG = OFF_DLT + NS * BM * 4;  // dQ_i staging, fp32 [BM][D]
+  static constexpr int STG_BYTES = BM * D * 4;
+  static constexpr int OFF_BAR = OFF_STG + STG_BYTES;
   // barriers
   static constexpr int B_KV = 0;
   static constexpr int B_QF = 1;             // [NS]
@@ -61,30 +66,27 @@ struct Cfg {
   static constexpr int NBAR = 10 + 2 * NS;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
-  static constexpr int THREADS = 384;
+  // warps 0-3: dQ warpgroup, 4-11: two compute warpgroups, 12: TMA producer, 13: UMMA issuer
+  static constexpr int THREADS = 448;
+  static constexpr int W_PRODUCER = 12, W_MMA = 13;
   // TMEM columns
   static constexpr int T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 256 + D;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, BM, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
   static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, true, true);    // dQ^T (A, B MN-major)
-  static_assert(Q_TILE % 1024 == 0 && KV_TILE % 1024 == 0, "alignment");
+  static_assert(Q_TILE % 1024 == 0 && KV_TILE % 1024 == 0 && OFF_STG % 128 == 0, "alignment");
 };
 
-// K-major operand with `rows` rows (chunk = rows * ROWB bytes), kk-th 16-wide K slice.
+// Byte offset of the kk-th 16-wide K slice of a K-major tile whose CHUNK-wide column
+// blocks are `chunk_bytes` apart.
 template <int D>
-__device__ __forceinline__ uint64_t desc_k(uint32_t tile, uint32_t chunk_bytes, int kk) {
-  using C = Cfg<D>;
-  const int el = kk * 16;
-  return sdesc(tile + (el / C::CHUNK) * chunk_bytes + (el % C::CHUNK) * 2, 16, 8 * C::ROWB, C::LAYOUT);
+__host__ __device__ constexpr uint32_t koff(uint32_t chunk_bytes, int kk) {
+  return (uint32_t)((kk * 16 / Cfg<D>::CHUNK) * chunk_bytes + (kk * 16 % Cfg<D>::CHUNK) * 2);
 }
-
-// MN-major operand stored as rows of D (D contiguous): the K dimension runs over rows.
+// Byte offset of the kk-th slice of 16 rows of an MN-major operand stored as rows of D.
 template <int D>
-__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, uint32_t lbo, int kk) {
-  using C = Cfg<D>;
-  return sdesc(tile + kk * 16 * C::ROWB, lbo, 8 * C::ROWB, C::LAYOUT);
-}
+__host__ __device__ constexpr uint32_t mnoff(int kk) { return (uint32_t)(kk * 16 * Cfg<D>::ROWB); }
 
 // TMEM column of the packed bf16 A operand (P^T or dS^T) for the kk-th 16-query slice:
 // queries 0..31 live in columns [0,16), queries 32..63 in [32,48).
@@ -148,13 +150,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     mbar_init(&bars[C::B_DSF], 256);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[C::B_DQF + b], 1);
-      mbar_init(&bars[C::B_DQE + b], 256);
+      mbar_init(&bars[C::B_DQE + b], 128);
     }
     mbar_init(&bars[C::B_DRAIN], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == C::W_MMA) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == C::W_PRODUCER) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && n_it > 0) {
       tma_prefetch_desc(&tm_q);
@@ -201,54 +203,80 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           mbar_wait(&bars[C::B_QF + it % C::NS], (it / C::NS) & 1, w2, 41);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------------- UMMA issuer
     if (lane == 0) {
-      const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+      // Base descriptors, built once; per-stage / per-slice variants are one add away.
       const uint32_t kt_lbo = (D == 128) ? (uint32_t)C::K_CHUNK_BYTES : 0u;  // K^T as A: M = d padded to 128
-      if (n_it > 0 && mbar_wait(&bars[C::B_KV], 0, wc, 32)) {
-        for (int it = 0; it < n_it; ++it) {
-          const int s = it % C::NS;
-          if (!mbar_wait(&bars[C::B_QF + s], (it / C::NS) & 1, wc, 33)) break;
+      const uint64_t dK = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);       // K, K-major
+      const uint64_t dV = sdesc(sbase + C::OFF_V, 16, 8 * C::ROWB, C::LAYOUT);       // V, K-major
+      const uint64_t dKT = sdesc(sbase + C::OFF_K, kt_lbo, 8 * C::ROWB, C::LAYOUT);  // K^T, MN-major
+      const uint64_t dQk = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);      // Q stage 0, K-major
+      const uint64_t dOk = sdesc(sbase + C::OFF_DO, 16, 8 * C::ROWB, C::LAYOUT);     // dO stage 0, K-major
+      const uint64_t dQm = sdesc(sbase + C::OFF_Q, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // MN-major
+      const uint64_t dOm = sdesc(sbase + C::OFF_DO, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);  // MN-major
+      const uint64_t dS0 = sdesc(sbase + C::OFF_DS, C::DS_BYTES, 1024, 2u);          // dS^T buffer 0, MN-major
+      auto issue_s = [&](int s) {  // S^T = K Q_s^T
+        const uint64_t q = desc_adv(dQk, (uint32_t)(s * C::Q_TILE));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + C::T_S, desc_adv(dK, koff<D>(C::K_CHUNK_BYTES, kk)),
+                  desc_adv(q, koff<D>(C::Q_CHUNK_BYTES, kk)), C::IDESC_S, kk > 0 ? 1u : 0u);
+        umma_commit(&bars[C::B_SF]);
+      };
+      auto issue_dp = [&](int s) {  // dP^T = V dO_s^T
+        const uint64_t o = desc_adv(dOk, (uint32_t)(s * C::Q_TILE));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + C::T_DP, desc_adv(dV, koff<D>(C::K_CHUNK_BYTES, kk)),
+                  desc_adv(o, koff<D>(C::Q_CHUNK_BYTES, kk)), C::IDESC_S, kk > 0 ? 1u : 0u);
+        umma_commit(&bars[C::B_DPF]);
+      };
+      bool ok = n_it > 0 && mbar_wait(&bars[C::B_KV], 0, wc, 32) && mbar_wait(&bars[C::B_QF], 0, wc, 33);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % C::NS;
+        const int s1 = (it + 1) % C::NS;
+        const bool more = it + 1 < n_it;
+        const uint64_t qm = desc_adv(dQm, (uint32_t)(s * C::Q_TILE));
+        const uint64_t om = desc_adv(dOm, (uint32_t)(s * C::Q_TILE));
+        // dV += P^T dO_i once P^T is in TMEM
+        if (!(ok = mbar_wait(&bars[C::B_PF], it & 1, wc, 34))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          umma_ts(tmem + C::T_DV, tmem + C::T_S + a_col(kk), desc_adv(om, mnoff<D>(kk)), C::IDESC_KV,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        // S^T of the next tile overwrites P^T only after dV has read it (in-order UMMA)
+        if (more) {
+          if (!(ok = mbar_wait(&bars[C::B_QF + s1], ((it + 1) / C::NS) & 1, wc, 35))) break;
           tc_fence_after();
-          const uint32_t sQ = sbase + C::OFF_Q + s * C::Q_TILE;
-          const uint32_t sdO = sbase + C::OFF_DO + s * C::Q_TILE;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + C::T_S, desc_k<D>(sK, C::K_CHUNK_BYTES, kk), desc_k<D>(sQ, C::Q_CHUNK_BYTES, kk),
-                    C::IDESC_S, kk > 0 ? 1u : 0u);
-          umma_commit(&bars[C::B_SF]);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + C::T_DP, desc_k<D>(sV, C::K_CHUNK_BYTES, kk), desc_k<D>(sdO, C::Q_CHUNK_BYTES, kk),
-                    C::IDESC_S, kk > 0 ? 1u : 0u);
-          umma_commit(&bars[C::B_DPF]);
-
-          if (!mbar_wait(&bars[C::B_PF], it & 1, wc, 34)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < C::BM / 16; ++kk)
-            umma_ts(tmem + C::T_DV, tmem + C::T_S + a_col(kk), desc_mn<D>(sdO, C::Q_CHUNK_BYTES, kk),
-                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-
-          if (!mbar_wait(&bars[C::B_DSF], it & 1, wc, 35)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < C::BM / 16; ++kk)
-            umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_mn<D>(sQ, C::Q_CHUNK_BYTES, kk),
-                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&bars[C::B_QE + s]);
-
-          const int b = it & 1;
-          if (it >= 2 && !mbar_wait(&bars[C::B_DQE + b], ((it - 2) >> 1) & 1, wc, 36)) break;
-          tc_fence_after();
-          const uint32_t sdS = sbase + C::OFF_DS + b * C::DS_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk)
-            umma_ss(tmem + C::T_DQ + b * C::BM, desc_mn<D>(sK, kt_lbo, kk),
-                    sdesc(sdS + kk * 16 * 128, C::DS_BYTES, 1024, 2u), C::IDESC_DQ, kk > 0 ? 1u : 0u);
-          umma_commit(&bars[C::B_DQF + b]);
+          issue_s(s1);
         }
+        // dK += dS^T Q_i once dS^T is in TMEM (and in shared memory for dQ)
+        if (!(ok = mbar_wait(&bars[C::B_DSF], it & 1, wc, 36))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[C::B_QE + s]);
+        // dQ_i^T = K^T dS^T into the TMEM buffer the dQ warpgroup has drained
+        const int b = it & 1;
+        if (it >= 2 && !(ok = mbar_wait(&bars[C::B_DQE + b], ((it - 2) >> 1) & 1, wc, 37))) break;
+        tc_fence_after();
+        const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          umma_ss(tmem + C::T_DQ + b * C::BM, desc_adv(dKT, mnoff<D>(kk)), desc_adv(ds, (uint32_t)(kk * 16 * 128)),
+                  C::IDESC_DQ, kk > 0 ? 1u : 0u);
+        umma_commit(&bars[C::B_DQF + b]);
+        // dP^T of the next tile overwrites dS^T only after dK has read it
+        if (more) issue_dp(s1);
       }
       umma_commit(&bars[C::B_DRAIN]);
       volatile int no_abort = 0;
@@ -266,23 +294,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const float sl2 = p.scale_log2;
     uint8_t* sds_row_base = smem + C::OFF_DS + row * 128;
     bool ok = true;
-
-    auto readout = [&](int t) -> bool {
-      const int b = t & 1;
-      if (!warp_wait(&bars[C::B_DQF + b], (t >> 1) & 1, wc, 37)) return false;
-      tc_fence_after();
-      uint32_t v[32];
-      tmem_ld32(t_lane + C::T_DQ + b * C::BM + col0, v);
-      tmem_wait_ld(v);
-      if (row < D) {
-        float* dst = p.dq_accum + ((size_t)bh * p.Nq_pad + (size_t)(i_start + t) * C::BM + col0) * D + row;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) red_add_f32(dst + (size_t)c * D, as_f(v[c]));
-      }
-      tc_fence_before();
-      mbar_arrive(&bars[C::B_DQE + b]);
-      return true;
-    };
 
     for (int it = 0; it < n_it && ok; ++it) {
       const int s = it % C::NS;
@@ -332,7 +343,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         dk[c] = pack_bf16(d0, d1);
       }
       tmem_st16(t_lane + C::T_DP + wg * 32, dk);
-      // dS^T row into shared memory (128-byte rows, 128B swizzle) for the dQ^T MMA.
+      // dS^T row into shared memory (128-byte rows, 128B swizzle) for the dQ^T MMA, once the
+      // dQ^T MMA two tiles back has finished reading this buffer.
+      if (it >= 2 && !warp_wait(&bars[C::B_DQF + (it & 1)], ((it - 2) >> 1) & 1, wc, 44)) {
+        ok = false;
+        tmem_wait_st();
+        break;
+      }
       uint8_t* dsrow = sds_row_base + (it & 1) * C::DS_BYTES;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -343,21 +360,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars[C::B_DSF]);
-
-      if (it >= 1 && !readout(it - 1)) {
-        ok = false;
-        break;
-      }
     }
-    if (ok && n_it > 0) ok = readout(n_it - 1);
 
-    // epilogue: WG0 writes dK = scale * acc, WG1 writes dV
+    // epilogue: WG0 writes dK = scale * acc, WG1 writes dV; the last dQ commit covers both
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) + ((size_t)bh * p.Nk + key) * D;
     if (n_it == 0) {
       if (key < p.Nk) {
         for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(dst + d) = make_uint4(0, 0, 0, 0);
       }
-    } else if (ok) {
+    } else if (ok && warp_wait(&bars[C::B_DQF + ((n_it - 1) & 1)], ((n_it - 1) >> 1) & 1, wc, 45)) {
       tc_fence_after();
       const float mul = (wg == 0) ? p.scale : 1.f;
 #pragma unroll
@@ -368,11 +379,46 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (key < p.Nk) store_row_bf16<D>(dst + g * 16, v, mul);
       }
     }
+  } else {
+    // ---------------------------------------------------------------- dQ warpgroup (warps 0-3)
+    const int d = warp * 32 + lane;  // TMEM lane = row d of dQ^T
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    float* stg = reinterpret_cast<float*>(smem + C::OFF_STG);
+    for (int it = 0; it < n_it; ++it) {
+      const int b = it & 1;
+      // the four warps agree before any of them reaches the named barriers below
+      if (!named_bar_and(1, 128, warp_wait(&bars[C::B_DQF + b], (it >> 1) & 1, wc, 46))) break;
+      tc_fence_after();
+      uint32_t v0[32], v1[32];
+      tmem_ld32(t_lane + C::T_DQ + b * C::BM, v0);
+      tmem_ld32(t_lane + C::T_DQ + b * C::BM + 32, v1);
+      tmem_wait_ld(v0);
+      reg_tie(v1);
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_DQE + b]);
+      // the previous bulk reduce must have finished reading the staging buffer
+      if (threadIdx.x == 0) bulk_wait_read_all();
+      named_bar_sync(1, 128);
+      if (d < D) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) stg[c * D + d] = as_f(v0[c]);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) stg[(32 + c) * D + d] = as_f(v1[c]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (threadIdx.x == 0) {
+        float* gdst = p.dq_accum + ((size_t)bh * p.Nq_pad + (size_t)(i_start + it) * C::BM) * D;
+        bulk_reduce_add_f32(gdst, stg, C::STG_BYTES);
+        bulk_commit_group();
+      }
+    }
+    if (threadIdx.x == 0) bulk_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == C::W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }

@@ -8,15 +8,24 @@
 // kept in base 2: with c = scale*log2(e), t = c*S, p = 2^(t - m2) and
 // L = (m2 + log2 l) * ln 2, which is the same softmax.
 //
-// GB300 mapping (one CTA per (batch*head, 128-row query tile), 6 warps):
-//   warp 0     TMA producer: Q once, then K_j / V_j through an NS-stage ring
-//   warp 1     TMEM allocator and UMMA issuer (one thread):
-//                S_j = Q K_j^T  -> TMEM (double-buffered, 128 fp32 columns each)
-//                O  += P_j V_j  -> TMEM (P read from TMEM, aliasing S_j)
-//   warps 2-5  softmax warpgroup, one thread per query row: TMEM -> registers,
-//              mask (diagonal / ragged tiles only), online max / exp2 / sum,
-//              P as bf16 back into TMEM, O rescale by alpha when the max moved,
-//              and the epilogue O / l -> bf16, L.
+// The subtracted maximum is refreshed only when a row's maximum grows by more than
+// TAU = 8 (base 2): softmax is unchanged by the constant it subtracts, and until the
+// refresh every p stays <= 2^8, so l and O_acc are exact in fp32 and P in bf16 keeps
+// its relative precision.  This skips almost every O rescale after the first tiles.
+// O is normalised by the sum of the bf16-rounded weights that P V actually used (lr),
+// so the applied weights sum to one exactly (a one-hot row returns its V row exactly);
+// L uses the unrounded sum l.
+//
+// GB300 mapping: one CTA per (batch*head, pair of 128-row query tiles), 10 warps,
+// the two tiles ping-ponging on the tensor core:
+//   warps 0-3  softmax warpgroup for tile 0 (one thread per query row)
+//   warps 4-7  softmax warpgroup for tile 1
+//   warp 8     TMA producer: Q0, Q1 once, then K_j / V_j through an NS-stage ring
+//   warp 9     TMEM allocator and UMMA issuer (one thread), per key tile j:
+//                O0 += P0_j V_j, S0_{j+1} = Q0 K_{j+1}^T, O1 += P1_j V_j, S1_{j+1} = ...
+//              so the tensor core works on one tile while the other's softmax runs.
+//   TMEM (512 columns): S0 | S1 (128 fp32 each; P as bf16 overwrites the first 64)
+//                       | O0 | O1 (D fp32 each)
 // Every wait is bounded; a timeout records FA_ERR_TIMEOUT in the status word and
 // the CTA drains its in-flight copies and MMAs before freeing TMEM.
 #include "fa_kernels.h"
@@ -27,7 +36,7 @@ namespace fwd {
 
 template <int D>
 struct Cfg {
-  static constexpr int BM = 128;                       // query rows per CTA
+  static constexpr int BM = 128;                       // query rows per tile (2 tiles per CTA)
   static constexpr int BN = 128;                       // keys per tile
   static constexpr int CHUNK = D < 64 ? D : 64;        // elements per swizzled smem row
   static constexpr int NCHUNK = D / CHUNK;
@@ -36,45 +45,41 @@ struct Cfg {
   static constexpr int TILE_BYTES = 128 * D * 2;
   static constexpr int NS = D <= 64 ? 4 : 2;           // K/V ring depth
   static constexpr uint32_t LAYOUT = umma_layout_for_swizzle(ROWB);
-  static constexpr int TMEM_O = 256;
+  static constexpr int TMEM_S = 0;                     // + 128 * tile
+  static constexpr int TMEM_O = 256;                   // + D * tile
   static constexpr int TMEM_COLS = 512;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = TILE_BYTES;
-  static constexpr int OFF_V = TILE_BYTES * (1 + NS);
-  static constexpr int OFF_BAR = TILE_BYTES * (1 + 2 * NS);
-  // barriers: q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], o_ready, drain
+  static constexpr int OFF_Q = 0;                      // 2 tiles
+  static constexpr int OFF_K = 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
+  // barriers: q_full[2], k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
   static constexpr int B_Q = 0;
-  static constexpr int B_KF = 1;
-  static constexpr int B_VF = 1 + NS;
-  static constexpr int B_KVE = 1 + 2 * NS;
-  static constexpr int B_SF = 1 + 3 * NS;
-  static constexpr int B_PF = 3 + 3 * NS;
-  static constexpr int B_O = 5 + 3 * NS;
-  static constexpr int B_DRAIN = 6 + 3 * NS;
-  static constexpr int NBAR = 7 + 3 * NS;
+  static constexpr int B_KF = 2;
+  static constexpr int B_VF = 2 + NS;
+  static constexpr int B_KVE = 2 + 2 * NS;
+  static constexpr int B_SF = 2 + 3 * NS;
+  static constexpr int B_PF = 4 + 3 * NS;
+  static constexpr int B_O = 6 + 3 * NS;
+  static constexpr int B_DRAIN = 8 + 3 * NS;
+  static constexpr int NBAR = 9 + 3 * NS;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // At least ~120 KB so only one CTA (and one 512-column TMEM allocation) fits per SM.
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 320;
+  static constexpr int W_PRODUCER = 8, W_MMA = 9;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
   static_assert(TILE_BYTES % 1024 == 0, "tiles must keep 1024-byte alignment");
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
-// K-major operand (rows of the tile x D contiguous): descriptor for the kk-th 16-wide K slice.
-template <int D>
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
-  using C = Cfg<D>;
-  const int el = kk * 16;
-  const uint32_t start = tile + (el / C::CHUNK) * C::CHUNK_BYTES + (el % C::CHUNK) * 2;
-  return sdesc(start, 16, 8 * C::ROWB, C::LAYOUT);
-}
+constexpr float kTau = 8.0f;  // base-2 growth of a row max that forces a rescale
 
-// MN-major B operand (V: keys x D, D contiguous), kk-th slice of 16 keys.
+// Byte offset of the kk-th 16-wide K slice inside a K-major tile (rows x D, D in
+// CHUNK-wide swizzled column blocks of CHUNK_BYTES each).
 template <int D>
-__device__ __forceinline__ uint64_t desc_v(uint32_t tile, int kk) {
-  using C = Cfg<D>;
-  return sdesc(tile + kk * 16 * C::ROWB, C::CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);
+__host__ __device__ constexpr uint32_t kmajor_off(int kk) {
+  return (uint32_t)((kk * 16 / Cfg<D>::CHUNK) * Cfg<D>::CHUNK_BYTES + (kk * 16 % Cfg<D>::CHUNK) * 2);
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtx& w, uint32_t site) {
@@ -96,33 +101,35 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = (int)warp_id(), lane = (int)lane_id();
-  // Query tiles of one head are adjacent in launch order, so the CTAs resident at
+  // Query-tile pairs of one head are adjacent in launch order, so the CTAs resident at
   // any moment share the K/V of a few heads in L2; within a head the heaviest
-  // (causal) query tiles go first.
-  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;
+  // (causal) pairs go first.
+  const int pair = (int)gridDim.x - 1 - (int)blockIdx.x;
   const int bh = blockIdx.y;
-  const int q0 = qt * C::BM;
+  const int q0 = pair * 2 * C::BM;
   const int nk_tiles = (p.Nk + C::BN - 1) / C::BN;
-  const int n_kv = CAUSAL ? min(nk_tiles, qt + 1) : nk_tiles;
+  // key tiles each query tile visits (causal: up to its diagonal tile)
+  const int n_kv0 = CAUSAL ? min(nk_tiles, 2 * pair + 1) : nk_tiles;
+  const int n_kv1 = CAUSAL ? min(nk_tiles, 2 * pair + 2) : nk_tiles;
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[C::B_Q], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars[C::B_Q + t], 1);
+      mbar_init(&bars[C::B_SF + t], 1);
+      mbar_init(&bars[C::B_PF + t], 128);
+      mbar_init(&bars[C::B_O + t], 1);
+    }
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&bars[C::B_KF + s], 1);
       mbar_init(&bars[C::B_VF + s], 1);
       mbar_init(&bars[C::B_KVE + s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars[C::B_SF + b], 1);
-      mbar_init(&bars[C::B_PF + b], 128);
-    }
-    mbar_init(&bars[C::B_O], 1);
     mbar_init(&bars[C::B_DRAIN], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == C::W_MMA) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -131,17 +138,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == C::W_PRODUCER) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars[C::B_Q], C::TILE_BYTES);
-      for (int c = 0; c < C::NCHUNK; ++c)
-        tma_load_3d(smem + C::OFF_Q + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q], c * C::CHUNK, q0, bh);
+      for (int t = 0; t < 2; ++t) {
+        mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
+                      c * C::CHUNK, q0 + t * C::BM, bh);
+      }
       int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = 0; j < n_kv1; ++j) {
         const int s = j % C::NS;
         if (j >= C::NS && !mbar_wait(&bars[C::B_KVE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
         mbar_arrive_expect_tx(&bars[C::B_KF + s], C::TILE_BYTES);
@@ -156,85 +166,106 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
       if (*abort_flag) {
         // Let every copy already issued land before the CTA can exit.
-        WaitCtx dw{p.wait_limit_ns, p.status, abort_flag};
+        volatile int no_abort = 0;
+        const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
         const int first = issued > C::NS ? issued - C::NS : 0;
         for (int j = first; j < issued; ++j) {
           const int s = j % C::NS;
-          volatile int no_abort = 0;
-          WaitCtx w2{dw.limit_ns, dw.status, &no_abort};
           mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, w2, 20);
           mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, w2, 21);
         }
-        volatile int no_abort = 0;
-        WaitCtx w2{dw.limit_ns, dw.status, &no_abort};
         mbar_wait(&bars[C::B_Q], 0, w2, 22);
+        mbar_wait(&bars[C::B_Q + 1], 0, w2, 22);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------------- UMMA issuer
     if (lane == 0) {
-      const uint32_t sQ = sbase + C::OFF_Q;
-      if (mbar_wait(&bars[C::B_Q], 0, wc, 2)) {
-        for (int j = 0; j <= n_kv; ++j) {
-          if (j < n_kv) {
-            const int s = j % C::NS;
-            if (!mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, wc, 3)) break;
-            tc_fence_after();
-            const uint32_t sK = sbase + C::OFF_K + s * C::TILE_BYTES;
-            const uint32_t dS = tmem + (uint32_t)((j & 1) * 128);
+      // Base descriptors, built once: Q tiles and the K ring K-major, the V ring MN-major.
+      const uint64_t dq0 = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);
+      const uint64_t dk0 = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);
+      const uint64_t dv0 = sdesc(sbase + C::OFF_V, C::CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);
+      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+        const uint64_t dq = desc_adv(dq0, (uint32_t)(t * C::TILE_BYTES));
+        const uint64_t dk = desc_adv(dk0, (uint32_t)((j % C::NS) * C::TILE_BYTES));
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              umma_ss(dS, desc_kmajor<D>(sQ, kk), desc_kmajor<D>(sK, kk), C::IDESC_S, kk > 0 ? 1u : 0u);
-            umma_commit(&bars[C::B_SF + (j & 1)]);
-          }
-          if (j > 0) {
-            const int jj = j - 1, s2 = jj % C::NS;
-            if (!mbar_wait(&bars[C::B_PF + (jj & 1)], (jj >> 1) & 1, wc, 4)) break;
-            if (!mbar_wait(&bars[C::B_VF + s2], (jj / C::NS) & 1, wc, 5)) break;
-            tc_fence_after();
-            const uint32_t sV = sbase + C::OFF_V + s2 * C::TILE_BYTES;
-            const uint32_t aP = tmem + (uint32_t)((jj & 1) * 128);
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + C::TMEM_S + t * 128, desc_adv(dq, kmajor_off<D>(kk)), desc_adv(dk, kmajor_off<D>(kk)),
+                  C::IDESC_S, kk > 0 ? 1u : 0u);
+        umma_commit(&bars[C::B_SF + t]);
+      };
+      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j   (A = P from TMEM)
+        const uint64_t dv = desc_adv(dv0, (uint32_t)((j % C::NS) * C::TILE_BYTES));
 #pragma unroll
-            for (int kk = 0; kk < C::BN / 16; ++kk)
-              umma_ts(tmem + C::TMEM_O, aP + kk * 8, desc_v<D>(sV, kk), C::IDESC_PV,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
-            umma_commit(&bars[C::B_KVE + s2]);
-            umma_commit(&bars[C::B_O]);
-          }
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          umma_ts(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * 128 + kk * 8,
+                  desc_adv(dv, (uint32_t)(kk * 16 * C::ROWB)), C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[C::B_O + t]);
+      };
+      bool ok = mbar_wait(&bars[C::B_Q], 0, wc, 2) && mbar_wait(&bars[C::B_KF], 0, wc, 3);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        if ((ok = mbar_wait(&bars[C::B_Q + 1], 0, wc, 2))) {
+          tc_fence_after();
+          issue_s(1, 0);
         }
+      }
+      for (int j = 0; ok && j < n_kv1; ++j) {
+        const int s = j % C::NS, s1 = (j + 1) % C::NS;
+        if (!(ok = mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
+        const bool next_k = j + 1 < n_kv1;
+        if (next_k && !(ok = mbar_wait(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
+        // tile 0: P0_j -> O0, then S0 of the next key tile over the consumed P0
+        if (j < n_kv0) {
+          if (!(ok = mbar_wait(&bars[C::B_PF], j & 1, wc, 4))) break;
+          tc_fence_after();
+          issue_pv(0, j);
+          if (j + 1 < n_kv0) issue_s(0, j + 1);
+        }
+        // tile 1
+        if (!(ok = mbar_wait(&bars[C::B_PF + 1], j & 1, wc, 4))) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        umma_commit(&bars[C::B_KVE + s]);
+        if (next_k) issue_s(1, j + 1);
       }
       // Every MMA issued so far must complete before TMEM is freed.
       umma_commit(&bars[C::B_DRAIN]);
       volatile int no_abort = 0;
-      WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+      const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
       mbar_wait(&bars[C::B_DRAIN], 0, w2, 23);
     }
   } else {
-    // ---------------------------------------------------------------- softmax warpgroup
-    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    // ---------------------------------------------------------------- softmax warpgroups
+    const int t = warp >> 2;   // which query tile of the pair
+    const int wq = warp & 3;   // TMEM lane quarter this warp may access
     const int row = wq * 32 + lane;
-    const int q_idx = q0 + row;
+    const int qt0 = q0 + t * C::BM;
+    const int q_idx = qt0 + row;
+    const int n_kv = t == 0 ? n_kv0 : n_kv1;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t t_s = t_lane + C::TMEM_S + t * 128;
+    const uint32_t t_o = t_lane + C::TMEM_O + t * D;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, lr = 0.f;  // m: the max subtracted (base 2); l, lr: sums of p, bf16(p)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      if (!warp_wait(&bars[C::B_SF + b], (j >> 1) & 1, wc, 6)) {
+      if (!warp_wait(&bars[C::B_SF + t], j & 1, wc, 6)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t s[4][32];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) tmem_ld32(t_lane + b * 128 + g * 32, s[g]);
+      for (int g = 0; g < 4; ++g) tmem_ld32(t_s + g * 32, s[g]);
       tmem_wait_ld(s[0]);
       reg_tie(s[1]);
       reg_tie(s[2]);
       reg_tie(s[3]);
 
       // Mask keys past Nk and (causal) keys after this row's query index.
-      const bool need_mask = ((j + 1) * C::BN > p.Nk) || (CAUSAL && (j * C::BN + C::BN - 1 > q0));
+      const bool need_mask = ((j + 1) * C::BN > p.Nk) || (CAUSAL && (j * C::BN + C::BN - 1 > qt0));
       if (need_mask) {
         int lim = p.Nk - 1 - j * C::BN;  // last visible column of this tile
         if (CAUSAL) lim = min(lim, q_idx - j * C::BN);
@@ -244,62 +275,68 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           for (int c = 0; c < 32; ++c)
             if (g * 32 + c > lim) s[g][c] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = as_f(s[i >> 1][(i & 1) * 16]);
 #pragma unroll
       for (int g = 0; g < 4; ++g)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) mx = fmaxf(mx, as_f(s[g][c]));
-      const float m_new = fmaxf(m, mx * sl2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m - m_use);
-      float sum = 0.f;
-      uint32_t pk[2][32];
+        for (int c = 0; c < 32; ++c)
+          if ((c & 15) != 0) mx8[g * 2 + (c >> 4)] = fmaxf(mx8[g * 2 + (c >> 4)], as_f(s[g][c]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mx2 = mx * sl2;
+      float alpha = 1.f;
+      if (mx2 > m + kTau) {  // also taken on the first tile, where m = -inf
+        alpha = ex2(m - mx2);
+        m = mx2;
+      }
+      float sum8[8], sumr8[8];
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
+      for (int i = 0; i < 8; ++i) sum8[i] = sumr8[i] = 0.f;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float p0 = ex2(fmaf(as_f(s[g][c]), sl2, -m_use));
-          const float p1 = ex2(fmaf(as_f(s[g][c + 1]), sl2, -m_use));
-          sum += p0 + p1;
-          pk[g >> 1][(g & 1) * 16 + (c >> 1)] = pack_bf16(p0, p1);
+          const float p0 = ex2(fmaf(as_f(s[g][c]), sl2, -m));
+          const float p1 = ex2(fmaf(as_f(s[g][c + 1]), sl2, -m));
+          const uint32_t w = pack_bf16(p0, p1);
+          sum8[g * 2 + (c >> 4)] += p0 + p1;
+          sumr8[g * 2 + (c >> 4)] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+          pk[c >> 1] = w;
         }
-      l = l * alpha + sum;
-      tmem_st32(t_lane + b * 128, pk[0]);
-      tmem_st32(t_lane + b * 128 + 32, pk[1]);
+        tmem_st16(t_s + g * 16, pk);
+      }
+      l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
+      lr = lr * alpha +
+           (((sumr8[0] + sumr8[1]) + (sumr8[2] + sumr8[3])) + ((sumr8[4] + sumr8[5]) + (sumr8[6] + sumr8[7])));
 
-      if (j > 0) {
-        // PV(j-1) must have landed in O before it is rescaled.
-        if (!warp_wait(&bars[C::B_O], (j - 1) & 1, wc, 7)) {
-          ok = false;
-          tmem_wait_st();
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // O holds P V up to tile j-1 (S_t(j) was issued after PV_t(j-1), so it has landed);
+      // rescale the rows whose subtracted max moved.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int g = 0; g < D / 16; ++g) {
-            uint32_t o[16];
-            tmem_ld16(t_lane + C::TMEM_O + g * 16, o);
-            tmem_wait_ld(o);
+        for (int g = 0; g < D / 16; ++g) {
+          uint32_t o[16];
+          tmem_ld16(t_o + g * 16, o);
+          tmem_wait_ld(o);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(as_f(o[c]) * alpha);
-            tmem_st16(t_lane + C::TMEM_O + g * 16, o);
-          }
+          for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(as_f(o[c]) * alpha);
+          tmem_st16(t_o + g * 16, o);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars[C::B_PF + b]);
-      m = m_new;
+      mbar_arrive(&bars[C::B_PF + t]);
     }
-    if (ok && warp_wait(&bars[C::B_O], (n_kv - 1) & 1, wc, 8)) {
+    if (ok && warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8)) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lr;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.Nq + q_idx) * D;
 #pragma unroll
       for (int g = 0; g < D / 16; ++g) {
         uint32_t o[16];
-        tmem_ld16(t_lane + C::TMEM_O + g * 16, o);
+        tmem_ld16(t_o + g * 16, o);
         tmem_wait_ld(o);
         uint4 w0, w1;
         w0.x = pack_bf16(as_f(o[0]) * inv_l, as_f(o[1]) * inv_l);
@@ -321,7 +358,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == C::W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -334,7 +371,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   auto kern = fwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.n_q_tiles, (unsigned)BH);
+  dim3 grid((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
