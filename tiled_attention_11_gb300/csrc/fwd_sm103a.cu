@@ -52,16 +52,19 @@ struct Cfg {
   static constexpr int OFF_K = 2 * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
-  // barriers: q_full[2], k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], o_done[2], drain
+  // barriers: q_full[2], k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2],
+  // o_done[2], drain.  K and V stages are released separately: K_j is dead once both S
+  // MMAs that read it finish, long before P V_j, so its refill starts earlier.
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 2;
   static constexpr int B_VF = 2 + NS;
-  static constexpr int B_KVE = 2 + 2 * NS;
-  static constexpr int B_SF = 2 + 3 * NS;
-  static constexpr int B_PF = 4 + 3 * NS;
-  static constexpr int B_O = 6 + 3 * NS;
-  static constexpr int B_DRAIN = 8 + 3 * NS;
-  static constexpr int NBAR = 9 + 3 * NS;
+  static constexpr int B_KE = 2 + 2 * NS;
+  static constexpr int B_VE = 2 + 3 * NS;
+  static constexpr int B_SF = 2 + 4 * NS;
+  static constexpr int B_PF = 4 + 4 * NS;
+  static constexpr int B_O = 6 + 4 * NS;
+  static constexpr int B_DRAIN = 8 + 4 * NS;
+  static constexpr int NBAR = 9 + 4 * NS;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // At least ~120 KB so only one CTA (and one 512-column TMEM allocation) fits per SM.
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
@@ -123,7 +126,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&bars[C::B_KF + s], 1);
       mbar_init(&bars[C::B_VF + s], 1);
-      mbar_init(&bars[C::B_KVE + s], 1);
+      mbar_init(&bars[C::B_KE + s], 1);
+      mbar_init(&bars[C::B_VE + s], 1);
     }
     mbar_init(&bars[C::B_DRAIN], 1);
     *abort_flag = 0;
@@ -153,11 +157,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       int issued = 0;
       for (int j = 0; j < n_kv1; ++j) {
         const int s = j % C::NS;
-        if (j >= C::NS && !mbar_wait(&bars[C::B_KVE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
+        if (j >= C::NS && !mbar_wait(&bars[C::B_KE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
         mbar_arrive_expect_tx(&bars[C::B_KF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
                       c * C::CHUNK, j * C::BN, bh);
+        if (j >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) {
+          issued = j;  // K_j is in flight; let the drain below wait for it
+          mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, wc, 24);
+          break;
+        }
         mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
@@ -209,6 +218,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if ((ok = mbar_wait(&bars[C::B_Q + 1], 0, wc, 2))) {
           tc_fence_after();
           issue_s(1, 0);
+          umma_commit(&bars[C::B_KE]);
         }
       }
       for (int j = 0; ok && j < n_kv1; ++j) {
@@ -227,8 +237,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (!(ok = mbar_wait(&bars[C::B_PF + 1], j & 1, wc, 4))) break;
         tc_fence_after();
         issue_pv(1, j);
-        umma_commit(&bars[C::B_KVE + s]);
-        if (next_k) issue_s(1, j + 1);
+        umma_commit(&bars[C::B_VE + s]);
+        if (next_k) {
+          issue_s(1, j + 1);
+          umma_commit(&bars[C::B_KE + s1]);
+        }
       }
       // Every MMA issued so far must complete before TMEM is freed.
       umma_commit(&bars[C::B_DRAIN]);
