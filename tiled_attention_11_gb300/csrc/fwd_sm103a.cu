@@ -288,42 +288,51 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           for (int c = 0; c < 32; ++c)
             if (g * 32 + c > lim) s[g][c] = __float_as_uint(-INFINITY);
       }
+      // row max: eight independent chains of 3-input max, then a short tree
       float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = as_f(s[i >> 1][(i & 1) * 16]);
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t* v = &s[i >> 1][(i & 1) * 16];
+        float a = fmax3(as_f(v[0]), as_f(v[1]), as_f(v[2]));
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if ((c & 15) != 0) mx8[g * 2 + (c >> 4)] = fmaxf(mx8[g * 2 + (c >> 4)], as_f(s[g][c]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int e = 3; e < 15; e += 2) a = fmax3(a, as_f(v[e]), as_f(v[e + 1]));
+        mx8[i] = fmaxf(a, as_f(v[15]));
+      }
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       const float mx2 = mx * sl2;
       float alpha = 1.f;
       if (mx2 > m + kTau) {  // also taken on the first tile, where m = -inf
         alpha = ex2(m - mx2);
         m = mx2;
       }
-      float sum8[8], sumr8[8];
+      // p = 2^(S*c - m) two lanes at a time; l and lr accumulate in packed pairs
+      const uint64_t c2 = f2pack(sl2, sl2), nm2 = f2pack(-m, -m);
+      uint64_t l2[4], lr2[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sum8[i] = sumr8[i] = 0.f;
+      for (int i = 0; i < 4; ++i) l2[i] = lr2[i] = 0ull;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float p0 = ex2(fmaf(as_f(s[g][c]), sl2, -m));
-          const float p1 = ex2(fmaf(as_f(s[g][c + 1]), sl2, -m));
+          float x0, x1;
+          f2unpack(ffma2(f2pack(as_f(s[g][c]), as_f(s[g][c + 1])), c2, nm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
           const uint32_t w = pack_bf16(p0, p1);
-          sum8[g * 2 + (c >> 4)] += p0 + p1;
-          sumr8[g * 2 + (c >> 4)] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+          l2[(c >> 1) & 3] = fadd2(l2[(c >> 1) & 3], f2pack(p0, p1));
+          lr2[(c >> 1) & 3] = fadd2(lr2[(c >> 1) & 3], f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
           pk[c >> 1] = w;
         }
         tmem_st16(t_s + g * 16, pk);
       }
-      l = l * alpha + (((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7])));
-      lr = lr * alpha +
-           (((sumr8[0] + sumr8[1]) + (sumr8[2] + sumr8[3])) + ((sumr8[4] + sumr8[5]) + (sumr8[6] + sumr8[7])));
+      float la[8], lb[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f2unpack(l2[i], la[2 * i], la[2 * i + 1]);
+        f2unpack(lr2[i], lb[2 * i], lb[2 * i + 1]);
+      }
+      l = l * alpha + (((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7])));
+      lr = lr * alpha + (((lb[0] + lb[1]) + (lb[2] + lb[3])) + ((lb[4] + lb[5]) + (lb[6] + lb[7])));
 
       // O holds P V up to tile j-1 (S_t(j) was issued after PV_t(j-1), so it has landed);
       // rescale the rows whose subtracted max moved.
