@@ -338,6 +338,58 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ per-workload table
+def run_table(args):
+    """Time fa_fwd and fa_bwd on every workload (median of `--steps` reps after 3
+    warm-ups); shapes whose inputs fit in L2 get an L2 flush (a 256 MB write)
+    before every timed call.  Prints one markdown row per workload."""
+    import torch
+    from tiled_attention_11_gb300 import _lib
+    from tiled_attention_11_gb300 import inputs as I
+
+    dev = torch.device("cuda", 0)
+    _lib.lib()
+    peaks, _ = load_peaks()
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    print("| workload | fwd ms | fwd TFLOP/s | fwd % peak | bwd ms | bwd TFLOP/s | bwd % peak | fwd GB/s (% HBM) | L2 flush |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for p in [I.SMALL] + I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]:
+        q, k, v, do = (t.to(dev) for t in I.draw(p, 0))
+        o = torch.empty_like(q)
+        lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(max(_lib.fa_bwd_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D), 256), dtype=torch.uint8,
+                         device=dev)
+        in_bytes = 2 * p.D * p.B * p.H * (2 * p.Nq + 2 * p.Nk) + 4 * p.B * p.H * p.Nq
+        small = 4 * q.numel() * 2 < (129 << 20)
+        fwd = lambda: _lib.fa_fwd(q, k, v, o, lse, p.causal, p.scale)  # noqa: E731
+        bwd = lambda: _lib.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, p.causal, p.scale, workspace=ws)  # noqa: E731
+        res = []
+        for fn in (fwd, bwd):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(args.steps):
+                if small:
+                    flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            res.append(statistics.median(ts))
+        ff, fb = I.flops_fwd(p), I.flops_bwd(p)
+        tf, tb = ff / res[0] / 1e9, fb / res[1] / 1e9
+        gbs = in_bytes / res[0] / 1e6
+        print(f"| {p.name()} | {res[0]:.4f} | {tf:.1f} | {100 * tf / sustained:.1f}% | {res[1]:.4f} | {tb:.1f} | "
+              f"{100 * tb / sustained:.1f}% | {gbs:.0f} ({100 * gbs / hbm:.1f}%) | {'yes' if small else 'no'} |", flush=True)
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ reference arm (the oracle)
 def run_reference(args):
     from tiled_attention_11_gb300 import inputs as I
@@ -389,9 +441,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--table", action="store_true", help="time every workload, print a markdown table")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.table:
+        run_table(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
