@@ -16,7 +16,7 @@
 //              dP^T = V dO_i^T           -> TMEM   dS^T = P^T o (dP^T - Dlt)
 //              dV  += P^T dO_i   (A = P^T from TMEM)
 //              dK  += dS^T Q_i   (A = dS^T from TMEM)
-//              dQ_i^T = K^T dS^T (both from shared memory) -> TMEM (double-buffered)
+//              dQ_i^T = K^T dS^T (A = K^T kept in TMEM, dS^T from shared memory) -> TMEM
 //            Issue order S(i+1) after dV(i) and dP(i+1) after dQ(i) keeps the tensor
 //            core busy while the compute warps work on the previous tile; a dQ
 //            warpgroup moves dQ_i^T from TMEM to shared memory and adds it into
@@ -60,21 +60,24 @@ struct Cfg {
   static constexpr int B_DPF = 2 + 2 * NS;
   static constexpr int B_PF = 3 + 2 * NS;
   static constexpr int B_DSF = 4 + 2 * NS;
-  static constexpr int B_DQF = 5 + 2 * NS;   // [2]
-  static constexpr int B_DQE = 7 + 2 * NS;   // [2]
-  static constexpr int B_DRAIN = 9 + 2 * NS;
-  static constexpr int NBAR = 10 + 2 * NS;
+  static constexpr int B_DQF = 5 + 2 * NS;   // [2] dQ^T MMA of a step done: its dS^T smem buffer is free
+  static constexpr int B_DQR = 7 + 2 * NS;   // dQ^T accumulator ready for the dQ warpgroup
+  static constexpr int B_DQE = 8 + 2 * NS;   // dQ^T accumulator drained
+  static constexpr int B_KT = 9 + 2 * NS;    // K^T written into TMEM
+  static constexpr int B_DRAIN = 10 + 2 * NS;
+  static constexpr int NBAR = 11 + 2 * NS;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
   // warps 0-3: dQ warpgroup, 4-11: two compute warpgroups, 12: TMA producer, 13: UMMA issuer
   static constexpr int THREADS = 448;
   static constexpr int W_PRODUCER = 12, W_MMA = 13;
   // TMEM columns
-  static constexpr int T_S = 0, T_DP = 64, T_DQ = 128, T_DV = 256, T_DK = 256 + D;
+  // TMEM columns: S^T | dP^T | dQ^T | K^T (bf16 pairs, A operand of dQ^T) | dV | dK
+  static constexpr int T_S = 0, T_DP = 64, T_DQ = 128, T_KT = 192, T_DV = 256, T_DK = 256 + D;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, BM, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
-  static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, true, true);    // dQ^T (A, B MN-major)
+  static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, false, true);   // dQ^T (A = K^T in TMEM, B MN-major)
   static_assert(Q_TILE % 1024 == 0 && KV_TILE % 1024 == 0 && OFF_STG % 128 == 0, "alignment");
 };
 
@@ -148,10 +151,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     mbar_init(&bars[C::B_DPF], 1);
     mbar_init(&bars[C::B_PF], 256);
     mbar_init(&bars[C::B_DSF], 256);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars[C::B_DQF + b], 1);
-      mbar_init(&bars[C::B_DQE + b], 128);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(&bars[C::B_DQF + b], 1);
+    mbar_init(&bars[C::B_DQR], 1);
+    mbar_init(&bars[C::B_DQE], 128);
+    mbar_init(&bars[C::B_KT], 128);
     mbar_init(&bars[C::B_DRAIN], 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -207,10 +210,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     // ---------------------------------------------------------------- UMMA issuer
     if (lane == 0) {
       // Base descriptors, built once; per-stage / per-slice variants are one add away.
-      const uint32_t kt_lbo = (D == 128) ? (uint32_t)C::K_CHUNK_BYTES : 0u;  // K^T as A: M = d padded to 128
       const uint64_t dK = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);       // K, K-major
       const uint64_t dV = sdesc(sbase + C::OFF_V, 16, 8 * C::ROWB, C::LAYOUT);       // V, K-major
-      const uint64_t dKT = sdesc(sbase + C::OFF_K, kt_lbo, 8 * C::ROWB, C::LAYOUT);  // K^T, MN-major
       const uint64_t dQk = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);      // Q stage 0, K-major
       const uint64_t dOk = sdesc(sbase + C::OFF_DO, 16, 8 * C::ROWB, C::LAYOUT);     // dO stage 0, K-major
       const uint64_t dQm = sdesc(sbase + C::OFF_Q, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // MN-major
@@ -265,16 +266,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
                   (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars[C::B_QE + s]);
-        // dQ_i^T = K^T dS^T into the TMEM buffer the dQ warpgroup has drained
+        // dQ_i^T = K^T dS^T (A = K^T from TMEM) once the dQ warpgroup drained the last one
         const int b = it & 1;
-        if (it >= 2 && !(ok = mbar_wait(&bars[C::B_DQE + b], ((it - 2) >> 1) & 1, wc, 37))) break;
+        if (it == 0 && !(ok = mbar_wait(&bars[C::B_KT], 0, wc, 47))) break;
+        if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DQE], (it - 1) & 1, wc, 37))) break;
         tc_fence_after();
         const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ss(tmem + C::T_DQ + b * C::BM, desc_adv(dKT, mnoff<D>(kk)), desc_adv(ds, (uint32_t)(kk * 16 * 128)),
-                  C::IDESC_DQ, kk > 0 ? 1u : 0u);
+          umma_ts(tmem + C::T_DQ, tmem + C::T_KT + kk * 8, desc_adv(ds, (uint32_t)(kk * 16 * 128)), C::IDESC_DQ,
+                  kk > 0 ? 1u : 0u);
         umma_commit(&bars[C::B_DQF + b]);
+        umma_commit(&bars[C::B_DQR]);
         // dP^T of the next tile overwrites dS^T only after dK has read it
         if (more) issue_dp(s1);
       }
@@ -384,18 +387,45 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int d = warp * 32 + lane;  // TMEM lane = row d of dQ^T
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
     float* stg = reinterpret_cast<float*>(smem + C::OFF_STG);
-    for (int it = 0; it < n_it; ++it) {
-      const int b = it & 1;
+    // K^T into TMEM once per CTA: lane d holds K[key][d] for all 128 keys as bf16 pairs
+    // (the A operand of dQ^T = K^T dS^T).  Lanes d >= D (D < 128) hold zeros.
+    bool ok = n_it > 0 && named_bar_and(1, 128, warp_wait(&bars[C::B_KV], 0, wc, 48));
+    if (ok) {
+      const uint8_t* sK = smem + C::OFF_K;
+      const int dc = d < D ? d : 0;
+      const int chunk = dc / C::CHUNK, col = dc % C::CHUNK;
+      const uint8_t* base = sK + chunk * C::K_CHUNK_BYTES + (col % 8) * 2;
+      const int u = col / 8;
+      uint32_t kt[2][32];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        uint32_t pr = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = 2 * c + h;  // key row of the swizzled K-major tile
+          const int phys = u ^ ((r * C::ROWB >> 7) & (C::ROWB / 16 - 1));
+          const uint32_t e = *reinterpret_cast<const uint16_t*>(base + r * C::ROWB + phys * 16);
+          pr |= (d < D ? e : 0u) << (16 * h);
+        }
+        kt[c >> 5][c & 31] = pr;
+      }
+      tmem_st32(t_lane + C::T_KT, kt[0]);
+      tmem_st32(t_lane + C::T_KT + 32, kt[1]);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_KT]);
+    }
+    for (int it = 0; ok && it < n_it; ++it) {
       // the four warps agree before any of them reaches the named barriers below
-      if (!named_bar_and(1, 128, warp_wait(&bars[C::B_DQF + b], (it >> 1) & 1, wc, 46))) break;
+      if (!named_bar_and(1, 128, warp_wait(&bars[C::B_DQR], it & 1, wc, 46))) break;
       tc_fence_after();
       uint32_t v0[32], v1[32];
-      tmem_ld32(t_lane + C::T_DQ + b * C::BM, v0);
-      tmem_ld32(t_lane + C::T_DQ + b * C::BM + 32, v1);
+      tmem_ld32(t_lane + C::T_DQ, v0);
+      tmem_ld32(t_lane + C::T_DQ + 32, v1);
       tmem_wait_ld(v0);
       reg_tie(v1);
       tc_fence_before();
-      mbar_arrive(&bars[C::B_DQE + b]);
+      mbar_arrive(&bars[C::B_DQE]);
       // the previous bulk reduce must have finished reading the staging buffer
       if (threadIdx.x == 0) bulk_wait_read_all();
       named_bar_sync(1, 128);
