@@ -353,9 +353,10 @@ def run_table(args):
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    print("| workload | fwd ms | fwd TFLOP/s | fwd % peak | bwd ms | bwd TFLOP/s | bwd % peak | fwd GB/s (% HBM) | L2 flush |")
-    print("|---|---|---|---|---|---|---|---|---|")
-    for p in [I.SMALL] + I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]:
+    print("| workload | fwd ms | fwd TFLOP/s | fwd % peak | bwd ms | bwd TFLOP/s | bwd % peak | fwd GB/s (% HBM) "
+          "| step ms direct / CUDA graph | L2 flush |")
+    print("|---|---|---|---|---|---|---|---|---|---|")
+    for p in I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]:
         q, k, v, do = (t.to(dev) for t in I.draw(p, 0))
         o = torch.empty_like(q)
         lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
@@ -381,11 +382,30 @@ def run_table(args):
                 torch.cuda.synchronize()
                 ts.append(e0.elapsed_time(e1))
             res.append(statistics.median(ts))
+        # whole step (fwd + bwd) as direct calls and as a CUDA graph replay
+        graph = _lib.StepGraph(q, k, v, o, lse, do, dq, dk, dv, p.causal, p.scale, workspace=ws)
+        steps = []
+        for fn in (lambda: (fwd(), bwd()), graph.launch):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(args.steps):
+                if small:
+                    flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            steps.append(statistics.median(ts))
+        graph.close()
         ff, fb = I.flops_fwd(p), I.flops_bwd(p)
         tf, tb = ff / res[0] / 1e9, fb / res[1] / 1e9
         gbs = in_bytes / res[0] / 1e6
         print(f"| {p.name()} | {res[0]:.4f} | {tf:.1f} | {100 * tf / sustained:.1f}% | {res[1]:.4f} | {tb:.1f} | "
-              f"{100 * tb / sustained:.1f}% | {gbs:.0f} ({100 * gbs / hbm:.1f}%) | {'yes' if small else 'no'} |", flush=True)
+              f"{100 * tb / sustained:.1f}% | {gbs:.0f} ({100 * gbs / hbm:.1f}%) | {steps[0]:.4f} / {steps[1]:.4f} "
+              f"| {'yes' if small else 'no'} |", flush=True)
         del q, k, v, do, o, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()
 

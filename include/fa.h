@@ -120,6 +120,23 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
 void fa_set_bwd_main_events(cudaEvent_t begin, cudaEvent_t end);
 
 /*
+ * CUDA Graph of one forward + backward step ([FA-hist] §3.2 and §5.2: launch overhead
+ * dominates short sequences, and a CUDA Graph removes it).  Captures fa_fwd followed by
+ * fa_bwd for these exact buffers, sizes and flags into an instantiated graph; every
+ * fa_graph_launch replays the four kernels on `stream` reading the buffers' current
+ * contents.  The buffers must stay allocated (and unmoved) for the graph's lifetime.
+ * Arguments are validated exactly as by fa_fwd / fa_bwd; on failure *out is NULL and
+ * nothing is captured.  Capture uses a private stream; the caller's streams are not
+ * touched.  Not thread-safe per handle.
+ */
+typedef struct fa_graph_st* fa_graph;
+int fa_graph_create(const void* q, const void* k, const void* v, void* o, float* lse, const void* dO, void* dq,
+                    void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal,
+                    void* workspace, size_t workspace_bytes, fa_graph* out);
+int fa_graph_launch(fa_graph g, cudaStream_t stream);
+void fa_graph_destroy(fa_graph g);
+
+/*
  * Backward without any device allocation, for callers that cannot call
  * cudaMalloc or hand over a workspace: for example a process that must not
  * allocate device memory after start-up (its memory budget is fixed), or a

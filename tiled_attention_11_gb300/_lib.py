@@ -28,7 +28,8 @@ FA_ERR_TIMEOUT = 7
 FA_ERR_SCRATCH_LIMIT = 8
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_device_status",
-            "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc")
+            "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
+            "fa_graph_create", "fa_graph_launch", "fa_graph_destroy")
 
 _lib = None
 
@@ -67,6 +68,13 @@ def lib() -> ctypes.CDLL:
     L.fa_set_bwd_main_events.restype = None
     L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     L.fa_bwd_noalloc.restype = i
+    L.fa_graph_create.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz,
+                                  ctypes.POINTER(vp)]
+    L.fa_graph_create.restype = i
+    L.fa_graph_launch.argtypes = [vp, vp]
+    L.fa_graph_launch.restype = i
+    L.fa_graph_destroy.argtypes = [vp]
+    L.fa_graph_destroy.restype = None
     _lib = L
     return L
 
@@ -188,3 +196,43 @@ def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float |
                               _ptr(dv, "dv", torch.bfloat16), B, H, Nq, Nk, D, float(scale),
                               int(bool(causal)), _stream(stream))
     _check(rc, "fa_bwd_noalloc")
+
+
+class StepGraph:
+    """One fwd + bwd step captured as a CUDA graph (C ``fa_graph_create``) on fixed
+    tensors; ``launch()`` replays it reading the tensors' current contents.  Keeps
+    references to every tensor so none is freed while the graph exists."""
+
+    def __init__(self, q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None = None, workspace=None):
+        B, H, Nq, D = q.shape
+        Nk = k.shape[2]
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        if workspace is None:
+            workspace = torch.empty(max(fa_bwd_workspace_size(B, H, Nq, Nk, D), 256), dtype=torch.uint8,
+                                    device=q.device)
+        self._keep = (q, k, v, o, lse, do, dq, dk, dv, workspace)
+        h = ctypes.c_void_p(0)
+        rc = lib().fa_graph_create(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
+                                   _ptr(v, "v", torch.bfloat16), _ptr(o, "o", torch.bfloat16),
+                                   _ptr(lse, "lse", torch.float32), _ptr(do, "do", torch.bfloat16),
+                                   _ptr(dq, "dq", torch.bfloat16), _ptr(dk, "dk", torch.bfloat16),
+                                   _ptr(dv, "dv", torch.bfloat16), B, H, Nq, Nk, D, float(scale),
+                                   int(bool(causal)), _ptr(workspace, "workspace", torch.uint8),
+                                   workspace.numel(), ctypes.byref(h))
+        _check(rc, "fa_graph_create")
+        self._h = h
+
+    def launch(self, stream=None) -> None:
+        _check(lib().fa_graph_launch(self._h, _stream(stream)), "fa_graph_launch")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().fa_graph_destroy(self._h)
+            self._h = ctypes.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <new>
 
 #include "fa.h"
 #include "fa_kernels.h"
@@ -292,6 +293,73 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------
+// fa_graph_*: one fwd + bwd step captured into a CUDA graph.
+// ------------------------------------------------------------------------------------
+struct fa_graph_st {
+  cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" int fa_graph_create(const void* q, const void* k, const void* v, void* o, float* lse, const void* dO,
+                               void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale,
+                               int causal, void* workspace, size_t workspace_bytes, fa_graph* out) {
+  if (!out) return FA_ERR_INVALID_ARG;
+  *out = nullptr;
+  unsigned* status = nullptr;
+  int rc = current_device(&status);  // one-time per-device set-up happens outside the capture
+  if (rc != FA_OK) return rc;
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_LAUNCH;
+  }
+  // An uncaptured call first: validates the arguments, loads the kernels and sets their
+  // attributes, so the capture below records launches only.
+  rc = fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, D, scale, causal, s);
+  if (rc == FA_OK)
+    rc = fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, D, scale, causal, workspace, workspace_bytes, s);
+  if (rc == FA_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = FA_ERR_LAUNCH;
+  cudaGraph_t graph = nullptr;
+  if (rc == FA_OK) {
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      rc = FA_ERR_LAUNCH;
+    } else {
+      rc = fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, D, scale, causal, s);
+      if (rc == FA_OK)
+        rc = fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, D, scale, causal, workspace, workspace_bytes, s);
+      if (cudaStreamEndCapture(s, &graph) != cudaSuccess && rc == FA_OK) rc = FA_ERR_LAUNCH;
+    }
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (rc == FA_OK && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) rc = FA_ERR_LAUNCH;
+  if (graph) cudaGraphDestroy(graph);
+  cudaStreamDestroy(s);
+  if (rc != FA_OK) {
+    cudaGetLastError();
+    if (exec) cudaGraphExecDestroy(exec);
+    return rc;
+  }
+  fa_graph g = new (std::nothrow) fa_graph_st;
+  if (!g) {
+    cudaGraphExecDestroy(exec);
+    return FA_ERR_LAUNCH;
+  }
+  g->exec = exec;
+  *out = g;
+  return FA_OK;
+}
+
+extern "C" int fa_graph_launch(fa_graph g, cudaStream_t stream) {
+  if (!g || !g->exec) return FA_ERR_INVALID_ARG;
+  return cudaGraphLaunch(g->exec, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" void fa_graph_destroy(fa_graph g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  delete g;
+}
 
 // ------------------------------------------------------------------------------------
 // fa_bwd_noalloc: the backward with its scratch in a fixed device array, for
