@@ -356,7 +356,7 @@ def run_table(args):
     print("| workload | fwd ms | fwd TFLOP/s | fwd % peak | bwd ms | bwd TFLOP/s | bwd % peak | fwd GB/s (% HBM) "
           "| step ms direct / CUDA graph | L2 flush |")
     print("|---|---|---|---|---|---|---|---|---|---|")
-    for p in I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]:
+    for p in ([] if args.varlen_only else I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]):
         q, k, v, do = (t.to(dev) for t in I.draw(p, 0))
         o = torch.empty_like(q)
         lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
@@ -408,6 +408,49 @@ def run_table(args):
               f"| {'yes' if small else 'no'} |", flush=True)
         del q, k, v, do, o, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()
+    _table_varlen(args, dev, sustained, hbm)
+
+
+def _table_varlen(args, dev, sustained, hbm):
+    """Packed variable-length row: fa_fwd_varlen / fa_bwd_varlen on the document mix."""
+    import torch
+    from tiled_attention_11_gb300 import _lib
+    from tiled_attention_11_gb300 import inputs as I
+
+    w = I.VARLEN_DOCS
+    lens, H, D, causal = w["lens"], w["H"], w["D"], w["causal"]
+    q, k, v, do, cu_q, cu_k = I.draw_varlen(lens, lens, H, D, 0, w["factor"])
+    q, k, v, do, cu_q, cu_k = (t.to(dev) for t in (q, k, v, do, cu_q, cu_k))
+    total, mx = sum(lens), max(lens)
+    scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(_lib.fa_bwd_varlen_workspace_size(len(lens), H, total, mx, D), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    fwd = lambda: _lib.fa_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, mx, mx, causal, scale)  # noqa: E731
+    bwd = lambda: _lib.fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_q, cu_k, mx, mx, causal, scale,  # noqa: E731
+                                     workspace=ws)
+    res = []
+    for fn in (fwd, bwd, lambda: (fwd(), bwd())):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        res.append(statistics.median(ts))
+    ff, fb = I.flops_varlen(lens, lens, H, D, causal), I.flops_varlen(lens, lens, H, D, causal, backward=True)
+    tf, tb = ff / res[0] / 1e9, fb / res[1] / 1e9
+    gbs = (2 * D * H * 4 * total + 4 * H * total) / res[0] / 1e6
+    name = f"varlen docs {len(lens)} seqs, {total} tok (max {mx}) H{H}D{D}{'c' if causal else 'n'}"
+    print(f"| {name} | {res[0]:.4f} | {tf:.1f} | {100 * tf / sustained:.1f}% | {res[1]:.4f} | {tb:.1f} | "
+          f"{100 * tb / sustained:.1f}% | {gbs:.0f} ({100 * gbs / hbm:.1f}%) | {res[2]:.4f} / - | yes |", flush=True)
 
 
 # ------------------------------------------------------------------ reference arm (the oracle)
@@ -462,6 +505,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--table", action="store_true", help="time every workload, print a markdown table")
+    ap.add_argument("--varlen-only", action="store_true", help="with --table: only the packed variable-length row")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.table:

@@ -120,6 +120,31 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
 void fa_set_bwd_main_events(cudaEvent_t begin, cudaEvent_t end);
 
 /*
+ * Variable-length ("ragged") batches ([FA2-impl] §7 names ragged inputs as the next step;
+ * [FA-hist] §2.3 dynamic sequence lengths): B independent sequences packed back to back.
+ *   q, o, dO, dq: [total_q, H, D] bf16;  k, v, dk, dv: [total_k, H, D] bf16 (D innermost)
+ *   lse: [H, total_q] fp32 (natural log)
+ *   cu_seqlens_q / cu_seqlens_k: device int32 [B + 1], non-decreasing, cu[0] = 0,
+ *   cu[B] = total; sequence b owns tokens cu[b] .. cu[b+1]-1 of every head.
+ *   max_seqlen_q / max_seqlen_k: upper bounds of the per-sequence lengths (grid size).
+ * Each sequence is attended on its own (causal: top-left within the sequence). A
+ * sequence with queries but no keys gets O = 0 and L = -inf (and zero gradients).
+ * Offsets are read on the device and clamped to [0, total] and to the maximum lengths,
+ * so inconsistent offsets cannot make a kernel touch memory outside the buffers.
+ * Other conventions (alignment, ownership, asynchrony, errors) as for fa_fwd / fa_bwd.
+ */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int B, int H, int total_q, int total_k, int max_seqlen_q,
+                  int max_seqlen_k, int D, float scale, int causal, cudaStream_t stream);
+/* Workspace bytes for fa_bwd_varlen: H * 64*(ceil(total_q/64) + B) rows of dq_accum (D fp32),
+ * Dlt and L*log2(e), each segment 256-byte aligned (0 if the sizes are invalid). */
+size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int max_seqlen_q, int D);
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                  int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int D, float scale, int causal,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * CUDA Graph of one forward + backward step ([FA-hist] §3.2 and §5.2: launch overhead
  * dominates short sequences, and a CUDA Graph removes it).  Captures fa_fwd followed by
  * fa_bwd for these exact buffers, sizes and flags into an instantiated graph; every

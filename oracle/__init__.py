@@ -16,5 +16,5 @@ closed forms, brute-force scalar loops, PyTorch's fp64 CPU
 ``scaled_dot_product_attention`` and autograd (a library routine for the same
 definition), central finite differences and gradient invariants.
 """
-from .attn_ref import attention_forward, attention_backward, forward_head, backward_head  # noqa: F401
+from .attn_ref import attention_forward, attention_backward, attention_varlen, backward_head, forward_head  # noqa: F401
 from .tiled_ref import tiled_forward_head  # noqa: F401

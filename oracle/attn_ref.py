@@ -188,3 +188,29 @@ def attention_backward(q, k, v, do, scale, causal, row_chunk=1024):
             dq[b, h], dk[b, h], dv[b, h] = backward_head(
                 q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, row_chunk=row_chunk)
     return dq, dk, dv
+
+
+def attention_varlen(q, k, v, do, cu_q, cu_k, scale, causal, backward=True, row_chunk=1024):
+    """Packed variable-length batch: sequence b is tokens cu_q[b]..cu_q[b+1]-1 of q/do
+    ([total_q, H, D]) and cu_k[b]..cu_k[b+1]-1 of k/v ([total_k, H, D]); each (sequence,
+    head) is attended independently (causal: top-left within the sequence).  A sequence
+    with queries but no keys gets O = 0, L = -inf and zero gradients.
+    Returns (o [total_q,H,D], lse [H,total_q], dq, dk, dv) (gradients None if not backward)."""
+    total_q, H, D = q.shape
+    o = np.zeros((total_q, H, v.shape[2]))
+    lse = np.full((H, total_q), -np.inf)
+    dq = np.zeros_like(q) if backward else None
+    dk = np.zeros_like(k) if backward else None
+    dv = np.zeros_like(v) if backward else None
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        if q1 <= q0 or k1 <= k0:
+            continue
+        for h in range(H):
+            oo, ll = forward_head(q[q0:q1, h], k[k0:k1, h], v[k0:k1, h], scale, causal, row_chunk=row_chunk)
+            o[q0:q1, h], lse[h, q0:q1] = oo, ll
+            if backward:
+                gq, gk, gv = backward_head(q[q0:q1, h], k[k0:k1, h], v[k0:k1, h], do[q0:q1, h], scale, causal,
+                                           row_chunk=row_chunk)
+                dq[q0:q1, h], dk[k0:k1, h], dv[k0:k1, h] = gq, gk, gv
+    return o, lse, dq, dk, dv

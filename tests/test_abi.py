@@ -136,3 +136,20 @@ def test_noalloc_size_limit_checked_on_host(L):
     p = [vp(x) for x in ptrs(9)]
     assert L.fa_bwd_noalloc(*p, 4, 32, 4096, 4096, 128, 0.088, 1, None) == _lib.FA_ERR_SCRATCH_LIMIT
     assert L.fa_bwd_noalloc(*p, 2, 3, 100, 77, 64, 0.125, 1, None) == _lib.FA_ERR_DEVICE
+
+
+def test_varlen_validation_codes(L):
+    vp = ctypes.c_void_p
+    q, k, v, o, lse, cq, ck = (vp(x) for x in ptrs(7))
+    call = lambda **kw: L.fa_fwd_varlen(q, k, v, o, lse, kw.get("cq", cq), ck, kw.get("B", 3), 2, 100, 90,  # noqa: E731
+                                        kw.get("mq", 60), 50, kw.get("D", 64), 0.125, 1, None)
+    assert call(cq=vp(0)) == _lib.FA_ERR_INVALID_ARG
+    assert call(B=0) == _lib.FA_ERR_INVALID_ARG
+    assert call(mq=0) == _lib.FA_ERR_INVALID_ARG
+    assert call(D=80) == _lib.FA_ERR_UNSUPPORTED_D
+    assert call(cq=vp(ptrs(1)[0] + 2)) == _lib.FA_ERR_MISALIGNED
+    assert call() == _lib.FA_ERR_DEVICE
+    rows = 64 * ((100 + 63) // 64 + 3)
+    def rnd(x):
+        return (x + 255) // 256 * 256
+    assert L.fa_bwd_varlen_workspace_size(3, 2, 100, 60, 64) == rnd(2 * rows * 64 * 4) + 2 * rnd(2 * rows * 4)

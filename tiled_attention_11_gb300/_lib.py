@@ -29,7 +29,8 @@ FA_ERR_SCRATCH_LIMIT = 8
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_device_status",
             "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
-            "fa_graph_create", "fa_graph_launch", "fa_graph_destroy")
+            "fa_graph_create", "fa_graph_launch", "fa_graph_destroy", "fa_fwd_varlen", "fa_bwd_varlen",
+            "fa_bwd_varlen_workspace_size")
 
 _lib = None
 
@@ -75,6 +76,12 @@ def lib() -> ctypes.CDLL:
     L.fa_graph_launch.restype = i
     L.fa_graph_destroy.argtypes = [vp]
     L.fa_graph_destroy.restype = None
+    L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    L.fa_fwd_varlen.restype = i
+    L.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i, i]
+    L.fa_bwd_varlen_workspace_size.restype = sz
+    L.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
+    L.fa_bwd_varlen.restype = i
     _lib = L
     return L
 
@@ -236,3 +243,48 @@ class StepGraph:
             self.close()
         except Exception:
             pass
+
+
+# ----------------------------------------------------------------------------- varlen
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                  causal: bool, scale: float | None = None, stream=None) -> None:
+    """C ``fa_fwd_varlen``: packed [total, H, D] bf16 tensors, lse [H, total_q] fp32,
+    cu_seqlens int32 CUDA tensors of B + 1 offsets."""
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib().fa_fwd_varlen(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
+                             _ptr(v, "v", torch.bfloat16), _ptr(o, "o", torch.bfloat16),
+                             _ptr(lse, "lse", torch.float32), _ptr(cu_seqlens_q, "cu_seqlens_q", torch.int32),
+                             _ptr(cu_seqlens_k, "cu_seqlens_k", torch.int32), B, H, total_q, total_k,
+                             int(max_seqlen_q), int(max_seqlen_k), D, float(scale), int(bool(causal)),
+                             _stream(stream))
+    _check(rc, "fa_fwd_varlen")
+
+
+def fa_bwd_varlen_workspace_size(B: int, H: int, total_q: int, max_seqlen_q: int, D: int) -> int:
+    return int(lib().fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_q, D))
+
+
+def fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, causal: bool, scale: float | None = None, workspace=None, stream=None) -> None:
+    """C ``fa_bwd_varlen``; allocates the workspace with torch when none is given."""
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    B = cu_seqlens_q.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if workspace is None:
+        workspace = torch.empty(max(fa_bwd_varlen_workspace_size(B, H, total_q, max_seqlen_q, D), 256),
+                                dtype=torch.uint8, device=q.device)
+    rc = lib().fa_bwd_varlen(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
+                             _ptr(v, "v", torch.bfloat16), _ptr(o, "o", torch.bfloat16),
+                             _ptr(lse, "lse", torch.float32), _ptr(do, "do", torch.bfloat16),
+                             _ptr(dq, "dq", torch.bfloat16), _ptr(dk, "dk", torch.bfloat16),
+                             _ptr(dv, "dv", torch.bfloat16), _ptr(cu_seqlens_q, "cu_seqlens_q", torch.int32),
+                             _ptr(cu_seqlens_k, "cu_seqlens_k", torch.int32), B, H, total_q, total_k,
+                             int(max_seqlen_q), int(max_seqlen_k), D, float(scale), int(bool(causal)),
+                             _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(rc, "fa_bwd_varlen")

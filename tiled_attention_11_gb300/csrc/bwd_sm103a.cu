@@ -116,7 +116,7 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   reinterpret_cast<uint4*>(dst)[1] = w1;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -136,7 +136,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   const int kt = blockIdx.x;
   const int bh = blockIdx.y;
   const int k0 = kt * C::BN;
-  const int n_qt = (p.Nq + C::BM - 1) / C::BM;
+  const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, bh);
+  if (VARLEN && k0 >= sv.Nk) return;  // this sequence has fewer keys: nothing to do
+  // TMA coordinates (dense maps [B*H][N][D]: y = row, z = bh; packed [total][H][D]: y = head,
+  // z = token) and the first workspace row of this sequence
+  const int qz_b = VARLEN ? sv.q_tok : bh, kz_b = VARLEN ? sv.k_tok : bh;
+  auto ty = [&](int r) { return VARLEN ? sv.h : r; };
+  auto tzq = [&](int r) { return VARLEN ? qz_b + r : qz_b; };
+  auto tzk = [&](int r) { return VARLEN ? kz_b + r : kz_b; };
+  const long long wrow0 = ws_row0(VARLEN, bh, p.Nq_pad, sv);
+  const int n_qt = (sv.Nq + C::BM - 1) / C::BM;
   const int i_start = CAUSAL ? min(k0 / C::BM, n_qt) : 0;
   const int n_it = n_qt - i_start;
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
@@ -177,8 +186,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(&bars[C::B_KV], 2 * C::KV_TILE);
       for (int c = 0; c < C::NCHUNK; ++c) {
-        tma_load_3d(smem + C::OFF_K + c * C::K_CHUNK_BYTES, &tm_k, &bars[C::B_KV], c * C::CHUNK, k0, bh);
-        tma_load_3d(smem + C::OFF_V + c * C::K_CHUNK_BYTES, &tm_v, &bars[C::B_KV], c * C::CHUNK, k0, bh);
+        tma_load_3d(smem + C::OFF_K + c * C::K_CHUNK_BYTES, &tm_k, &bars[C::B_KV], c * C::CHUNK, ty(k0), tzk(k0));
+        tma_load_3d(smem + C::OFF_V + c * C::K_CHUNK_BYTES, &tm_v, &bars[C::B_KV], c * C::CHUNK, ty(k0), tzk(k0));
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
@@ -188,11 +197,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars[C::B_QF + s], 2 * C::Q_TILE + 2 * C::BM * 4);
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_load_3d(smem + C::OFF_Q + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_q, &bars[C::B_QF + s],
-                      c * C::CHUNK, i * C::BM, bh);
+                      c * C::CHUNK, ty(i * C::BM), tzq(i * C::BM));
           tma_load_3d(smem + C::OFF_DO + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_do, &bars[C::B_QF + s],
-                      c * C::CHUNK, i * C::BM, bh);
+                      c * C::CHUNK, ty(i * C::BM), tzq(i * C::BM));
         }
-        const size_t roff = (size_t)bh * p.Nq_pad + (size_t)i * C::BM;
+        const size_t roff = (size_t)wrow0 + (size_t)i * C::BM;
         bulk_load(smem + C::OFF_LSE + s * C::BM * 4, p.lse2 + roff, C::BM * 4, &bars[C::B_QF + s]);
         bulk_load(smem + C::OFF_DLT + s * C::BM * 4, p.dlt + roff, C::BM * 4, &bars[C::B_QF + s]);
         issued = it + 1;
@@ -306,19 +315,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(t_lane + C::T_S + col0, sv);
-      tmem_wait_ld(sv);
+      uint32_t sreg[32];
+      tmem_ld32(t_lane + C::T_S + col0, sreg);
+      tmem_wait_ld(sreg);
       const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * C::BM * 4) + col0;
       const float* dlt = reinterpret_cast<const float*>(smem + C::OFF_DLT + s * C::BM * 4) + col0;
-      const bool need_mask = (k0 + C::BN > p.Nk) || (CAUSAL && (k0 + C::BN - 1 > i * C::BM + col0));
+      const bool need_mask = (k0 + C::BN > sv.Nk) || (CAUSAL && (k0 + C::BN - 1 > i * C::BM + col0));
       int lim = 1 << 30;  // columns c with q = i*64+col0+c < key are masked (causal)
       if (CAUSAL) lim = key - (i * C::BM + col0);
-      const bool key_valid = key < p.Nk;
+      const bool key_valid = key < sv.Nk;
       float pv[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        float x = ex2(fmaf(as_f(sv[c]), sl2, -lse2[c]));
+        float x = ex2(fmaf(as_f(sreg[c]), sl2, -lse2[c]));
         if (need_mask && (!key_valid || (CAUSAL && c < lim))) x = 0.f;
         pv[c] = x;
       }
@@ -366,9 +375,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     }
 
     // epilogue: WG0 writes dK = scale * acc, WG1 writes dV; the last dQ commit covers both
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) + ((size_t)bh * p.Nk + key) * D;
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) +
+                         (VARLEN ? ((size_t)(sv.k_tok + key) * p.va.H + sv.h) * D : ((size_t)bh * sv.Nk + key) * D);
     if (n_it == 0) {
-      if (key < p.Nk) {
+      if (key < sv.Nk) {
         for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(dst + d) = make_uint4(0, 0, 0, 0);
       }
     } else if (ok && warp_wait(&bars[C::B_DQF + ((n_it - 1) & 1)], ((n_it - 1) >> 1) & 1, wc, 45)) {
@@ -379,7 +389,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         uint32_t v[16];
         tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + g * 16, v);
         tmem_wait_ld(v);
-        if (key < p.Nk) store_row_bf16<D>(dst + g * 16, v, mul);
+        if (key < sv.Nk) store_row_bf16<D>(dst + g * 16, v, mul);
       }
     }
   } else {
@@ -438,7 +448,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (threadIdx.x == 0) {
-        float* gdst = p.dq_accum + ((size_t)bh * p.Nq_pad + (size_t)(i_start + it) * C::BM) * D;
+        float* gdst = p.dq_accum + ((size_t)wrow0 + (size_t)(i_start + it) * C::BM) * D;
         bulk_reduce_add_f32(gdst, stg, C::STG_BYTES);
         bulk_commit_group();
       }
@@ -455,76 +465,85 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 }
 
 // ------------------------------------------------------------------------------------
-// prep: Dlt = rowsum(dO o O), lse2 = L * log2(e) (+inf past Nq), dq_accum = 0
+// prep: Dlt = rowsum(dO o O), lse2 = L * log2(e) (+inf past Nq), dq_accum = 0, for the
+// 64-row-padded workspace rows of one (sequence, head) per blockIdx.y.
 // ------------------------------------------------------------------------------------
 template <int D>
+struct RowCfg {
+  static constexpr int TPR = D / 8;          // threads per row, 8 bf16 each
+  static constexpr int ROWS = 256 / TPR;     // rows per 256-thread block
+};
+
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
-  constexpr int TPR = D / 8;  // threads per row, 8 bf16 each
-  const long long rows = (long long)p.BH * p.Nq_pad;
-  const long long total = rows * TPR;
+  constexpr int TPR = RowCfg<D>::TPR;
+  const int bh = blockIdx.y;
+  const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nq, bh);
+  const int rows = VARLEN ? (sv.Nq + 63) / 64 * 64 : p.Nq_pad;  // padded rows of this sequence
+  const long long row0 = ws_row0(VARLEN, bh, p.Nq_pad, sv);
+  const int r = blockIdx.x * RowCfg<D>::ROWS + threadIdx.x / TPR;
   const int part = threadIdx.x % TPR;
-  for (long long base = (long long)blockIdx.x * blockDim.x; base < total; base += (long long)gridDim.x * blockDim.x) {
-    const long long gid = base + threadIdx.x;
-    const bool active = gid < total;
-    const long long r = gid / TPR;
-    const int bh = (int)(r / p.Nq_pad), q = (int)(r % p.Nq_pad);
-    float acc = 0.f;
-    if (active && q < p.Nq) {
-      const size_t off = ((size_t)bh * p.Nq + q) * D + part * 8;
-      const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.o) + off);
-      const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dout) + off);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  const bool active = r < rows;
+  const bool valid = active && r < sv.Nq;
+  const size_t tok = VARLEN ? ((size_t)(sv.q_tok + r) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + r);
+  float acc = 0.f;
+  if (valid) {
+    const size_t off = tok * D + part * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.o) + off);
+    const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dout) + off);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 fa = __bfloat1622float2(a2[t]);
-        const float2 fb = __bfloat1622float2(b2[t]);
-        acc = fmaf(fa.x, fb.x, acc);
-        acc = fmaf(fa.y, fb.y, acc);
-      }
+    for (int t = 0; t < 4; ++t) {
+      const float2 fa = __bfloat1622float2(a2[t]);
+      const float2 fb = __bfloat1622float2(b2[t]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
     }
+  }
 #pragma unroll
-    for (int w = TPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (active) {
-      float4* z = reinterpret_cast<float4*>(p.dq_accum + (size_t)r * D + part * 8);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (part == 0) {
-        p.dlt[r] = acc;
-        p.lse2[r] = (q < p.Nq) ? p.lse[(size_t)bh * p.Nq + q] * 1.4426950408889634f : INFINITY;
-      }
+  for (int w = TPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+  if (active) {
+    const size_t wr = (size_t)(row0 + r);
+    float4* z = reinterpret_cast<float4*>(p.dq_accum + wr * D + part * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (part == 0) {
+      p.dlt[wr] = acc;
+      const size_t li = VARLEN ? (size_t)sv.h * p.va.total_q + sv.q_tok + r : (size_t)bh * sv.Nq + r;
+      p.lse2[wr] = valid ? p.lse[li] * 1.4426950408889634f : INFINITY;
     }
   }
 }
 
 // ------------------------------------------------------------------------------------
-// convert: dq = bf16(dq_accum * scale), rows < Nq only
+// convert: dq = bf16(dq_accum * scale), rows < Nq of one (sequence, head) per blockIdx.y
 // ------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) convert_kernel(const ConvParams p) {
-  const long long nvec = (long long)p.BH * p.Nq * (D / 8);
-  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
-       v += (long long)gridDim.x * blockDim.x) {
-    const long long e = v * 8;
-    const long long row = e / D;  // bh*Nq + q
-    const int d = (int)(e % D);
-    const int bh = (int)(row / p.Nq), q = (int)(row % p.Nq);
-    const float4* src = reinterpret_cast<const float4*>(p.dq_accum + ((size_t)bh * p.Nq_pad + q) * D + d);
-    const float4 a = src[0], b = src[1];
-    uint4 w;
-    w.x = pack_bf16(a.x * p.scale, a.y * p.scale);
-    w.y = pack_bf16(a.z * p.scale, a.w * p.scale);
-    w.z = pack_bf16(b.x * p.scale, b.y * p.scale);
-    w.w = pack_bf16(b.z * p.scale, b.w * p.scale);
-    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + e) = w;
-  }
+  constexpr int TPR = RowCfg<D>::TPR;
+  const int bh = blockIdx.y;
+  const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nq, bh);
+  const int r = blockIdx.x * RowCfg<D>::ROWS + threadIdx.x / TPR;
+  if (r >= sv.Nq) return;
+  const int d = (threadIdx.x % TPR) * 8;
+  const long long row0 = ws_row0(VARLEN, bh, p.Nq_pad, sv);
+  const float4* src = reinterpret_cast<const float4*>(p.dq_accum + (size_t)(row0 + r) * D + d);
+  const float4 a = src[0], b = src[1];
+  uint4 w;
+  w.x = pack_bf16(a.x * p.scale, a.y * p.scale);
+  w.y = pack_bf16(a.z * p.scale, a.w * p.scale);
+  w.z = pack_bf16(b.x * p.scale, b.y * p.scale);
+  w.w = pack_bf16(b.z * p.scale, b.w * p.scale);
+  const size_t tok = VARLEN ? ((size_t)(sv.q_tok + r) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + r);
+  *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + tok * D + d) = w;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                      const BwdParams& p, int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = bwd_kernel<D, CAUSAL>;
+  auto kern = bwd_kernel<D, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.n_k_tiles, (unsigned)BH);
@@ -532,25 +551,20 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   return cudaGetLastError();
 }
 
-static int grid_for(long long work_items, int threads) {
-  long long b = (work_items + threads - 1) / threads;
-  const long long cap = 152LL * 16;  // enough resident blocks to saturate HBM on 152 SMs
-  if (b > cap) b = cap;
-  if (b < 1) b = 1;
-  return (int)b;
-}
-
 template <int D>
 cudaError_t prep_t(const PrepParams& p, cudaStream_t st) {
-  const long long total = (long long)p.BH * p.Nq_pad * (D / 8);
-  prep_kernel<D><<<grid_for(total, 256), 256, 0, st>>>(p);
+  const int rows = p.va.cu_q ? (p.Nq + 63) / 64 * 64 : p.Nq_pad;  // varlen: padded maximum length
+  dim3 grid((unsigned)((rows + RowCfg<D>::ROWS - 1) / RowCfg<D>::ROWS), (unsigned)p.BH);
+  if (p.va.cu_q) prep_kernel<D, true><<<grid, 256, 0, st>>>(p);
+  else prep_kernel<D, false><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t conv_t(const ConvParams& p, cudaStream_t st) {
-  const long long total = (long long)p.BH * p.Nq * (D / 8);
-  convert_kernel<D><<<grid_for(total, 256), 256, 0, st>>>(p);
+  dim3 grid((unsigned)((p.Nq + RowCfg<D>::ROWS - 1) / RowCfg<D>::ROWS), (unsigned)p.BH);
+  if (p.va.cu_q) convert_kernel<D, true><<<grid, 256, 0, st>>>(p);
+  else convert_kernel<D, false><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -567,8 +581,12 @@ cudaError_t conv_t(const ConvParams& p, cudaStream_t st) {
 
 cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int BH, cudaStream_t st) {
-  TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true>(tq, tk, tv, tdo, p, BH, st)
-                           : bwd::launch_t<DD, false>(tq, tk, tv, tdo, p, BH, st)))
+  if (p.va.cu_q) {
+    TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true, true>(tq, tk, tv, tdo, p, BH, st)
+                             : bwd::launch_t<DD, false, true>(tq, tk, tv, tdo, p, BH, st)))
+  }
+  TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true, false>(tq, tk, tv, tdo, p, BH, st)
+                           : bwd::launch_t<DD, false, false>(tq, tk, tv, tdo, p, BH, st)))
 }
 
 cudaError_t launch_bwd_prep(int D, const PrepParams& p, cudaStream_t st) {

@@ -94,6 +94,24 @@ bool make_map(CUtensorMap* m, const void* base, int D, int N, int BH, int box_ro
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor map over a packed [total][H][D] tensor: box {chunk, 1, box_rows}
+// (rows of one head) lands in shared memory exactly like the dense box.
+bool make_map_packed(CUtensorMap* m, const void* base, int D, int H, int total, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int chunk = D < 64 ? D : 64;
+  const CUtensorMapSwizzle sw = chunk == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : chunk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)chunk, 1, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct Range {
@@ -131,6 +149,27 @@ WsLayout ws_layout(int B, int H, int Nq, int D) {
   w.lse2_off = w.dlt_off + round256(rows * 4);
   w.total = w.lse2_off + round256(rows * 4);
   return w;
+}
+
+// Varlen workspace: per head 64*(ceil(total_q/64) + B) rows; sequence b starts at row
+// 64*(ceil(cu_q[b]/64) + b) of its head (64-row aligned, never overlapping).
+WsLayout ws_layout_varlen(int B, int H, int total_q, int D) {
+  WsLayout w;
+  w.Nq_pad = 64 * ((total_q + 63) / 64 + B);
+  const size_t rows = (size_t)H * w.Nq_pad;
+  w.dq_off = 0;
+  w.dlt_off = round256(rows * D * 4);
+  w.lse2_off = w.dlt_off + round256(rows * 4);
+  w.total = w.lse2_off + round256(rows * 4);
+  return w;
+}
+
+int check_varlen(int B, int H, int total_q, int total_k, int max_q, int max_k, int D, float scale) {
+  if (B < 1 || H < 1 || total_q < 1 || total_k < 1 || max_q < 1 || max_k < 1) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H > 65535) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!valid_d(D)) return FA_ERR_UNSUPPORTED_D;
+  return FA_OK;
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -184,7 +223,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (!make_map(&tq, q, D, Nq, (int)BH, 128) || !make_map(&tk, k, D, Nk, (int)BH, 128) ||
       !make_map(&tv, v, D, Nk, (int)BH, 128))
     return FA_ERR_LAUNCH;
-  ta11::FwdParams p;
+  ta11::FwdParams p{};
   p.o = o;
   p.lse = lse;
   p.Nq = Nq;
@@ -235,7 +274,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, (int)BH, Nq, w.Nq_pad};
   if (ta11::launch_bwd_prep(D, pp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
 
-  ta11::BwdParams bp;
+  ta11::BwdParams bp{};
   bp.dk = dk;
   bp.dv = dv;
   bp.dq_accum = dq_accum;
@@ -441,7 +480,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   // dq_accum and fills Dlt and L*log2(e)), so the previous call's contents never leak in.
   ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, (int)BH, Nq, w.Nq_pad};
   if (ta11::launch_bwd_prep(D, pp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
-  ta11::BwdParams bp;
+  ta11::BwdParams bp{};
   bp.dk = dk;
   bp.dv = dv;
   bp.dq_accum = dq_accum;
@@ -457,6 +496,110 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   bp.status = status;
   if (ta11::launch_bwd(D, causal != 0, tq, tk, tv, tdo, bp, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale};
+  if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
+// ------------------------------------------------------------------------------------
+// Variable-length batches: packed [total, H, D] tensors, sequences cu[b] .. cu[b+1].
+// ------------------------------------------------------------------------------------
+extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                             const int* cu_seqlens_k, int B, int H, int total_q, int total_k, int max_seqlen_q,
+                             int max_seqlen_k, int D, float scale, int causal, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  int rc = check_varlen(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, D, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+    return FA_ERR_MISALIGNED;
+  const size_t tq_b = (size_t)total_q * H * D * 2, tk_b = (size_t)total_k * H * D * 2;
+  const Range ins[] = {rng(q, tq_b), rng(k, tk_b), rng(v, tk_b), rng(cu_seqlens_q, (size_t)(B + 1) * 4),
+                       rng(cu_seqlens_k, (size_t)(B + 1) * 4)};
+  const Range ro = rng(o, tq_b), rl = rng(lse, (size_t)H * total_q * 4);
+  for (const Range& in : ins)
+    if (overlap(ro, in) || overlap(rl, in)) return FA_ERR_INVALID_ARG;
+  if (overlap(ro, rl)) return FA_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_packed(&tq, q, D, H, total_q, 128) || !make_map_packed(&tk, k, D, H, total_k, 128) ||
+      !make_map_packed(&tv, v, D, H, total_k, 128))
+    return FA_ERR_LAUNCH;
+  ta11::FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.Nq = max_seqlen_q;
+  p.Nk = max_seqlen_k;
+  p.n_q_tiles = (max_seqlen_q + 127) / 128;
+  p.scale_log2 = scale * kLog2e;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.status = status;
+  p.va = ta11::VarlenArgs{cu_seqlens_q, cu_seqlens_k, H, total_q, total_k};
+  return ta11::launch_fwd(D, causal != 0, tq, tk, tv, p, B * H, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int max_seqlen_q, int D) {
+  if (check_varlen(B, H, total_q, 1, max_seqlen_q, 1, D, 1.f) != FA_OK) return 0;
+  return ws_layout_varlen(B, H, total_q, D).total;
+}
+
+extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dO, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                             const int* cu_seqlens_k, int B, int H, int total_q, int total_k, int max_seqlen_q,
+                             int max_seqlen_k, int D, float scale, int causal, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !cu_seqlens_q || !cu_seqlens_k)
+    return FA_ERR_INVALID_ARG;
+  int rc = check_varlen(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, D, scale);
+  if (rc != FA_OK) return rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_k, 4))
+    return FA_ERR_MISALIGNED;
+  const WsLayout w = ws_layout_varlen(B, H, total_q, D);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+  const size_t tq_b = (size_t)total_q * H * D * 2, tk_b = (size_t)total_k * H * D * 2;
+  const Range ins[] = {rng(q, tq_b), rng(k, tk_b), rng(v, tk_b), rng(o, tq_b), rng(lse, (size_t)H * total_q * 4),
+                       rng(dO, tq_b), rng(cu_seqlens_q, (size_t)(B + 1) * 4), rng(cu_seqlens_k, (size_t)(B + 1) * 4)};
+  const Range outs[] = {rng(dq, tq_b), rng(dk, tk_b), rng(dv, tk_b), rng(workspace, w.total)};
+  for (int a = 0; a < 4; ++a) {
+    for (const Range& in : ins)
+      if (overlap(outs[a], in)) return FA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlap(outs[a], outs[b])) return FA_ERR_INVALID_ARG;
+  }
+  unsigned* status = nullptr;
+  rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map_packed(&tq, q, D, H, total_q, 64) || !make_map_packed(&tk, k, D, H, total_k, 128) ||
+      !make_map_packed(&tv, v, D, H, total_k, 128) || !make_map_packed(&tdo, dO, D, H, total_q, 64))
+    return FA_ERR_LAUNCH;
+  char* ws = static_cast<char*>(workspace);
+  float* dq_accum = reinterpret_cast<float*>(ws + w.dq_off);
+  float* dlt = reinterpret_cast<float*>(ws + w.dlt_off);
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+  const ta11::VarlenArgs va{cu_seqlens_q, cu_seqlens_k, H, total_q, total_k};
+  ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, B * H, max_seqlen_q, w.Nq_pad, va};
+  if (ta11::launch_bwd_prep(D, pp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  ta11::BwdParams bp{};
+  bp.dk = dk;
+  bp.dv = dv;
+  bp.dq_accum = dq_accum;
+  bp.lse2 = lse2;
+  bp.dlt = dlt;
+  bp.Nq = max_seqlen_q;
+  bp.Nk = max_seqlen_k;
+  bp.Nq_pad = w.Nq_pad;
+  bp.n_k_tiles = (max_seqlen_k + 127) / 128;
+  bp.scale = scale;
+  bp.scale_log2 = scale * kLog2e;
+  bp.wait_limit_ns = g_wait_limit_ns.load();
+  bp.status = status;
+  bp.va = va;
+  if (ta11::launch_bwd(D, causal != 0, tq, tk, tv, tdo, bp, B * H, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  ta11::ConvParams cp{dq_accum, dq, B * H, max_seqlen_q, w.Nq_pad, scale, va};
   if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;
 }

@@ -7,48 +7,102 @@
 
 namespace ta11 {
 
+// Variable-length batches: packed [total, H, D] tensors with per-sequence offsets
+// cu[b] .. cu[b+1] (device int32, B+1 entries).  In that mode Nq / Nk hold the maximum
+// sequence lengths, and every CTA derives its own sequence bounds (clamped to the packed
+// extents, so inconsistent offsets can never make a kernel write outside its buffers).
+struct VarlenArgs {
+  const int* cu_q;      // null: dense [B,H,N,D] layout
+  const int* cu_k;
+  int H;                // heads
+  int total_q, total_k; // packed token counts
+};
+
+// One (sequence, head) as seen by a CTA, for either layout.
+struct SeqView {
+  int Nq, Nk;           // this sequence's lengths
+  int q_tok, k_tok;     // packed token index of row 0 (dense: 0)
+  int h;                // head (varlen)
+  int b;                // batch entry (varlen)
+};
+
+template <bool VARLEN>
+__device__ __forceinline__ SeqView seq_view(const VarlenArgs& va, int Nq, int Nk, int by) {
+  SeqView s;
+  if (!VARLEN) {
+    s.Nq = Nq; s.Nk = Nk; s.q_tok = 0; s.k_tok = 0; s.h = 0; s.b = 0;
+    return s;
+  }
+  s.b = by / va.H;
+  s.h = by % va.H;
+  int qa = __ldg(va.cu_q + s.b), qe = __ldg(va.cu_q + s.b + 1);
+  int ka = __ldg(va.cu_k + s.b), ke = __ldg(va.cu_k + s.b + 1);
+  qa = max(0, min(qa, va.total_q));
+  qe = max(qa, min(qe, va.total_q));
+  ka = max(0, min(ka, va.total_k));
+  ke = max(ka, min(ke, va.total_k));
+  s.q_tok = qa;
+  s.k_tok = ka;
+  s.Nq = min(qe - qa, Nq);
+  s.Nk = min(ke - ka, Nk);
+  return s;
+}
+
 struct FwdParams {
-  void* o;              // bf16 [B,H,Nq,D]
-  float* lse;           // fp32 [B,H,Nq], natural log
-  int Nq, Nk;
+  void* o;              // bf16 [B,H,Nq,D] (varlen: [total_q,H,D])
+  float* lse;           // fp32 [B,H,Nq] (varlen: [H,total_q]), natural log
+  int Nq, Nk;           // lengths (varlen: maximum lengths)
   int n_q_tiles;        // ceil(Nq / 128)
   float scale_log2;     // scale * log2(e)
   unsigned long long wait_limit_ns;
   unsigned* status;     // device status word pair
+  VarlenArgs va;
 };
 
+// Backward workspace rows: dense, head bh owns rows [bh*Nq_pad, bh*Nq_pad + Nq_pad);
+// varlen, head h owns Nq_pad rows (Nq_pad = 64*(ceil(total_q/64) + B)) and sequence b
+// starts at row 64*(ceil(cu_q[b]/64) + b) of it: 64-row aligned, never overlapping.
+__device__ __forceinline__ long long ws_row0(bool varlen, int bh, int Nq_pad, const SeqView& s) {
+  if (!varlen) return (long long)bh * Nq_pad;
+  return (long long)s.h * Nq_pad + 64LL * ((s.q_tok + 63) / 64 + s.b);
+}
+
 struct BwdParams {
-  void* dk;             // bf16 [B,H,Nk,D]
-  void* dv;             // bf16 [B,H,Nk,D]
-  float* dq_accum;      // fp32 [B*H, Nq_pad, D]
-  const float* lse2;    // fp32 [B*H, Nq_pad]: lse * log2(e); +inf on padded rows
-  const float* dlt;     // fp32 [B*H, Nq_pad]: rowsum(dO o O); 0 on padded rows
-  int Nq, Nk, Nq_pad;
+  void* dk;             // bf16 [B,H,Nk,D] (varlen: [total_k,H,D])
+  void* dv;
+  float* dq_accum;      // fp32 workspace rows x D
+  const float* lse2;    // fp32 workspace rows: lse * log2(e); +inf on padded rows
+  const float* dlt;     // fp32 workspace rows: rowsum(dO o O); 0 on padded rows
+  int Nq, Nk, Nq_pad;   // (varlen: maximum lengths, rows per head)
   int n_k_tiles;        // ceil(Nk / 128)
   float scale;          // softmax scale
   float scale_log2;     // scale * log2(e)
   unsigned long long wait_limit_ns;
   unsigned* status;
+  VarlenArgs va;
 };
 
 struct PrepParams {
-  const void* o;        // bf16 [B,H,Nq,D]
-  const void* dout;     // bf16 [B,H,Nq,D]
-  const float* lse;     // fp32 [B,H,Nq]
-  float* dq_accum;      // fp32 [B*H, Nq_pad, D] (zeroed here)
-  float* lse2;          // fp32 [B*H, Nq_pad]
-  float* dlt;           // fp32 [B*H, Nq_pad]
-  int BH, Nq, Nq_pad;
+  const void* o;        // bf16, layout as q
+  const void* dout;     // bf16, layout as q
+  const float* lse;     // fp32 [B,H,Nq] (varlen: [H,total_q])
+  float* dq_accum;      // fp32 workspace rows x D (zeroed here)
+  float* lse2;          // fp32 workspace rows
+  float* dlt;           // fp32 workspace rows
+  int BH, Nq, Nq_pad;   // (varlen: B*H, maximum Nq, rows per head)
+  VarlenArgs va;
 };
 
 struct ConvParams {
-  const float* dq_accum;  // fp32 [B*H, Nq_pad, D]
-  void* dq;               // bf16 [B,H,Nq,D]
+  const float* dq_accum;  // fp32 workspace rows x D
+  void* dq;               // bf16, layout as q
   int BH, Nq, Nq_pad;
   float scale;
+  VarlenArgs va;
 };
 
 // Host launchers (return cudaError_t of the launch).
+// Launchers; p.va.cu_q != nullptr selects the variable-length layout.
 cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int BH, cudaStream_t st);
 cudaError_t launch_bwd_prep(int D, const PrepParams& p, cudaStream_t st);

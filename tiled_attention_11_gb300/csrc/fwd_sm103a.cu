@@ -91,7 +91,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -110,7 +110,28 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   const int pair = (int)gridDim.x - 1 - (int)blockIdx.x;
   const int bh = blockIdx.y;
   const int q0 = pair * 2 * C::BM;
-  const int nk_tiles = (p.Nk + C::BN - 1) / C::BN;
+  const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, bh);
+  if (VARLEN) {
+    if (q0 >= sv.Nq) return;  // this sequence is shorter than the pair: nothing to do
+    if (sv.Nk == 0) {         // no keys: every row attends to nothing; O = 0, L = -inf
+      for (int e = threadIdx.x; e < 2 * C::BM * (D / 8); e += blockDim.x) {
+        const int q = q0 + e / (D / 8), part = e % (D / 8);
+        if (q >= sv.Nq) continue;
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                  ((size_t)(sv.q_tok + q) * p.va.H + sv.h) * D + part * 8) = make_uint4(0, 0, 0, 0);
+        if (part == 0) p.lse[(size_t)sv.h * p.va.total_q + sv.q_tok + q] = -INFINITY;
+      }
+      return;
+    }
+  }
+  // TMA coordinates of row r of this sequence: dense maps are [B*H][N][D] (y = row, z = bh),
+  // packed maps [total][H][D] (y = head, z = token); both land in shared memory alike.
+  const int qy_h = VARLEN ? sv.h : 0, qz_b = VARLEN ? sv.q_tok : bh;
+  const int kz_b = VARLEN ? sv.k_tok : bh;
+  auto ty = [&](int r) { return VARLEN ? qy_h : r; };
+  auto tzq = [&](int r) { return VARLEN ? qz_b + r : qz_b; };
+  auto tzk = [&](int r) { return VARLEN ? kz_b + r : kz_b; };
+  const int nk_tiles = (sv.Nk + C::BN - 1) / C::BN;
   // key tiles each query tile visits (causal: up to its diagonal tile)
   const int n_kv0 = CAUSAL ? min(nk_tiles, 2 * pair + 1) : nk_tiles;
   const int n_kv1 = CAUSAL ? min(nk_tiles, 2 * pair + 2) : nk_tiles;
@@ -152,7 +173,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
-                      c * C::CHUNK, q0 + t * C::BM, bh);
+                      c * C::CHUNK, ty(q0 + t * C::BM), tzq(q0 + t * C::BM));
       }
       int issued = 0;
       for (int j = 0; j < n_kv1; ++j) {
@@ -161,7 +182,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars[C::B_KF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
-                      c * C::CHUNK, j * C::BN, bh);
+                      c * C::CHUNK, ty(j * C::BN), tzk(j * C::BN));
         if (j >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) {
           issued = j;  // K_j is in flight; let the drain below wait for it
           mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, wc, 24);
@@ -170,7 +191,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
-                      c * C::CHUNK, j * C::BN, bh);
+                      c * C::CHUNK, ty(j * C::BN), tzk(j * C::BN));
         issued = j + 1;
       }
       if (*abort_flag) {
@@ -278,9 +299,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       reg_tie(s[3]);
 
       // Mask keys past Nk and (causal) keys after this row's query index.
-      const bool need_mask = ((j + 1) * C::BN > p.Nk) || (CAUSAL && (j * C::BN + C::BN - 1 > qt0));
+      const bool need_mask = ((j + 1) * C::BN > sv.Nk) || (CAUSAL && (j * C::BN + C::BN - 1 > qt0));
       if (need_mask) {
-        int lim = p.Nk - 1 - j * C::BN;  // last visible column of this tile
+        int lim = sv.Nk - 1 - j * C::BN;  // last visible column of this tile
         if (CAUSAL) lim = min(lim, q_idx - j * C::BN);
 #pragma unroll
         for (int g = 0; g < 4; ++g)
@@ -354,7 +375,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     if (ok && warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8)) {
       tc_fence_after();
       const float inv_l = 1.f / lr;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.Nq + q_idx) * D;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                            (VARLEN ? ((size_t)(sv.q_tok + q_idx) * p.va.H + sv.h) * D
+                                    : ((size_t)bh * sv.Nq + q_idx) * D);
 #pragma unroll
       for (int g = 0; g < D / 16; ++g) {
         uint32_t o[16];
@@ -369,12 +392,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         w1.y = pack_bf16(as_f(o[10]) * inv_l, as_f(o[11]) * inv_l);
         w1.z = pack_bf16(as_f(o[12]) * inv_l, as_f(o[13]) * inv_l);
         w1.w = pack_bf16(as_f(o[14]) * inv_l, as_f(o[15]) * inv_l);
-        if (q_idx < p.Nq) {
+        if (q_idx < sv.Nq) {
           reinterpret_cast<uint4*>(orow + g * 16)[0] = w0;
           reinterpret_cast<uint4*>(orow + g * 16)[1] = w1;
         }
       }
-      if (q_idx < p.Nq) p.lse[(size_t)bh * p.Nq + q_idx] = (m + log2f(l)) * 0.69314718055994530942f;
+      if (q_idx < sv.Nq)
+        p.lse[VARLEN ? (size_t)sv.h * p.va.total_q + sv.q_tok + q_idx : (size_t)bh * sv.Nq + q_idx] =
+            (m + log2f(l)) * 0.69314718055994530942f;
     }
   }
 
@@ -386,11 +411,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                      int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL>;
+  auto kern = fwd_kernel<D, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH);
@@ -419,10 +444,13 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, unsigned* status)
 
 cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int BH, cudaStream_t st) {
-#define TA11_FWD_CASE(DD)                                                        \
-  case DD:                                                                       \
-    return causal ? fwd::launch_t<DD, true>(tq, tk, tv, p, BH, st)               \
-                  : fwd::launch_t<DD, false>(tq, tk, tv, p, BH, st);
+#define TA11_FWD_CASE(DD)                                                                          \
+  case DD:                                                                                         \
+    if (p.va.cu_q)                                                                                 \
+      return causal ? fwd::launch_t<DD, true, true>(tq, tk, tv, p, BH, st)                         \
+                    : fwd::launch_t<DD, false, true>(tq, tk, tv, p, BH, st);                       \
+    return causal ? fwd::launch_t<DD, true, false>(tq, tk, tv, p, BH, st)                          \
+                  : fwd::launch_t<DD, false, false>(tq, tk, tv, p, BH, st);
   switch (D) {
     TA11_FWD_CASE(16)
     TA11_FWD_CASE(32)

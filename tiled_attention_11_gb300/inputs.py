@@ -89,3 +89,44 @@ def flops_fwd(p: Problem) -> float:
 def flops_bwd(p: Problem) -> float:
     """Backward FLOPs: 2.5x the forward convention."""
     return 2.5 * flops_fwd(p)
+
+
+def draw_varlen(lens_q, lens_k, H: int, D: int, seed: int, factor: float = 1.0):
+    """Packed variable-length batch: Q, K, V, dO as bf16 [total, H, D] drawn like `draw`
+    (standard normal float32, order Q, K, V, dO, times `factor`, bf16 RN) plus the
+    int32 offsets cu_q, cu_k (B + 1 entries, starting at 0)."""
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    rng = np.random.default_rng(seed)
+    out = []
+    for n in (int(cu_q[-1]), int(cu_k[-1]), int(cu_k[-1]), int(cu_q[-1])):
+        x = rng.standard_normal((n, H, D), dtype=np.float32)
+        if factor != 1.0:
+            x *= np.float32(factor)
+        out.append(torch.from_numpy(x).to(torch.bfloat16).contiguous())
+    return (*out, torch.from_numpy(cu_q), torch.from_numpy(cu_k))
+
+
+def doc_lengths(total: int, seed: int, median: float = 1024.0, lo: int = 16, hi: int = 8192) -> list[int]:
+    """Sequence lengths of a packed batch of documents: log-normal (sigma 1) around
+    `median`, clipped to [lo, hi], drawn until they fill `total` tokens (the last one
+    cut to fit)."""
+    rng = np.random.default_rng(seed)
+    lens, left = [], total
+    while left > 0:
+        n = int(np.clip(np.exp(rng.normal(np.log(median), 1.0)), lo, hi))
+        n = min(n, left)
+        lens.append(n)
+        left -= n
+    return lens
+
+
+def flops_varlen(lens_q, lens_k, H: int, D: int, causal: bool, backward: bool = False) -> float:
+    """FLOPs of a packed batch: the dense convention summed over its sequences."""
+    f = sum(4.0 * H * nq * nk * D * (0.5 if causal else 1.0) for nq, nk in zip(lens_q, lens_k))
+    return 2.5 * f if backward else f
+
+
+# Packed batch of documents, 16384 tokens (the token count of the 4 x 4096 layer) with
+# 32 heads of D = 128, causal within each document.
+VARLEN_DOCS = dict(lens=doc_lengths(16384, seed=7), H=32, D=128, causal=True, factor=0.5)
