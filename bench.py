@@ -356,7 +356,7 @@ def run_table(args):
     print("| workload | fwd ms | fwd TFLOP/s | fwd % peak | bwd ms | bwd TFLOP/s | bwd % peak | fwd GB/s (% HBM) "
           "| step ms direct / CUDA graph | L2 flush |")
     print("|---|---|---|---|---|---|---|---|---|---|")
-    for p in ([] if args.varlen_only else I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]):
+    for p in ([] if args.varlen_only or args.window_only else I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]):
         q, k, v, do = (t.to(dev) for t in I.draw(p, 0))
         o = torch.empty_like(q)
         lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
@@ -408,7 +408,75 @@ def run_table(args):
               f"| {'yes' if small else 'no'} |", flush=True)
         del q, k, v, do, o, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()
-    _table_varlen(args, dev, sustained, hbm)
+    if not args.window_only:
+        _table_varlen(args, dev, sustained, hbm)
+    if not args.varlen_only:
+        _table_window(args, dev, sustained)
+
+
+def window_pairs(Nq: int, Nk: int, causal: bool, window_left: int, window_right: int, n_global: int) -> int:
+    """(query, key) pairs the local-window + global-token mask allows, row by row in closed
+    form: a global row sees every key up to its last visible one (hi); another row sees its
+    window [wlo, whi] plus the global keys [0, g) not already in it, all clipped to hi."""
+    import numpy as np
+    i = np.arange(Nq, dtype=np.int64)
+    hi = np.full(Nq, Nk - 1, np.int64)
+    if causal:
+        hi = np.minimum(hi, i)
+    wlo = np.zeros(Nq, np.int64) if window_left < 0 else np.maximum(i - window_left, 0)
+    whi = hi if window_right < 0 else np.minimum(hi, i + window_right)
+    win = np.maximum(whi - wlo + 1, 0)
+    a = np.minimum(min(n_global, Nk) - 1, hi)                 # last global key a row may see
+    overlap = np.maximum(np.minimum(a, whi) - wlo + 1, 0)
+    cnt = win + np.maximum(a + 1, 0) - overlap
+    cnt = np.where(i < n_global, hi + 1, cnt)
+    return int(np.maximum(cnt, 0).sum())
+
+
+# Local-window workloads of --table: (B, H, N, D, causal, window_left, window_right, n_global)
+WINDOW_TABLE = [(1, 32, 32768, 128, True, 4096, -1, 0), (1, 32, 32768, 128, True, 1024, -1, 64),
+                (1, 16, 65536, 64, False, 512, 512, 128)]
+
+
+def _table_window(args, dev, sustained):
+    """Local-window + global-token rows: FLOPs count only the allowed (query, key) pairs."""
+    import torch
+    from tiled_attention_11_gb300 import _lib
+    from tiled_attention_11_gb300 import inputs as I
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for (B, H, N, D, causal, wl, wr, g) in WINDOW_TABLE:
+        p = I.Problem(B, H, N, N, D, causal, factor=0.5)
+        q, k, v, do = (t.to(dev) for t in I.draw(p, 0))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(_lib.fa_bwd_workspace_size(B, H, N, N, D), dtype=torch.uint8, device=dev)
+        fwd = lambda: _lib.fa_fwd_window(q, k, v, o, lse, causal, wl, wr, g, p.scale)  # noqa: E731
+        bwd = lambda: _lib.fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, causal, wl, wr, g, p.scale,  # noqa: E731
+                                         workspace=ws)
+        res = []
+        for fn in (fwd, bwd, lambda: (fwd(), bwd())):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(args.steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            res.append(statistics.median(ts))
+        ff = 4.0 * B * H * D * window_pairs(N, N, causal, wl, wr, g)
+        tf, tb = ff / res[0] / 1e9, 2.5 * ff / res[1] / 1e9
+        gbs = (2 * D * B * H * 4 * N + 4 * B * H * N) / res[0] / 1e6
+        name = f"window B{B}H{H}N{N}D{D}{'c' if causal else 'n'} wl{wl} wr{wr} g{g}"
+        print(f"| {name} | {res[0]:.4f} | {tf:.1f} | {100 * tf / sustained:.1f}% | {res[1]:.4f} | {tb:.1f} | "
+              f"{100 * tb / sustained:.1f}% | {gbs:.0f} | {res[2]:.4f} / - | yes |", flush=True)
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
 
 
 def _table_varlen(args, dev, sustained, hbm):
@@ -506,6 +574,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--table", action="store_true", help="time every workload, print a markdown table")
     ap.add_argument("--varlen-only", action="store_true", help="with --table: only the packed variable-length row")
+    ap.add_argument("--window-only", action="store_true", help="with --table: only the local-window rows")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.table:

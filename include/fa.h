@@ -120,6 +120,29 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
 void fa_set_bwd_main_events(cudaEvent_t begin, cudaEvent_t end);
 
 /*
+ * Local-window + global-token attention ([FA2-impl] §7: sparse attention combining local
+ * windows and global tokens; [FA-mem] case 2: local blocks plus global key points for
+ * 100K-token sequences), as an exact mask on absolute (top-left) indices: key j is visible
+ * to query i iff
+ *     j < Nk  and  (causal == 0 or j <= i)  and
+ *     ( (window_left < 0 or j >= i - window_left) and (window_right < 0 or j <= i + window_right)
+ *       or j < n_global or i < n_global )
+ * A negative window bound is unbounded; n_global tokens (the first queries and keys) see
+ * and are seen by every token (subject to the causal condition).  A query row with no
+ * visible key gets O = 0 and L = -inf, and zero gradients.  Key tiles that no row of a
+ * query tile can see are skipped, so the work grows with the window, not with Nk.
+ * Layout, workspace (fa_bwd_workspace_size), ownership, asynchrony and errors as for
+ * fa_fwd / fa_bwd.
+ */
+int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                  int D, float scale, int causal, int window_left, int window_right, int n_global,
+                  cudaStream_t stream);
+int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal,
+                  int window_left, int window_right, int n_global, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream);
+
+/*
  * Variable-length ("ragged") batches ([FA2-impl] §7 names ragged inputs as the next step;
  * [FA-hist] §2.3 dynamic sequence lengths): B independent sequences packed back to back.
  *   q, o, dO, dq: [total_q, H, D] bf16;  k, v, dk, dv: [total_k, H, D] bf16 (D innermost)

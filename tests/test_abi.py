@@ -153,3 +153,20 @@ def test_varlen_validation_codes(L):
     def rnd(x):
         return (x + 255) // 256 * 256
     assert L.fa_bwd_varlen_workspace_size(3, 2, 100, 60, 64) == rnd(2 * rows * 64 * 4) + 2 * rnd(2 * rows * 4)
+
+
+def test_window_validation_codes(L):
+    vp = ctypes.c_void_p
+    q, k, v, o, lse = (vp(x) for x in ptrs(5))
+    call = lambda **kw: L.fa_fwd_window(kw.get("q", q), k, v, o, lse, 2, 3, 100, 77, kw.get("D", 64), 0.125, 1,  # noqa: E731
+                                        kw.get("wl", 16), -1, kw.get("g", 4), None)
+    assert call(q=vp(0)) == _lib.FA_ERR_INVALID_ARG
+    assert call(D=48) == _lib.FA_ERR_UNSUPPORTED_D
+    assert call(q=vp(ptrs(1)[0] + 8)) == _lib.FA_ERR_MISALIGNED
+    # any window / global-token values are valid (negative: unbounded, large: clipped)
+    for wl, g in ((-1, 0), (0, 0), (1 << 30, 1 << 30), (-5, -3)):
+        assert call(wl=wl, g=g) == _lib.FA_ERR_DEVICE
+    p = [vp(x) for x in ptrs(10)]
+    need = L.fa_bwd_workspace_size(2, 3, 100, 77, 64)
+    assert L.fa_bwd_window(*p[:9], 2, 3, 100, 77, 64, 0.125, 1, 16, -1, 4, p[9], need - 1, None) == _lib.FA_ERR_WORKSPACE
+    assert L.fa_bwd_window(*p[:9], 2, 3, 100, 77, 64, 0.125, 1, 16, -1, 4, p[9], need, None) == _lib.FA_ERR_DEVICE

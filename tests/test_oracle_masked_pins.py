@@ -247,3 +247,13 @@ def test_planted_mistakes_are_caught(name, old, new):
         except Exception:  # a crash is also a caught mistake
             results[pin.__name__] = False
     assert not all(results.values()), f"planted mistake '{name}' passed every pin"
+
+
+@pytest.mark.parametrize("nq,nk,causal,wl,wr,g", [(40, 40, True, 5, -1, 0), (40, 40, True, 7, -1, 3),
+                                                  (33, 50, False, 4, 9, 6), (50, 33, False, 0, 0, 0),
+                                                  (30, 30, False, -1, 2, 40), (45, 20, True, 3, -1, 25)])
+def test_bench_pair_count_matches_the_mask(nq, nk, causal, wl, wr, g):
+    # the FLOP count bench.py reports for local-window rows counts exactly the allowed pairs
+    import bench
+    want = int(masked_ref.allowed(np.arange(nq), np.arange(nk), nk, causal, wl, wr, g).sum())
+    assert bench.window_pairs(nq, nk, causal, wl, wr, g) == want

@@ -30,7 +30,7 @@ FA_ERR_SCRATCH_LIMIT = 8
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_device_status",
             "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
             "fa_graph_create", "fa_graph_launch", "fa_graph_destroy", "fa_fwd_varlen", "fa_bwd_varlen",
-            "fa_bwd_varlen_workspace_size")
+            "fa_bwd_varlen_workspace_size", "fa_fwd_window", "fa_bwd_window")
 
 _lib = None
 
@@ -76,6 +76,10 @@ def lib() -> ctypes.CDLL:
     L.fa_graph_launch.restype = i
     L.fa_graph_destroy.argtypes = [vp]
     L.fa_graph_destroy.restype = None
+    L.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp]
+    L.fa_fwd_window.restype = i
+    L.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp, sz, vp]
+    L.fa_bwd_window.restype = i
     L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
     L.fa_fwd_varlen.restype = i
     L.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i, i]
@@ -288,3 +292,38 @@ def fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, m
                              int(max_seqlen_q), int(max_seqlen_k), D, float(scale), int(bool(causal)),
                              _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(rc, "fa_bwd_varlen")
+
+
+# ----------------------------------------------------------------------------- local window + global tokens
+def fa_fwd_window(q, k, v, o, lse, causal: bool, window_left: int, window_right: int, n_global: int,
+                  scale: float | None = None, stream=None) -> None:
+    """C ``fa_fwd_window`` on [B,H,N,D] bf16 tensors (negative window bound: unbounded)."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib().fa_fwd_window(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
+                             _ptr(v, "v", torch.bfloat16), _ptr(o, "o", torch.bfloat16),
+                             _ptr(lse, "lse", torch.float32), B, H, Nq, Nk, D, float(scale), int(bool(causal)),
+                             int(window_left), int(window_right), int(n_global), _stream(stream))
+    _check(rc, "fa_fwd_window")
+
+
+def fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, causal: bool, window_left: int, window_right: int,
+                  n_global: int, scale: float | None = None, workspace=None, stream=None) -> None:
+    """C ``fa_bwd_window``; allocates the workspace with torch when none is given."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if workspace is None:
+        workspace = torch.empty(max(fa_bwd_workspace_size(B, H, Nq, Nk, D), 256), dtype=torch.uint8,
+                                device=q.device)
+    rc = lib().fa_bwd_window(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
+                             _ptr(v, "v", torch.bfloat16), _ptr(o, "o", torch.bfloat16),
+                             _ptr(lse, "lse", torch.float32), _ptr(do, "do", torch.bfloat16),
+                             _ptr(dq, "dq", torch.bfloat16), _ptr(dk, "dk", torch.bfloat16),
+                             _ptr(dv, "dv", torch.bfloat16), B, H, Nq, Nk, D, float(scale), int(bool(causal)),
+                             int(window_left), int(window_right), int(n_global),
+                             _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(rc, "fa_bwd_window")

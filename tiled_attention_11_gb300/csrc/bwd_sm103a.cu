@@ -116,7 +116,7 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   reinterpret_cast<uint4*>(dst)[1] = w1;
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -145,9 +145,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   auto tzq = [&](int r) { return VARLEN ? qz_b + r : qz_b; };
   auto tzk = [&](int r) { return VARLEN ? kz_b + r : kz_b; };
   const long long wrow0 = ws_row0(VARLEN, bh, p.Nq_pad, sv);
+  // Query steps (64 rows) that see a key of this tile: causal ones start at the diagonal;
+  // with the local mask they are the global query steps [a, g) and the window steps [L, hi)
+  // (every step when the tile holds a global key).
   const int n_qt = (sv.Nq + C::BM - 1) / C::BM;
-  const int i_start = CAUSAL ? min(k0 / C::BM, n_qt) : 0;
-  const int n_it = n_qt - i_start;
+  const int qlo = CAUSAL ? k0 : 0;  // first query that may see key k0
+  TileSet qs = TileSet::make(qlo / C::BM, qlo / C::BM, qlo / C::BM, n_qt);
+  if (LOCAL && k0 >= p.lm.n_glob) {
+    const int ke = min(k0 + C::BN, sv.Nk) - 1;
+    const int qmax = min(sv.Nq - 1, ke + p.lm.win_l);
+    qs = TileSet::make(qlo / C::BM, (p.lm.n_glob + C::BM - 1) / C::BM, max(qlo, k0 - p.lm.win_r) / C::BM,
+                       qmax >= 0 ? qmax / C::BM + 1 : 0);
+  }
+  const int n_it = qs.count();
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
 
   if (threadIdx.x == 0) {
@@ -192,7 +202,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % C::NS;
-        const int i = i_start + it;
+        const int i = qs.at(it);
         if (it >= C::NS && !mbar_wait(&bars[C::B_QE + s], ((it / C::NS) - 1) & 1, wc, 31)) break;
         mbar_arrive_expect_tx(&bars[C::B_QF + s], 2 * C::Q_TILE + 2 * C::BM * 4);
         for (int c = 0; c < C::NCHUNK; ++c) {
@@ -309,7 +319,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 
     for (int it = 0; it < n_it && ok; ++it) {
       const int s = it % C::NS;
-      const int i = i_start + it;
+      const int i = qs.at(it);
       if (!warp_wait(&bars[C::B_QF + s], (it / C::NS) & 1, wc, 38) || !warp_wait(&bars[C::B_SF], it & 1, wc, 39)) {
         ok = false;
         break;
@@ -320,15 +330,24 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       tmem_wait_ld(sreg);
       const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * C::BM * 4) + col0;
       const float* dlt = reinterpret_cast<const float*>(smem + C::OFF_DLT + s * C::BM * 4) + col0;
-      const bool need_mask = (k0 + C::BN > sv.Nk) || (CAUSAL && (k0 + C::BN - 1 > i * C::BM + col0));
-      int lim = 1 << 30;  // columns c with q = i*64+col0+c < key are masked (causal)
-      if (CAUSAL) lim = key - (i * C::BM + col0);
+      const int qb = i * C::BM + col0;  // query of column 0 of this warpgroup's half
+      bool need_mask = (k0 + C::BN > sv.Nk) || (CAUSAL && (k0 + C::BN - 1 > qb));
+      if (LOCAL)
+        need_mask = need_mask || !(k0 + C::BN <= p.lm.n_glob || qb + 31 < p.lm.n_glob ||
+                                   (k0 >= qb + 31 - p.lm.win_l && k0 + C::BN - 1 <= qb + p.lm.win_r));
+      int lim = 1 << 30;  // columns c with q = qb + c < key are masked (causal)
+      if (CAUSAL) lim = key - qb;
       const bool key_valid = key < sv.Nk;
+      // local: for a non-global key, columns c >= gq (non-global queries) are visible only
+      // inside the window key - win_r <= q <= key + win_l
+      const bool kglob = !LOCAL || key < p.lm.n_glob;
+      const int gq = p.lm.n_glob - qb, wlo = key - p.lm.win_r - qb, whi = key + p.lm.win_l - qb;
       float pv[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         float x = ex2(fmaf(as_f(sreg[c]), sl2, -lse2[c]));
         if (need_mask && (!key_valid || (CAUSAL && c < lim))) x = 0.f;
+        if (LOCAL && need_mask && !kglob && c >= gq && (c < wlo || c > whi)) x = 0.f;
         pv[c] = x;
       }
       uint32_t pk[16];
@@ -448,7 +467,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (threadIdx.x == 0) {
-        float* gdst = p.dq_accum + ((size_t)wrow0 + (size_t)(i_start + it) * C::BM) * D;
+        float* gdst = p.dq_accum + ((size_t)wrow0 + (size_t)qs.at(it) * C::BM) * D;
         bulk_reduce_add_f32(gdst, stg, C::STG_BYTES);
         bulk_commit_group();
       }
@@ -511,7 +530,8 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
     if (part == 0) {
       p.dlt[wr] = acc;
       const size_t li = VARLEN ? (size_t)sv.h * p.va.total_q + sv.q_tok + r : (size_t)bh * sv.Nq + r;
-      p.lse2[wr] = valid ? p.lse[li] * 1.4426950408889634f : INFINITY;
+      const float L = valid ? p.lse[li] : -INFINITY;  // -inf: the row sees no key
+      p.lse2[wr] = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
     }
   }
 }
@@ -539,11 +559,11 @@ __global__ void __launch_bounds__(256) convert_kernel(const ConvParams p) {
   *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + tok * D + d) = w;
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                      const BwdParams& p, int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = bwd_kernel<D, CAUSAL, VARLEN>;
+  auto kern = bwd_kernel<D, CAUSAL, VARLEN, LOCAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.n_k_tiles, (unsigned)BH);
@@ -581,6 +601,10 @@ cudaError_t conv_t(const ConvParams& p, cudaStream_t st) {
 
 cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int BH, cudaStream_t st) {
+  if (p.local) {
+    TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true, false, true>(tq, tk, tv, tdo, p, BH, st)
+                             : bwd::launch_t<DD, false, false, true>(tq, tk, tv, tdo, p, BH, st)))
+  }
   if (p.va.cu_q) {
     TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true, true>(tq, tk, tv, tdo, p, BH, st)
                              : bwd::launch_t<DD, false, true>(tq, tk, tv, tdo, p, BH, st)))

@@ -200,8 +200,23 @@ size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int D) {
   return ws_layout(B, H, Nq, D).total;
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
-           float scale, int causal, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Mask arguments of the local-window entry points -> kernel form (negative: unbounded;
+// global-token counts beyond both lengths change nothing and are clipped).
+ta11::LocalMask local_mask(int Nq, int Nk, int window_left, int window_right, int n_global) {
+  ta11::LocalMask m;
+  m.win_l = (window_left < 0 || window_left >= ta11::kUnbounded) ? ta11::kUnbounded : window_left;
+  m.win_r = (window_right < 0 || window_right >= ta11::kUnbounded) ? ta11::kUnbounded : window_right;
+  const int nmax = Nq > Nk ? Nq : Nk;
+  m.n_glob = n_global < 0 ? 0 : (n_global > nmax ? nmax : n_global);
+  return m;
+}
+
+int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
+              float scale, int causal, const ta11::LocalMask* lm, cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   int rc = check_sizes(B, H, Nq, Nk, D, scale);
   if (rc != FA_OK) return rc;
@@ -232,12 +247,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = status;
+  if (lm) {
+    p.lm = *lm;
+    p.local = 1;
+  }
   return ta11::launch_fwd(D, causal != 0, tq, tk, tv, p, (int)BH, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
-           void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal, void* workspace,
-           size_t workspace_bytes, cudaStream_t stream) {
+int bwd_dense(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+              void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal,
+              const ta11::LocalMask* lm, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   int rc = check_sizes(B, H, Nq, Nk, D, scale);
   if (rc != FA_OK) return rc;
@@ -288,6 +307,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   bp.scale_log2 = scale * kLog2e;
   bp.wait_limit_ns = g_wait_limit_ns.load();
   bp.status = status;
+  if (lm) {
+    bp.lm = *lm;
+    bp.local = 1;
+  }
   cudaEvent_t ev_b = nullptr, ev_e = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_ev_mu);
@@ -301,6 +324,38 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale};
   if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
+           float scale, int causal, cudaStream_t stream) {
+  return fwd_dense(q, k, v, o, lse, B, H, Nq, Nk, D, scale, causal, nullptr, stream);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+           void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal, void* workspace,
+           size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_dense(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, D, scale, causal, nullptr, workspace,
+                   workspace_bytes, stream);
+}
+
+int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                  int D, float scale, int causal, int window_left, int window_right, int n_global,
+                  cudaStream_t stream) {
+  const ta11::LocalMask m = local_mask(Nq, Nk, window_left, window_right, n_global);
+  return fwd_dense(q, k, v, o, lse, B, H, Nq, Nk, D, scale, causal, &m, stream);
+}
+
+int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal,
+                  int window_left, int window_right, int n_global, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+  const ta11::LocalMask m = local_mask(Nq, Nk, window_left, window_right, n_global);
+  return bwd_dense(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, D, scale, causal, &m, workspace, workspace_bytes,
+                   stream);
 }
 
 int fa_device_status(unsigned* site, int reset) {

@@ -48,6 +48,42 @@ __device__ __forceinline__ SeqView seq_view(const VarlenArgs& va, int Nq, int Nk
   return s;
 }
 
+// Local-window + global-token mask (absolute indices, top-left like the causal mask):
+// key j is visible to query i iff j < Nk, (not causal or j <= i) and
+// (i - win_l <= j <= i + win_r  or  j < n_glob  or  i < n_glob).  An unbounded side is
+// stored as kUnbounded, so the comparisons need no special case and cannot overflow.
+constexpr int kUnbounded = 1 << 29;
+struct LocalMask {
+  int win_l, win_r;     // window extents (kUnbounded: no limit)
+  int n_glob;           // global tokens: the first n_glob queries and keys
+};
+
+// Tile indices [a, g) U [L, hi), ascending; make() orders and clips the bounds so the
+// two parts are disjoint (g <= L) and count() is their total size.
+struct TileSet {
+  int a, g, L, hi;
+  static __host__ __device__ __forceinline__ TileSet make(int a, int g, int L, int hi) {
+    TileSet t;
+    t.hi = hi > 0 ? hi : 0;
+    t.a = a < 0 ? 0 : (a > t.hi ? t.hi : a);
+    t.g = g < t.a ? t.a : (g > t.hi ? t.hi : g);
+    t.L = L < t.g ? t.g : (L > t.hi ? t.hi : L);
+    return t;
+  }
+  __host__ __device__ __forceinline__ int count() const { return (g - a) + (hi - L); }
+  __host__ __device__ __forceinline__ int at(int n) const { return n < g - a ? a + n : L + (n - (g - a)); }
+  __host__ __device__ __forceinline__ bool has(int x) const { return (x >= a && x < g) || (x >= L && x < hi); }
+  // smallest member greater than x, or kNone
+  static constexpr int kNone = 0x7fffffff;
+  __host__ __device__ __forceinline__ int next(int x) const {
+    int y = x + 1;
+    if (y < a) y = a;
+    if (y < g) return y;
+    if (y < L) y = L;
+    return y < hi ? y : kNone;
+  }
+};
+
 struct FwdParams {
   void* o;              // bf16 [B,H,Nq,D] (varlen: [total_q,H,D])
   float* lse;           // fp32 [B,H,Nq] (varlen: [H,total_q]), natural log
@@ -57,6 +93,8 @@ struct FwdParams {
   unsigned long long wait_limit_ns;
   unsigned* status;     // device status word pair
   VarlenArgs va;
+  LocalMask lm;         // used when `local` is set
+  int local;            // 1: apply the local-window + global-token mask
 };
 
 // Backward workspace rows: dense, head bh owns rows [bh*Nq_pad, bh*Nq_pad + Nq_pad);
@@ -80,6 +118,8 @@ struct BwdParams {
   unsigned long long wait_limit_ns;
   unsigned* status;
   VarlenArgs va;
+  LocalMask lm;         // used when `local` is set
+  int local;            // 1: apply the local-window + global-token mask
 };
 
 struct PrepParams {
@@ -102,7 +142,8 @@ struct ConvParams {
 };
 
 // Host launchers (return cudaError_t of the launch).
-// Launchers; p.va.cu_q != nullptr selects the variable-length layout.
+// Launchers; p.va.cu_q != nullptr selects the variable-length layout, p.local the
+// local-window + global-token mask (dense layout only).
 cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int BH, cudaStream_t st);
 cudaError_t launch_bwd_prep(int D, const PrepParams& p, cudaStream_t st);

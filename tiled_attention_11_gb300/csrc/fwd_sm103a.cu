@@ -91,7 +91,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -107,23 +107,42 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   // Query-tile pairs of one head are adjacent in launch order, so the CTAs resident at
   // any moment share the K/V of a few heads in L2; within a head the heaviest
   // (causal) pairs go first.
-  const int pair = (int)gridDim.x - 1 - (int)blockIdx.x;
+  // (Local mask: pair 0 holds the global query rows, which see every key; it goes first.)
+  const int pair = LOCAL ? (int)blockIdx.x : (int)gridDim.x - 1 - (int)blockIdx.x;
   const int bh = blockIdx.y;
   const int q0 = pair * 2 * C::BM;
   const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, bh);
-  if (VARLEN) {
-    if (q0 >= sv.Nq) return;  // this sequence is shorter than the pair: nothing to do
-    if (sv.Nk == 0) {         // no keys: every row attends to nothing; O = 0, L = -inf
-      for (int e = threadIdx.x; e < 2 * C::BM * (D / 8); e += blockDim.x) {
-        const int q = q0 + e / (D / 8), part = e % (D / 8);
-        if (q >= sv.Nq) continue;
-        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
-                                  ((size_t)(sv.q_tok + q) * p.va.H + sv.h) * D + part * 8) = make_uint4(0, 0, 0, 0);
-        if (part == 0) p.lse[(size_t)sv.h * p.va.total_q + sv.q_tok + q] = -INFINITY;
-      }
-      return;
+  if (VARLEN && q0 >= sv.Nq) return;  // this sequence is shorter than the pair: nothing to do
+  auto o_row = [&](int q) -> size_t {  // element offset of output row q
+    return (VARLEN ? ((size_t)(sv.q_tok + q) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + q)) * D;
+  };
+  auto lse_idx = [&](int q) -> size_t {
+    return VARLEN ? (size_t)sv.h * p.va.total_q + sv.q_tok + q : (size_t)bh * sv.Nq + q;
+  };
+  // Key tiles each query tile visits: [0, hi) for the plain masks (causal: up to the
+  // diagonal tile); with the local mask the global key tiles [0, g) and the window tiles
+  // [L, hi).  A query tile past the sequence visits nothing.
+  auto key_set = [&](int qa) -> TileSet {
+    if (!LOCAL) {  // plain masks: [0, hi); a tile past the sequence is computed, never stored
+      const int nkt = (sv.Nk + C::BN - 1) / C::BN;
+      return TileSet::make(0, 0, 0, CAUSAL ? min(nkt, qa / C::BM + 1) : nkt);
     }
-  }
+    if (qa >= sv.Nq) return TileSet::make(0, 0, 0, 0);
+    const int qb = min(qa + C::BM, sv.Nq) - 1;
+    int kmax = sv.Nk - 1;
+    if (LOCAL && qa >= p.lm.n_glob) kmax = min(kmax, max(qb + p.lm.win_r, p.lm.n_glob - 1));
+    if (CAUSAL) kmax = min(kmax, qb);
+    const int hi = kmax >= 0 ? kmax / C::BN + 1 : 0;
+    if (!LOCAL || qa < p.lm.n_glob) return TileSet::make(0, 0, 0, hi);
+    return TileSet::make(0, (p.lm.n_glob + C::BN - 1) / C::BN, max(qa - p.lm.win_l, 0) / C::BN, hi);
+  };
+  const TileSet ks0 = key_set(q0), ks1 = key_set(q0 + C::BM);
+  // The producer and the UMMA issuer walk the union of both sets in ascending order.
+  auto next_kt = [&](int kt) { return min(ks0.next(kt), ks1.next(kt)); };
+  // kNone when no row of the pair sees a key (a sequence without keys, or a local mask
+  // that hides every key): then nothing is loaded or issued, and the softmax warps write
+  // O = 0, L = -inf.
+  const int first_kt = next_kt(-1);
   // TMA coordinates of row r of this sequence: dense maps are [B*H][N][D] (y = row, z = bh),
   // packed maps [total][H][D] (y = head, z = token); both land in shared memory alike.
   const int qy_h = VARLEN ? sv.h : 0, qz_b = VARLEN ? sv.q_tok : bh;
@@ -131,10 +150,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   auto ty = [&](int r) { return VARLEN ? qy_h : r; };
   auto tzq = [&](int r) { return VARLEN ? qz_b + r : qz_b; };
   auto tzk = [&](int r) { return VARLEN ? kz_b + r : kz_b; };
-  const int nk_tiles = (sv.Nk + C::BN - 1) / C::BN;
-  // key tiles each query tile visits (causal: up to its diagonal tile)
-  const int n_kv0 = CAUSAL ? min(nk_tiles, 2 * pair + 1) : nk_tiles;
-  const int n_kv1 = CAUSAL ? min(nk_tiles, 2 * pair + 2) : nk_tiles;
+  const bool has_q[2] = {ks0.count() > 0, ks1.count() > 0};
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
 
   if (threadIdx.x == 0) {
@@ -170,19 +186,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       for (int t = 0; t < 2; ++t) {
+        if (!has_q[t]) continue;  // a tile without keys is never read
         mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
                       c * C::CHUNK, ty(q0 + t * C::BM), tzq(q0 + t * C::BM));
       }
       int issued = 0;
-      for (int j = 0; j < n_kv1; ++j) {
+      int j = 0;
+      for (int kt = first_kt; kt != TileSet::kNone; kt = next_kt(kt), ++j) {
         const int s = j % C::NS;
         if (j >= C::NS && !mbar_wait(&bars[C::B_KE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
         mbar_arrive_expect_tx(&bars[C::B_KF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
-                      c * C::CHUNK, ty(j * C::BN), tzk(j * C::BN));
+                      c * C::CHUNK, ty(kt * C::BN), tzk(kt * C::BN));
         if (j >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) {
           issued = j;  // K_j is in flight; let the drain below wait for it
           mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, wc, 24);
@@ -191,7 +209,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
-                      c * C::CHUNK, ty(j * C::BN), tzk(j * C::BN));
+                      c * C::CHUNK, ty(kt * C::BN), tzk(kt * C::BN));
         issued = j + 1;
       }
       if (*abort_flag) {
@@ -204,64 +222,132 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, w2, 20);
           mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, w2, 21);
         }
-        mbar_wait(&bars[C::B_Q], 0, w2, 22);
-        mbar_wait(&bars[C::B_Q + 1], 0, w2, 22);
+        for (int t = 0; t < 2; ++t)
+          if (has_q[t]) mbar_wait(&bars[C::B_Q + t], 0, w2, 22);
       }
     }
   } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------------- UMMA issuer
-    if (lane == 0) {
+    if (lane == 0 && first_kt != TileSet::kNone) {
       // Base descriptors, built once: Q tiles and the K ring K-major, the V ring MN-major.
       const uint64_t dq0 = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);
       const uint64_t dk0 = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);
       const uint64_t dv0 = sdesc(sbase + C::OFF_V, C::CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);
-      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+      auto issue_s = [&](int t, int slot) {  // S_t = Q_t K^T (K in ring slot `slot`)
         const uint64_t dq = desc_adv(dq0, (uint32_t)(t * C::TILE_BYTES));
-        const uint64_t dk = desc_adv(dk0, (uint32_t)((j % C::NS) * C::TILE_BYTES));
+        const uint64_t dk = desc_adv(dk0, (uint32_t)(slot * C::TILE_BYTES));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tmem + C::TMEM_S + t * 128, desc_adv(dq, kmajor_off<D>(kk)), desc_adv(dk, kmajor_off<D>(kk)),
                   C::IDESC_S, kk > 0 ? 1u : 0u);
         umma_commit(&bars[C::B_SF + t]);
       };
-      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j   (A = P from TMEM)
-        const uint64_t dv = desc_adv(dv0, (uint32_t)((j % C::NS) * C::TILE_BYTES));
+      auto issue_pv = [&](int t, int slot, bool acc) {  // O_t (+)= P_t V   (A = P from TMEM)
+        const uint64_t dv = desc_adv(dv0, (uint32_t)(slot * C::TILE_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           umma_ts(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * 128 + kk * 8,
-                  desc_adv(dv, (uint32_t)(kk * 16 * C::ROWB)), C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                  desc_adv(dv, (uint32_t)(kk * 16 * C::ROWB)), C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
         umma_commit(&bars[C::B_O + t]);
       };
-      bool ok = mbar_wait(&bars[C::B_Q], 0, wc, 2) && mbar_wait(&bars[C::B_KF], 0, wc, 3);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        if ((ok = mbar_wait(&bars[C::B_Q + 1], 0, wc, 2))) {
+      // Position j of the walk holds key tile kt in ring slot j % NS; query tile t takes
+      // part when its set has kt.  S_t of a position is issued one position ahead, after
+      // P_t V of t's previous position (in-order UMMA), so t's softmax of one tile
+      // overlaps the other tile's MMAs.
+      bool ok;
+      if (!LOCAL) {
+        // Plain masks: each tile visits a prefix [0, n_kv_t) of the key tiles, tile 1 as
+        // many as tile 0 or (causal diagonal) one more.  The issuer's per-step bookkeeping
+        // sits on the critical path (a general walk here cost 2% of the forward), so it
+        // stays this lean.
+        const int n_kv0 = ks0.count(), n_kv1 = ks1.count();
+        ok = mbar_wait(&bars[C::B_Q], 0, wc, 2) && mbar_wait(&bars[C::B_KF], 0, wc, 3);
+        if (ok) {
           tc_fence_after();
-          issue_s(1, 0);
-          umma_commit(&bars[C::B_KE]);
+          issue_s(0, 0);
+          if ((ok = mbar_wait(&bars[C::B_Q + 1], 0, wc, 2))) {
+            tc_fence_after();
+            issue_s(1, 0);
+            umma_commit(&bars[C::B_KE]);
+          }
         }
-      }
-      for (int j = 0; ok && j < n_kv1; ++j) {
-        const int s = j % C::NS, s1 = (j + 1) % C::NS;
-        if (!(ok = mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
-        const bool next_k = j + 1 < n_kv1;
-        if (next_k && !(ok = mbar_wait(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
-        // tile 0: P0_j -> O0, then S0 of the next key tile over the consumed P0
-        if (j < n_kv0) {
-          if (!(ok = mbar_wait(&bars[C::B_PF], j & 1, wc, 4))) break;
+        for (int j = 0; ok && j < n_kv1; ++j) {
+          const int s = j % C::NS, s1 = (j + 1) % C::NS;
+          if (!(ok = mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
+          const bool next_k = j + 1 < n_kv1;
+          if (next_k && !(ok = mbar_wait(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
+          // tile 0: P0_j -> O0, then S0 of the next key tile over the consumed P0
+          if (j < n_kv0) {
+            if (!(ok = mbar_wait(&bars[C::B_PF], j & 1, wc, 4))) break;
+            tc_fence_after();
+            issue_pv(0, s, j > 0);
+            if (j + 1 < n_kv0) issue_s(0, s1);
+          }
+          // tile 1
+          if (!(ok = mbar_wait(&bars[C::B_PF + 1], j & 1, wc, 4))) break;
           tc_fence_after();
-          issue_pv(0, j);
-          if (j + 1 < n_kv0) issue_s(0, j + 1);
+          issue_pv(1, s, j > 0);
+          umma_commit(&bars[C::B_VE + s]);
+          if (next_k) {
+            issue_s(1, s1);
+            umma_commit(&bars[C::B_KE + s1]);
+          }
         }
-        // tile 1
-        if (!(ok = mbar_wait(&bars[C::B_PF + 1], j & 1, wc, 4))) break;
-        tc_fence_after();
-        issue_pv(1, j);
-        umma_commit(&bars[C::B_VE + s]);
-        if (next_k) {
-          issue_s(1, j + 1);
-          umma_commit(&bars[C::B_KE + s1]);
+      } else {
+        ok = mbar_wait(&bars[C::B_KF], 0, wc, 3);
+        bool q0_ready = false, q1_ready = false;
+        auto wait_q = [&](int t, bool& ready) {  // Q_t lands once; wait before its first S
+          if (!ready) {
+            if (!mbar_wait(&bars[C::B_Q + t], 0, wc, 2)) return false;
+            ready = true;
+          }
+          tc_fence_after();
+          return true;
+        };
+        if (ok && ks0.has(first_kt) && (ok = wait_q(0, q0_ready))) issue_s(0, 0);
+        if (ok && ks1.has(first_kt) && (ok = wait_q(1, q1_ready))) issue_s(1, 0);
+        if (ok) umma_commit(&bars[C::B_KE]);
+        int n_pv0 = 0, n_pv1 = 0;
+        int j = 0;
+        for (int kt = first_kt; ok && kt != TileSet::kNone; ++j) {
+          const int s = j % C::NS, s1 = (j + 1) % C::NS;
+          const int kn = next_kt(kt);
+          const bool next_k = kn != TileSet::kNone;
+          const bool a0 = ks0.has(kt), a1 = ks1.has(kt);            // tiles taking part now
+          const bool n0 = next_k && ks0.has(kn), n1 = next_k && ks1.has(kn);  // and at the next position
+          if (!(ok = mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
+          if (next_k && !(ok = mbar_wait(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
+          // tile 0: P0 -> O0, then S0 of its next key tile over the consumed P0
+          if (a0) {
+            if (!(ok = mbar_wait(&bars[C::B_PF], n_pv0 & 1, wc, 4))) break;
+            tc_fence_after();
+            issue_pv(0, s, n_pv0 > 0);
+            ++n_pv0;
+          }
+          if (n0) {
+            if (!a0 || !q0_ready) {  // (after a P wait the fence is already done)
+              if (!(ok = wait_q(0, q0_ready))) break;
+            }
+            issue_s(0, s1);
+          }
+          // tile 1
+          if (a1) {
+            if (!(ok = mbar_wait(&bars[C::B_PF + 1], n_pv1 & 1, wc, 4))) break;
+            tc_fence_after();
+            issue_pv(1, s, n_pv1 > 0);
+            ++n_pv1;
+          }
+          umma_commit(&bars[C::B_VE + s]);
+          if (next_k) {
+            if (n1) {
+              if (!a1 || !q1_ready) {
+                if (!(ok = wait_q(1, q1_ready))) break;
+              }
+              issue_s(1, s1);
+            }
+            umma_commit(&bars[C::B_KE + s1]);
+          }
+          kt = kn;
         }
       }
       // Every MMA issued so far must complete before TMEM is freed.
@@ -277,15 +363,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int row = wq * 32 + lane;
     const int qt0 = q0 + t * C::BM;
     const int q_idx = qt0 + row;
-    const int n_kv = t == 0 ? n_kv0 : n_kv1;
+    const TileSet ks = t == 0 ? ks0 : ks1;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t t_s = t_lane + C::TMEM_S + t * 128;
     const uint32_t t_o = t_lane + C::TMEM_O + t * D;
     const float sl2 = p.scale_log2;
     float m = -INFINITY, l = 0.f, lr = 0.f;  // m: the max subtracted (base 2); l, lr: sums of p, bf16(p)
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!warp_wait(&bars[C::B_SF + t], j & 1, wc, 6)) {
+    const int n_kv_all = ks.count();
+    int n_kv = 0;  // key tiles processed
+    for (; n_kv < n_kv_all; ++n_kv) {
+      const int kt = LOCAL ? ks.at(n_kv) : n_kv;  // the plain masks visit [0, hi)
+      if (!warp_wait(&bars[C::B_SF + t], n_kv & 1, wc, 6)) {
         ok = false;
         break;
       }
@@ -298,16 +387,35 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       reg_tie(s[2]);
       reg_tie(s[3]);
 
-      // Mask keys past Nk and (causal) keys after this row's query index.
-      const bool need_mask = ((j + 1) * C::BN > sv.Nk) || (CAUSAL && (j * C::BN + C::BN - 1 > qt0));
+      // Mask keys past Nk, (causal) keys after this row's query index and (local) keys
+      // outside the window that are not global, unless the row is global.
+      const int ka = kt * C::BN;
+      bool need_mask = (ka + C::BN > sv.Nk) || (CAUSAL && (ka + C::BN - 1 > qt0));
+      if (LOCAL)
+        need_mask = need_mask || !(ka + C::BN <= p.lm.n_glob || qt0 + C::BM - 1 < p.lm.n_glob ||
+                                   (ka >= qt0 + C::BM - 1 - p.lm.win_l && ka + C::BN - 1 <= qt0 + p.lm.win_r));
       if (need_mask) {
-        int lim = sv.Nk - 1 - j * C::BN;  // last visible column of this tile
-        if (CAUSAL) lim = min(lim, q_idx - j * C::BN);
+        int lim = sv.Nk - 1 - ka;  // last visible column of this tile
+        if (CAUSAL) lim = min(lim, q_idx - ka);
+        if (!LOCAL) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
+          for (int g = 0; g < 4; ++g)
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (g * 32 + c > lim) s[g][c] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < 32; ++c)
+              if (g * 32 + c > lim) s[g][c] = __float_as_uint(-INFINITY);
+        } else {
+          // visible: c <= lim and (c < gc or wlo <= c <= whi)
+          const bool grow = q_idx < p.lm.n_glob;
+          const int gc = grow ? C::BN : p.lm.n_glob - ka;
+          const int wlo = q_idx - p.lm.win_l - ka, whi = q_idx + p.lm.win_r - ka;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int cc = g * 32 + c;
+              if (cc > lim || (cc >= gc && (cc < wlo || cc > whi))) s[g][c] = __float_as_uint(-INFINITY);
+            }
+        }
       }
       // row max: eight independent chains of 3-input max, then a short tree
       float mx8[8];
@@ -326,8 +434,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         alpha = ex2(m - mx2);
         m = mx2;
       }
-      // p = 2^(S*c - m) two lanes at a time; l and lr accumulate in packed pairs
-      const uint64_t c2 = f2pack(sl2, sl2), nm2 = f2pack(-m, -m);
+      // p = 2^(S*c - m) two lanes at a time; l and lr accumulate in packed pairs.  (Local
+      // mask: a row whose keys so far were all masked keeps m = -inf; subtract 0 instead.)
+      const float msub = (LOCAL && m == -INFINITY) ? 0.f : m;
+      const uint64_t c2 = f2pack(sl2, sl2), nm2 = f2pack(-msub, -msub);
       uint64_t l2[4], lr2[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) l2[i] = lr2[i] = 0ull;
@@ -357,7 +467,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 
       // O holds P V up to tile j-1 (S_t(j) was issued after PV_t(j-1), so it has landed);
       // rescale the rows whose subtracted max moved.
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      if (n_kv > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
         for (int g = 0; g < D / 16; ++g) {
           uint32_t o[16];
@@ -372,12 +482,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       tc_fence_before();
       mbar_arrive(&bars[C::B_PF + t]);
     }
-    if (ok && warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8)) {
+    if (ok && n_kv == 0) {  // this tile's rows see no key: O = 0, L = -inf
+      if (q_idx < sv.Nq) {
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + o_row(q_idx);
+        for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+        p.lse[lse_idx(q_idx)] = -INFINITY;
+      }
+    } else if (ok && warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8)) {
       tc_fence_after();
-      const float inv_l = 1.f / lr;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                            (VARLEN ? ((size_t)(sv.q_tok + q_idx) * p.va.H + sv.h) * D
-                                    : ((size_t)bh * sv.Nq + q_idx) * D);
+      // (local mask: a row with no visible key has lr = l = 0 and gets O = 0, L = -inf)
+      const float inv_l = (LOCAL && lr == 0.f) ? 0.f : 1.f / lr;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + o_row(q_idx);
 #pragma unroll
       for (int g = 0; g < D / 16; ++g) {
         uint32_t o[16];
@@ -398,8 +513,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         }
       }
       if (q_idx < sv.Nq)
-        p.lse[VARLEN ? (size_t)sv.h * p.va.total_q + sv.q_tok + q_idx : (size_t)bh * sv.Nq + q_idx] =
-            (m + log2f(l)) * 0.69314718055994530942f;
+        p.lse[lse_idx(q_idx)] = (LOCAL && l == 0.f) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
     }
   }
 
@@ -411,11 +525,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                      int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL, VARLEN>;
+  auto kern = fwd_kernel<D, CAUSAL, VARLEN, LOCAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH);
@@ -446,6 +560,9 @@ cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensor
                        const FwdParams& p, int BH, cudaStream_t st) {
 #define TA11_FWD_CASE(DD)                                                                          \
   case DD:                                                                                         \
+    if (p.local)                                                                                   \
+      return causal ? fwd::launch_t<DD, true, false, true>(tq, tk, tv, p, BH, st)                  \
+                    : fwd::launch_t<DD, false, false, true>(tq, tk, tv, p, BH, st);                \
     if (p.va.cu_q)                                                                                 \
       return causal ? fwd::launch_t<DD, true, true>(tq, tk, tv, p, BH, st)                         \
                     : fwd::launch_t<DD, false, true>(tq, tk, tv, p, BH, st);                       \

@@ -130,3 +130,4 @@ def flops_varlen(lens_q, lens_k, H: int, D: int, causal: bool, backward: bool = 
 # Packed batch of documents, 16384 tokens (the token count of the 4 x 4096 layer) with
 # 32 heads of D = 128, causal within each document.
 VARLEN_DOCS = dict(lens=doc_lengths(16384, seed=7), H=32, D=128, causal=True, factor=0.5)
+
