@@ -356,7 +356,7 @@ def run_table(args):
     print("| workload | fwd ms | fwd TFLOP/s | fwd % peak | bwd ms | bwd TFLOP/s | bwd % peak | fwd GB/s (% HBM) "
           "| step ms direct / CUDA graph | L2 flush |")
     print("|---|---|---|---|---|---|---|---|---|---|")
-    for p in ([] if args.varlen_only or args.window_only else I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]):
+    for p in ([] if args.varlen_only or args.window_only or args.fp8_only else I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]):
         q, k, v, do = (t.to(dev) for t in I.draw(p, 0))
         o = torch.empty_like(q)
         lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
@@ -408,10 +408,15 @@ def run_table(args):
               f"| {'yes' if small else 'no'} |", flush=True)
         del q, k, v, do, o, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()
+    if args.fp8_only:
+        _table_fp8(args, dev, sustained, hbm)
+        return
     if not args.window_only:
         _table_varlen(args, dev, sustained, hbm)
     if not args.varlen_only:
         _table_window(args, dev, sustained)
+    if not (args.window_only or args.varlen_only):
+        _table_fp8(args, dev, sustained, hbm)
 
 
 def window_pairs(Nq: int, Nk: int, causal: bool, window_left: int, window_right: int, n_global: int) -> int:
@@ -476,6 +481,47 @@ def _table_window(args, dev, sustained):
         print(f"| {name} | {res[0]:.4f} | {tf:.1f} | {100 * tf / sustained:.1f}% | {res[1]:.4f} | {tb:.1f} | "
               f"{100 * tb / sustained:.1f}% | {gbs:.0f} | {res[2]:.4f} / - | yes |", flush=True)
         del q, k, v, do, o, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+
+
+def _table_fp8(args, dev, sustained, hbm):
+    """FP8 forward rows: the e4m3 kernel alone (inputs quantised once), and the three
+    per-tensor quantisations; % of the e4m3 dense peak = 2 x the measured bf16 peak (the
+    nominal fp8 / bf16 ratio)."""
+    import torch
+    from tiled_attention_11_gb300 import _lib
+    from tiled_attention_11_gb300 import inputs as I
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for p in (I.LAYER, I.Problem(8, 1, 16384, 16384, 128, True), I.Problem(1, 8, 65537, 65537, 128, True)):
+        q, k, v, _ = (t.to(dev) for t in I.draw(p, 0))
+        q8, _, qd = _lib.quantize_e4m3(q)
+        k8, _, kd = _lib.quantize_e4m3(k)
+        vt8, ldv, _, vd = _lib.quantize_e4m3_transposed(v)
+        o = torch.empty_like(q)
+        lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
+        fwd = lambda: _lib.fa_fwd_fp8(q8, k8, vt8, ldv, qd, kd, vd, o, lse, p.causal, p.scale)  # noqa: E731
+        quant = lambda: (_lib.quantize_e4m3(q), _lib.quantize_e4m3(k), _lib.quantize_e4m3_transposed(v))  # noqa: E731
+        res = []
+        for fn in (fwd, quant):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(args.steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            res.append(statistics.median(ts))
+        tf = I.flops_fwd(p) / res[0] / 1e9
+        qbytes = 3 * q.numel() * (2 + 2 + 1)  # amax read, quantise read + 1-byte write, per tensor
+        print(f"| fp8 fwd {p.name()} | {res[0]:.4f} | {tf:.1f} | {100 * tf / (2 * sustained):.1f}% of e4m3 | "
+              f"quantise q,k,v {res[1]:.4f} ms ({qbytes / res[1] / 1e6:.0f} GB/s, {100 * qbytes / res[1] / 1e6 / hbm:.0f}% HBM) |",
+              flush=True)
+        del q, k, v, q8, k8, vt8, o, lse
         torch.cuda.empty_cache()
 
 
@@ -575,6 +621,7 @@ def main(argv=None):
     ap.add_argument("--table", action="store_true", help="time every workload, print a markdown table")
     ap.add_argument("--varlen-only", action="store_true", help="with --table: only the packed variable-length row")
     ap.add_argument("--window-only", action="store_true", help="with --table: only the local-window rows")
+    ap.add_argument("--fp8-only", action="store_true", help="with --table: only the FP8 forward rows")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.table:

@@ -143,6 +143,35 @@ int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, co
                   cudaStream_t stream);
 
 /*
+ * FP8 (e4m3) forward with per-tensor scales ([FA-hist] §5.3 names FP8 quantisation as the
+ * method's next direction).  e4m3 = 1 sign, 4 exponent (bias 7), 3 mantissa bits, no
+ * infinity, largest finite 448.  A tensor x is held as codes with one fp32 descale:
+ * x ~= descale * e4m3(code).
+ *
+ * fa_quantize_e4m3: bf16 x[n] -> codes[n] (same element order), with
+ *   amax = max|x|, codes = e4m3_rn_satfinite(x * (448 / amax)), descale = amax / 448
+ *   (fp32 IEEE division and product: the codes are fixed bit for bit); an all-zero x uses
+ *   multiplier and descale 1.  `amax` and `descale` are device floats written by the call
+ *   (amax is zeroed first on `stream`).  x and codes 16-byte aligned.
+ * fa_quantize_e4m3_transposed: bf16 [B,H,N,D] -> codes_t [B,H,D,ldt] (keys innermost, the
+ *   layout fa_fwd_fp8 takes for V), same rule with one scale for the whole tensor;
+ *   ldt >= N and a multiple of 16; bytes of a row past N may be left unwritten; D in {64, 128}.
+ * fa_fwd_fp8: O = softmax(scale * (qd*Q8)(kd*K8)^T) (vd*V8) and L as for fa_fwd, with
+ *   q8, k8 e4m3 [B,H,N,D], vt8 e4m3 [B,H,D,ldv] (ldv >= Nk, multiple of 16), descales as
+ *   device floats; O bf16 [B,H,Nq,D], L fp32 [B,H,Nq].  Both GEMMs run on e4m3 operands
+ *   with fp32 accumulation; P is rounded to e4m3, so O carries ~2-3% relative error on
+ *   diffuse rows (the e4m3 step is 2^-3 of a binade) and is exact up to bf16 rounding on a
+ *   row dominated by one key.  D in {64, 128}; causal as for fa_fwd.
+ * Ownership, asynchrony and error codes as for fa_fwd.
+ */
+int fa_quantize_e4m3(const void* x, long long n, void* codes, float* amax, float* descale, cudaStream_t stream);
+int fa_quantize_e4m3_transposed(const void* x, int B, int H, int N, int D, int ldt, void* codes_t, float* amax,
+                                float* descale, cudaStream_t stream);
+int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int ldv, const float* q_descale,
+               const float* k_descale, const float* v_descale, void* o, float* lse, int B, int H, int Nq, int Nk,
+               int D, float scale, int causal, cudaStream_t stream);
+
+/*
  * Variable-length ("ragged") batches ([FA2-impl] §7 names ragged inputs as the next step;
  * [FA-hist] §2.3 dynamic sequence lengths): B independent sequences packed back to back.
  *   q, o, dO, dq: [total_q, H, D] bf16;  k, v, dk, dv: [total_k, H, D] bf16 (D innermost)

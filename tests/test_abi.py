@@ -170,3 +170,24 @@ def test_window_validation_codes(L):
     need = L.fa_bwd_workspace_size(2, 3, 100, 77, 64)
     assert L.fa_bwd_window(*p[:9], 2, 3, 100, 77, 64, 0.125, 1, 16, -1, 4, p[9], need - 1, None) == _lib.FA_ERR_WORKSPACE
     assert L.fa_bwd_window(*p[:9], 2, 3, 100, 77, 64, 0.125, 1, 16, -1, 4, p[9], need, None) == _lib.FA_ERR_DEVICE
+
+
+def test_fp8_validation_codes(L):
+    vp = ctypes.c_void_p
+    q, k, vt, qd, kd, vd, o, lse = (vp(x) for x in ptrs(8))
+    call = lambda **kw: L.fa_fwd_fp8(q, k, vt, kw.get("ldv", 96), qd, kd, vd, kw.get("o", o), lse, 2, 3, 100,  # noqa: E731
+                                     kw.get("Nk", 90), kw.get("D", 128), 0.125, 1, None)
+    assert call(D=32) == _lib.FA_ERR_UNSUPPORTED_D
+    assert call(ldv=88) == _lib.FA_ERR_INVALID_ARG      # < Nk
+    assert call(ldv=100) == _lib.FA_ERR_INVALID_ARG     # not a multiple of 16
+    assert call(o=vp(0)) == _lib.FA_ERR_INVALID_ARG
+    assert call(o=vp(ptrs(1)[0] + 8)) == _lib.FA_ERR_MISALIGNED
+    assert call() == _lib.FA_ERR_DEVICE
+    x, c, a, d = (vp(v) for v in ptrs(4))
+    assert L.fa_quantize_e4m3(x, 0, c, a, d, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_quantize_e4m3(vp(ptrs(1)[0] + 2), 100, c, a, d, None) == _lib.FA_ERR_MISALIGNED
+    assert L.fa_quantize_e4m3(x, 100, x, a, d, None) == _lib.FA_ERR_INVALID_ARG  # codes overlap x
+    assert L.fa_quantize_e4m3(x, 100, c, a, d, None) == _lib.FA_ERR_DEVICE
+    assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 64, 100, c, a, d, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 48, 112, c, a, d, None) == _lib.FA_ERR_UNSUPPORTED_D
+    assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 64, 112, c, a, d, None) == _lib.FA_ERR_DEVICE

@@ -30,7 +30,8 @@ FA_ERR_SCRATCH_LIMIT = 8
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_device_status",
             "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
             "fa_graph_create", "fa_graph_launch", "fa_graph_destroy", "fa_fwd_varlen", "fa_bwd_varlen",
-            "fa_bwd_varlen_workspace_size", "fa_fwd_window", "fa_bwd_window")
+            "fa_bwd_varlen_workspace_size", "fa_fwd_window", "fa_bwd_window", "fa_quantize_e4m3",
+            "fa_quantize_e4m3_transposed", "fa_fwd_fp8")
 
 _lib = None
 
@@ -76,6 +77,12 @@ def lib() -> ctypes.CDLL:
     L.fa_graph_launch.restype = i
     L.fa_graph_destroy.argtypes = [vp]
     L.fa_graph_destroy.restype = None
+    L.fa_quantize_e4m3.argtypes = [vp, ctypes.c_longlong, vp, vp, vp, vp]
+    L.fa_quantize_e4m3.restype = i
+    L.fa_quantize_e4m3_transposed.argtypes = [vp, i, i, i, i, i, vp, vp, vp, vp]
+    L.fa_quantize_e4m3_transposed.restype = i
+    L.fa_fwd_fp8.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    L.fa_fwd_fp8.restype = i
     L.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp]
     L.fa_fwd_window.restype = i
     L.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp, sz, vp]
@@ -327,3 +334,59 @@ def fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, causal: bool, window_left: in
                              int(window_left), int(window_right), int(n_global),
                              _ptr(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(rc, "fa_bwd_window")
+
+
+# ----------------------------------------------------------------------------- FP8 (e4m3) forward
+def quantize_e4m3(x, stream=None):
+    """C ``fa_quantize_e4m3`` on a bf16 CUDA tensor: returns (codes uint8, like x; amax, descale:
+    one-element float32 CUDA tensors)."""
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    sc = torch.empty(2, dtype=torch.float32, device=x.device)
+    amax, descale = sc[0:1], sc[1:2]
+    rc = lib().fa_quantize_e4m3(_ptr(x, "x", torch.bfloat16), x.numel(), _ptr(codes, "codes", torch.uint8),
+                                amax.data_ptr(), descale.data_ptr(), _stream(stream))
+    _check(rc, "fa_quantize_e4m3")
+    return codes, amax, descale
+
+
+def quantize_e4m3_transposed(v, stream=None):
+    """C ``fa_quantize_e4m3_transposed`` on bf16 [B,H,N,D]: returns (codes_t uint8 [B,H,D,ldt],
+    ldt, amax, descale) with ldt = N rounded up to 16."""
+    B, H, N, D = v.shape
+    ldt = (N + 15) // 16 * 16
+    codes = torch.zeros((B, H, D, ldt), dtype=torch.uint8, device=v.device)
+    sc = torch.empty(2, dtype=torch.float32, device=v.device)
+    amax, descale = sc[0:1], sc[1:2]
+    rc = lib().fa_quantize_e4m3_transposed(_ptr(v, "v", torch.bfloat16), B, H, N, D, ldt,
+                                           _ptr(codes, "codes_t", torch.uint8), amax.data_ptr(),
+                                           descale.data_ptr(), _stream(stream))
+    _check(rc, "fa_quantize_e4m3_transposed")
+    return codes, ldt, amax, descale
+
+
+def fa_fwd_fp8(q8, k8, vt8, ldv: int, q_descale, k_descale, v_descale, o, lse, causal: bool,
+               scale: float | None = None, stream=None) -> None:
+    """C ``fa_fwd_fp8``: q8, k8 uint8 [B,H,N,D]; vt8 uint8 [B,H,D,ldv]; descales float32 CUDA scalars."""
+    B, H, Nq, D = q8.shape
+    Nk = k8.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib().fa_fwd_fp8(_ptr(q8, "q8", torch.uint8), _ptr(k8, "k8", torch.uint8), _ptr(vt8, "vt8", torch.uint8),
+                          int(ldv), _ptr(q_descale, "q_descale", torch.float32),
+                          _ptr(k_descale, "k_descale", torch.float32), _ptr(v_descale, "v_descale", torch.float32),
+                          _ptr(o, "o", torch.bfloat16), _ptr(lse, "lse", torch.float32), B, H, Nq, Nk, D,
+                          float(scale), int(bool(causal)), _stream(stream))
+    _check(rc, "fa_fwd_fp8")
+
+
+def forward_fp8(q, k, v, causal: bool, scale: float | None = None, stream=None):
+    """Quantise bf16 q, k, v per tensor (three kernels each side) and run the FP8 forward;
+    returns (o bf16, lse float32)."""
+    q8, _, qd = quantize_e4m3(q, stream)
+    k8, _, kd = quantize_e4m3(k, stream)
+    vt8, ldv, _, vd = quantize_e4m3_transposed(v, stream)
+    B, H, Nq, D = q.shape
+    o = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    fa_fwd_fp8(q8, k8, vt8, ldv, qd, kd, vd, o, lse, causal, scale, stream)
+    return o, lse

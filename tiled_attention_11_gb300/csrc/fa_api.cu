@@ -112,6 +112,22 @@ bool make_map_packed(CUtensorMap* m, const void* base, int D, int H, int total, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D tensor map over 1-byte elements: dims {inner, rows, BH}, row stride `ld` bytes,
+// box {inner (= the swizzle width, 64 or 128 bytes), box_rows, 1}.
+bool make_map_u8(CUtensorMap* m, const void* base, int inner, int rows, int BH, long long ld, int box_inner,
+                 int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const CUtensorMapSwizzle sw = box_inner == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)ld, (cuuint64_t)ld * rows};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct Range {
@@ -657,4 +673,81 @@ extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const 
   ta11::ConvParams cp{dq_accum, dq, B * H, max_seqlen_q, w.Nq_pad, scale, va};
   if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;
+}
+
+// ------------------------------------------------------------------------------------
+// FP8 (e4m3) forward and the per-tensor quantisation feeding it
+// ------------------------------------------------------------------------------------
+extern "C" int fa_quantize_e4m3(const void* x, long long n, void* codes, float* amax, float* descale,
+                                cudaStream_t stream) {
+  if (!x || !codes || !amax || !descale || n < 1) return FA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(amax, 4) || !aligned(descale, 4)) return FA_ERR_MISALIGNED;
+  const Range rx = rng(x, (size_t)n * 2), rc = rng(codes, (size_t)n), ra = rng(amax, 4), rd = rng(descale, 4);
+  if (overlap(rc, rx) || overlap(ra, rx) || overlap(rd, rx) || overlap(rc, ra) || overlap(rc, rd) || overlap(ra, rd))
+    return FA_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  int rc_dev = current_device(&status);
+  if (rc_dev != FA_OK) return rc_dev;
+  if (cudaMemsetAsync(amax, 0, 4, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (ta11::launch_amax_bf16(x, n, amax, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  return ta11::launch_quant_e4m3(x, n, amax, codes, descale, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+extern "C" int fa_quantize_e4m3_transposed(const void* x, int B, int H, int N, int D, int ldt, void* codes_t,
+                                           float* amax, float* descale, cudaStream_t stream) {
+  if (!x || !codes_t || !amax || !descale) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || (long long)B * H > 65535 || ldt < N || ldt % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
+  if (!aligned(x, 16) || !aligned(codes_t, 16) || !aligned(amax, 4) || !aligned(descale, 4)) return FA_ERR_MISALIGNED;
+  const size_t BH = (size_t)B * H;
+  const Range rx = rng(x, BH * N * D * 2), rc = rng(codes_t, BH * D * ldt), ra = rng(amax, 4), rd = rng(descale, 4);
+  if (overlap(rc, rx) || overlap(ra, rx) || overlap(rd, rx) || overlap(rc, ra) || overlap(rc, rd) || overlap(ra, rd))
+    return FA_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  int rc_dev = current_device(&status);
+  if (rc_dev != FA_OK) return rc_dev;
+  if (cudaMemsetAsync(amax, 0, 4, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (ta11::launch_amax_bf16(x, (long long)BH * N * D, amax, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  return ta11::launch_quant_e4m3_t(x, (int)BH, N, D, ldt, amax, codes_t, descale, stream) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_LAUNCH;
+}
+
+extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int ldv, const float* q_descale,
+                          const float* k_descale, const float* v_descale, void* o, float* lse, int B, int H, int Nq,
+                          int Nk, int D, float scale, int causal, cudaStream_t stream) {
+  if (!q8 || !k8 || !vt8 || !q_descale || !k_descale || !v_descale || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (long long)B * H > 65535) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
+  if (ldv < Nk || ldv % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(vt8, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(q_descale, 4) || !aligned(k_descale, 4) || !aligned(v_descale, 4))
+    return FA_ERR_MISALIGNED;
+  const size_t BH = (size_t)B * H;
+  const Range ins[] = {rng(q8, BH * Nq * D), rng(k8, BH * Nk * D), rng(vt8, BH * D * (size_t)ldv),
+                       rng(q_descale, 4), rng(k_descale, 4), rng(v_descale, 4)};
+  const Range ro = rng(o, BH * Nq * D * 2), rl = rng(lse, BH * Nq * 4);
+  for (const Range& in : ins)
+    if (overlap(ro, in) || overlap(rl, in)) return FA_ERR_INVALID_ARG;
+  if (overlap(ro, rl)) return FA_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_u8(&tq, q8, D, Nq, (int)BH, D, D, 128) || !make_map_u8(&tk, k8, D, Nk, (int)BH, D, D, 128) ||
+      !make_map_u8(&tv, vt8, Nk, D, (int)BH, ldv, 128, D))
+    return FA_ERR_LAUNCH;
+  ta11::Fp8FwdParams p{};
+  p.o = o;
+  p.lse = lse;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.scale_log2 = scale * kLog2e;
+  p.q_descale = q_descale;
+  p.k_descale = k_descale;
+  p.v_descale = v_descale;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.status = status;
+  return ta11::launch_fwd_fp8(D, causal != 0, tq, tk, tv, p, (int)BH, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }

@@ -141,6 +141,19 @@ struct ConvParams {
   VarlenArgs va;
 };
 
+// FP8 forward: e4m3 Q, K [BH][N][D], V^T [BH][D][ldv]; descales are device scalars.
+struct Fp8FwdParams {
+  void* o;              // bf16 [B,H,Nq,D]
+  float* lse;           // fp32 [B,H,Nq], natural log
+  int Nq, Nk;
+  float scale_log2;     // softmax scale * log2(e) (the Q and K descales are applied on top)
+  const float* q_descale;
+  const float* k_descale;
+  const float* v_descale;
+  unsigned long long wait_limit_ns;
+  unsigned* status;
+};
+
 // Host launchers (return cudaError_t of the launch).
 // Launchers; p.va.cu_q != nullptr selects the variable-length layout, p.local the
 // local-window + global-token mask (dense layout only).
@@ -150,6 +163,15 @@ cudaError_t launch_bwd_prep(int D, const PrepParams& p, cudaStream_t st);
 cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int BH, cudaStream_t st);
 cudaError_t launch_bwd_convert(int D, const ConvParams& p, cudaStream_t st);
+cudaError_t launch_fwd_fp8(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                           const Fp8FwdParams& p, int BH, cudaStream_t st);
+// Per-tensor e4m3 quantisation: amax (device float, zeroed by the caller's stream
+// order), then codes = e4m3(x * (448 / amax)) and descale = amax / 448.
+cudaError_t launch_amax_bf16(const void* x, long long n, float* amax, cudaStream_t st);
+cudaError_t launch_quant_e4m3(const void* x, long long n, const float* amax, void* codes, float* descale,
+                              cudaStream_t st);
+cudaError_t launch_quant_e4m3_t(const void* x, int BH, int N, int D, int ldt, const float* amax, void* codes_t,
+                                float* descale, cudaStream_t st);
 cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned* status, cudaStream_t st);
 
 }  // namespace ta11
