@@ -143,6 +143,22 @@ int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, co
                   cudaStream_t stream);
 
 /*
+ * One forward + backward step from host buffers: copies q, k, v, dO (host, bf16 [B,H,N,D];
+ * pinned memory for asynchronous copies) into `dev`, runs fa_fwd and fa_bwd there and
+ * copies o, lse, dq, dk, dv back to the host buffers, all asynchronously on `stream` (one
+ * cudaMemcpyAsync per tensor).  `dev` (256-byte aligned, dev_bytes >=
+ * fa_step_host_device_bytes(...)) holds the device copies and the backward workspace.
+ * Host buffers must stay valid and untouched until the stream reaches the end of the
+ * step.  Steps on different streams with separate `dev` buffers run concurrently, which
+ * lets one step's copies overlap another's kernels.  Errors as for fa_fwd / fa_bwd;
+ * FA_ERR_WORKSPACE for a missing, misaligned or short `dev`.
+ */
+size_t fa_step_host_device_bytes(int B, int H, int Nq, int Nk, int D);
+int fa_step_host(const void* q_h, const void* k_h, const void* v_h, const void* do_h, void* o_h, float* lse_h,
+                 void* dq_h, void* dk_h, void* dv_h, void* dev, size_t dev_bytes, int B, int H, int Nq, int Nk,
+                 int D, float scale, int causal, cudaStream_t stream);
+
+/*
  * FP8 (e4m3) forward with per-tensor scales ([FA-hist] §5.3 names FP8 quantisation as the
  * method's next direction).  e4m3 = 1 sign, 4 exponent (bias 7), 3 mantissa bits, no
  * infinity, largest finite 448.  A tensor x is held as codes with one fp32 descale:

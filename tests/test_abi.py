@@ -191,3 +191,17 @@ def test_fp8_validation_codes(L):
     assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 64, 100, c, a, d, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 48, 112, c, a, d, None) == _lib.FA_ERR_UNSUPPORTED_D
     assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 64, 112, c, a, d, None) == _lib.FA_ERR_DEVICE
+
+
+def test_step_host_validation_codes(L):
+    vp = ctypes.c_void_p
+    p = [vp(x) for x in ptrs(10)]
+    need = L.fa_step_host_device_bytes(2, 3, 100, 77, 64)
+    assert need > 0 and need % 256 == 0
+    assert L.fa_step_host_device_bytes(2, 3, 100, 77, 48) == 0
+    call = lambda dev=p[9], nbytes=need, D=64: L.fa_step_host(*p[:9], dev, nbytes, 2, 3, 100, 77, D, 0.125, 1, None)  # noqa: E731
+    assert call(dev=vp(0)) == _lib.FA_ERR_INVALID_ARG
+    assert call(D=48) == _lib.FA_ERR_UNSUPPORTED_D
+    assert call(nbytes=need - 1) == _lib.FA_ERR_WORKSPACE
+    assert call(dev=vp(ptrs(1)[0] + 16)) == _lib.FA_ERR_WORKSPACE
+    assert call() == _lib.FA_ERR_DEVICE

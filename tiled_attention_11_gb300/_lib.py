@@ -31,7 +31,8 @@ EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_devi
             "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
             "fa_graph_create", "fa_graph_launch", "fa_graph_destroy", "fa_fwd_varlen", "fa_bwd_varlen",
             "fa_bwd_varlen_workspace_size", "fa_fwd_window", "fa_bwd_window", "fa_quantize_e4m3",
-            "fa_quantize_e4m3_transposed", "fa_fwd_fp8")
+            "fa_quantize_e4m3_transposed", "fa_fwd_fp8", "fa_step_host",
+            "fa_step_host_device_bytes")
 
 _lib = None
 
@@ -77,6 +78,10 @@ def lib() -> ctypes.CDLL:
     L.fa_graph_launch.restype = i
     L.fa_graph_destroy.argtypes = [vp]
     L.fa_graph_destroy.restype = None
+    L.fa_step_host_device_bytes.argtypes = [i, i, i, i, i]
+    L.fa_step_host_device_bytes.restype = sz
+    L.fa_step_host.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, i, vp]
+    L.fa_step_host.restype = i
     L.fa_quantize_e4m3.argtypes = [vp, ctypes.c_longlong, vp, vp, vp, vp]
     L.fa_quantize_e4m3.restype = i
     L.fa_quantize_e4m3_transposed.argtypes = [vp, i, i, i, i, i, vp, vp, vp, vp]
@@ -390,3 +395,35 @@ def forward_fp8(q, k, v, causal: bool, scale: float | None = None, stream=None):
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     fa_fwd_fp8(q8, k8, vt8, ldv, qd, kd, vd, o, lse, causal, scale, stream)
     return o, lse
+
+
+# ----------------------------------------------------------------------------- host-buffer step
+def step_host_device_bytes(B: int, H: int, Nq: int, Nk: int, D: int) -> int:
+    return int(lib().fa_step_host_device_bytes(B, H, Nq, Nk, D))
+
+
+def _host_ptr(t: torch.Tensor, name: str, dtype) -> int:
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def step_host(q, k, v, do, o, lse, dq, dk, dv, dev_buf, causal: bool, scale: float | None = None,
+              stream=None) -> None:
+    """C ``fa_step_host``: host (pinned) bf16 [B,H,N,D] inputs / outputs, lse float32 [B,H,Nq];
+    dev_buf a uint8 CUDA tensor of step_host_device_bytes(...) bytes."""
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    bf = torch.bfloat16
+    rc = lib().fa_step_host(_host_ptr(q, "q", bf), _host_ptr(k, "k", bf), _host_ptr(v, "v", bf),
+                            _host_ptr(do, "do", bf), _host_ptr(o, "o", bf), _host_ptr(lse, "lse", torch.float32),
+                            _host_ptr(dq, "dq", bf), _host_ptr(dk, "dk", bf), _host_ptr(dv, "dv", bf),
+                            _ptr(dev_buf, "dev_buf", torch.uint8), dev_buf.numel(), B, H, Nq, Nk, D, float(scale),
+                            int(bool(causal)), _stream(stream))
+    _check(rc, "fa_step_host")

@@ -751,3 +751,72 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int l
   p.status = status;
   return ta11::launch_fwd_fp8(D, causal != 0, tq, tk, tv, p, (int)BH, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
+
+// ------------------------------------------------------------------------------------
+// One training step from pinned host buffers: copies in, forward, backward, copies out
+// ------------------------------------------------------------------------------------
+namespace {
+
+struct StepLayout {
+  size_t q, k, v, dO, o, lse, dq, dk, dv, ws, total;
+};
+
+StepLayout step_layout(int B, int H, int Nq, int Nk, int D) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t BH = (size_t)B * H, nq = up(BH * Nq * D * 2), nk = up(BH * Nk * D * 2), nl = up(BH * Nq * 4);
+  StepLayout L{};
+  size_t off = 0;
+  L.q = off; off += nq;
+  L.k = off; off += nk;
+  L.v = off; off += nk;
+  L.dO = off; off += nq;
+  L.o = off; off += nq;
+  L.lse = off; off += nl;
+  L.dq = off; off += nq;
+  L.dk = off; off += nk;
+  L.dv = off; off += nk;
+  L.ws = off; off += up(ws_layout(B, H, Nq, D).total);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+extern "C" size_t fa_step_host_device_bytes(int B, int H, int Nq, int Nk, int D) {
+  if (check_sizes(B, H, Nq, Nk, D, 1.f) != FA_OK) return 0;
+  return step_layout(B, H, Nq, Nk, D).total;
+}
+
+extern "C" int fa_step_host(const void* q_h, const void* k_h, const void* v_h, const void* do_h, void* o_h,
+                            float* lse_h, void* dq_h, void* dk_h, void* dv_h, void* dev, size_t dev_bytes, int B,
+                            int H, int Nq, int Nk, int D, float scale, int causal, cudaStream_t stream) {
+  if (!q_h || !k_h || !v_h || !do_h || !o_h || !lse_h || !dq_h || !dk_h || !dv_h || !dev) return FA_ERR_INVALID_ARG;
+  int rc = check_sizes(B, H, Nq, Nk, D, scale);
+  if (rc != FA_OK) return rc;
+  const StepLayout L = step_layout(B, H, Nq, Nk, D);
+  if (!aligned(dev, 256) || dev_bytes < L.total) return FA_ERR_WORKSPACE;
+  unsigned* status = nullptr;
+  rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  char* d = static_cast<char*>(dev);
+  const size_t BH = (size_t)B * H, nq = BH * Nq * D * 2, nk = BH * Nk * D * 2, nl = BH * Nq * 4;
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  if (cudaMemcpyAsync(d + L.q, q_h, nq, h2d, stream) != cudaSuccess ||
+      cudaMemcpyAsync(d + L.k, k_h, nk, h2d, stream) != cudaSuccess ||
+      cudaMemcpyAsync(d + L.v, v_h, nk, h2d, stream) != cudaSuccess ||
+      cudaMemcpyAsync(d + L.dO, do_h, nq, h2d, stream) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  rc = fa_fwd(d + L.q, d + L.k, d + L.v, d + L.o, reinterpret_cast<float*>(d + L.lse), B, H, Nq, Nk, D, scale,
+              causal, stream);
+  if (rc != FA_OK) return rc;
+  rc = fa_bwd(d + L.q, d + L.k, d + L.v, d + L.o, reinterpret_cast<float*>(d + L.lse), d + L.dO, d + L.dq,
+              d + L.dk, d + L.dv, B, H, Nq, Nk, D, scale, causal, d + L.ws, L.total - L.ws, stream);
+  if (rc != FA_OK) return rc;
+  if (cudaMemcpyAsync(o_h, d + L.o, nq, d2h, stream) != cudaSuccess ||
+      cudaMemcpyAsync(lse_h, d + L.lse, nl, d2h, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dq_h, d + L.dq, nq, d2h, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dk_h, d + L.dk, nk, d2h, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dv_h, d + L.dv, nk, d2h, stream) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  return FA_OK;
+}
