@@ -16,11 +16,15 @@
 //              dP^T = V dO_i^T           -> TMEM   dS^T = P^T o (dP^T - Dlt)
 //              dV  += P^T dO_i   (A = P^T from TMEM)
 //              dK  += dS^T Q_i   (A = dS^T from TMEM)
-//              dQ_i^T = K^T dS^T (A = K^T kept in TMEM, dS^T from shared memory) -> TMEM
-//            Issue order S(i+1) after dV(i) and dP(i+1) after dQ(i) keeps the tensor
-//            core busy while the compute warps work on the previous tile; a dQ
-//            warpgroup moves dQ_i^T from TMEM to shared memory and adds it into
-//            dq_accum with one TMA bulk reduce-add per tile.
+//              dQ_i^T = K^T dS^T (both from shared memory)          -> TMEM
+//            Two threads issue the UMMAs: one the score GEMMs S^T, dP^T (which need only
+//            loaded tiles and free TMEM), the other the gradient GEMMs dV, dK, dQ^T
+//            (which wait for the compute warps).  The tensor core keeps almost no queue,
+//            so a single issuing thread lets it run dry at every wait (~200 cycles each,
+//            measured); with two, one feeds it while the other waits.  S^T / P^T is
+//            double-buffered in TMEM so S(i+1) need not wait for dV(i).  A dQ warpgroup
+//            moves dQ_i^T from TMEM to shared memory and adds it into dq_accum with one
+//            TMA bulk reduce-add per tile.
 //   convert  dq = bf16(dq_accum * scale).
 #include "fa_kernels.h"
 #include "ptx_sm103a.cuh"
@@ -52,32 +56,36 @@ struct Cfg {
   static constexpr int OFF_STG = OFF_DLT + NS * BM * 4;  // dQ_i staging, fp32 [BM][D]
   static constexpr int STG_BYTES = BM * D * 4;
   static constexpr int OFF_BAR = OFF_STG + STG_BYTES;
-  // barriers
+  // barriers ([2]: one per S^T/P^T TMEM buffer or dS^T smem buffer, where one side can
+  // run two phases ahead of the other)
   static constexpr int B_KV = 0;
-  static constexpr int B_QF = 1;             // [NS]
-  static constexpr int B_QE = 1 + NS;        // [NS]
-  static constexpr int B_SF = 1 + 2 * NS;
-  static constexpr int B_DPF = 2 + 2 * NS;
-  static constexpr int B_PF = 3 + 2 * NS;
-  static constexpr int B_DSF = 4 + 2 * NS;
-  static constexpr int B_DQF = 5 + 2 * NS;   // [2] dQ^T MMA of a step done: its dS^T smem buffer is free
-  static constexpr int B_DQR = 7 + 2 * NS;   // dQ^T accumulator ready for the dQ warpgroup
-  static constexpr int B_DQE = 8 + 2 * NS;   // dQ^T accumulator drained
-  static constexpr int B_KT = 9 + 2 * NS;    // K^T written into TMEM
-  static constexpr int B_DRAIN = 10 + 2 * NS;
-  static constexpr int NBAR = 11 + 2 * NS;
+  static constexpr int B_QF = 1;             // [NS] Q, dO, lse2, Dlt stage loaded
+  static constexpr int B_QE = 1 + NS;        // [NS] stage free (dK, its last reader, done)
+  static constexpr int B_SF = 1 + 2 * NS;    // [2] S^T in TMEM buffer b
+  static constexpr int B_DPF = 3 + 2 * NS;   // dP^T in TMEM
+  static constexpr int B_PF = 4 + 2 * NS;    // [2] P^T in TMEM buffer b (compute warps)
+  static constexpr int B_DSF = 6 + 2 * NS;   // dS^T in TMEM and shared memory (compute warps)
+  static constexpr int B_DQF = 7 + 2 * NS;   // [2] dQ^T MMA of a step done: its dS^T smem buffer is free
+  static constexpr int B_DQR = 9 + 2 * NS;   // dQ^T accumulator ready for the dQ warpgroup
+  static constexpr int B_DQE = 10 + 2 * NS;  // dQ^T accumulator drained
+  static constexpr int B_DVD = 11 + 2 * NS;  // [2] dV of the step using S buffer b done (buffer free)
+  static constexpr int B_DKD = 13 + 2 * NS;  // dK done (dP^T / dS^T TMEM free)
+  static constexpr int B_DRAIN = 14 + 2 * NS;  // [2] one per issuing thread
+  static constexpr int NBAR = 16 + 2 * NS;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
-  // warps 0-3: dQ warpgroup, 4-11: two compute warpgroups, 12: TMA producer, 13: UMMA issuer
-  static constexpr int THREADS = 448;
-  static constexpr int W_PRODUCER = 12, W_MMA = 13;
-  // TMEM columns
-  // TMEM columns: S^T | dP^T | dQ^T | K^T (bf16 pairs, A operand of dQ^T) | dV | dK
-  static constexpr int T_S = 0, T_DP = 64, T_DQ = 128, T_KT = 192, T_DV = 256, T_DK = 256 + D;
+  // warps 0-3: dQ warpgroup, 4-11: two compute warpgroups, 12: TMA producer,
+  // 13: UMMA issuer for S^T, dP^T (and TMEM allocator), 14: UMMA issuer for dV, dK, dQ^T
+  static constexpr int THREADS = 480;
+  static constexpr int W_PRODUCER = 12, W_MMA_A = 13, W_MMA_B = 14;
+  // TMEM columns: S^T/P^T buffer 0 | buffer 1 | dP^T/dS^T | dQ^T | dV | dK
+  static constexpr int T_S = 0, T_DP = 128, T_DQ = 192, T_DV = 256, T_DK = 256 + D;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, BM, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
-  static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, false, true);   // dQ^T (A = K^T in TMEM, B MN-major)
+  // dQ^T: A = K^T, the K tile read MN-major (M = d; for D < 128 the rows d >= D read other
+  // tiles and are never used), B = dS^T MN-major
+  static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, true, true);
   static_assert(Q_TILE % 1024 == 0 && KV_TILE % 1024 == 0 && OFF_STG % 128 == 0, "alignment");
 };
 
@@ -166,19 +174,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(&bars[C::B_QF + s], 1);
       mbar_init(&bars[C::B_QE + s], 1);
     }
-    mbar_init(&bars[C::B_SF], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[C::B_SF + b], 1);
+      mbar_init(&bars[C::B_PF + b], 256);
+      mbar_init(&bars[C::B_DQF + b], 1);
+      mbar_init(&bars[C::B_DVD + b], 1);
+      mbar_init(&bars[C::B_DRAIN + b], 1);
+    }
     mbar_init(&bars[C::B_DPF], 1);
-    mbar_init(&bars[C::B_PF], 256);
     mbar_init(&bars[C::B_DSF], 256);
-    for (int b = 0; b < 2; ++b) mbar_init(&bars[C::B_DQF + b], 1);
     mbar_init(&bars[C::B_DQR], 1);
     mbar_init(&bars[C::B_DQE], 128);
-    mbar_init(&bars[C::B_KT], 128);
-    mbar_init(&bars[C::B_DRAIN], 1);
+    mbar_init(&bars[C::B_DKD], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == C::W_MMA) {
+  if (warp == C::W_MMA_A) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -225,85 +236,98 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           mbar_wait(&bars[C::B_QF + it % C::NS], (it / C::NS) & 1, w2, 41);
       }
     }
-  } else if (warp == C::W_MMA) {
-    // ---------------------------------------------------------------- UMMA issuer
-    if (lane == 0) {
-      // Base descriptors, built once; per-stage / per-slice variants are one add away.
+  } else if (warp == C::W_MMA_A) {
+    // ---------------------------------------------------------------- UMMA issuer A: S^T, dP^T
+    if (lane == 0 && n_it > 0) {
       const uint64_t dK = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);       // K, K-major
       const uint64_t dV = sdesc(sbase + C::OFF_V, 16, 8 * C::ROWB, C::LAYOUT);       // V, K-major
       const uint64_t dQk = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);      // Q stage 0, K-major
       const uint64_t dOk = sdesc(sbase + C::OFF_DO, 16, 8 * C::ROWB, C::LAYOUT);     // dO stage 0, K-major
-      const uint64_t dQm = sdesc(sbase + C::OFF_Q, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // MN-major
-      const uint64_t dOm = sdesc(sbase + C::OFF_DO, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);  // MN-major
-      const uint64_t dS0 = sdesc(sbase + C::OFF_DS, C::DS_BYTES, 1024, 2u);          // dS^T buffer 0, MN-major
-      auto issue_s = [&](int s) {  // S^T = K Q_s^T
-        const uint64_t q = desc_adv(dQk, (uint32_t)(s * C::Q_TILE));
+      auto issue_s = [&](int it) {  // S^T(it) = K Q^T into TMEM buffer it & 1
+        const uint64_t q = desc_adv(dQk, (uint32_t)((it % C::NS) * C::Q_TILE));
+        const uint32_t d = tmem + C::T_S + (uint32_t)((it & 1) * 64);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + C::T_S, desc_adv(dK, koff<D>(C::K_CHUNK_BYTES, kk)),
-                  desc_adv(q, koff<D>(C::Q_CHUNK_BYTES, kk)), C::IDESC_S, kk > 0 ? 1u : 0u);
-        umma_commit(&bars[C::B_SF]);
+          umma_ss(d, desc_adv(dK, koff<D>(C::K_CHUNK_BYTES, kk)), desc_adv(q, koff<D>(C::Q_CHUNK_BYTES, kk)),
+                  C::IDESC_S, kk > 0 ? 1u : 0u);
+        umma_commit(&bars[C::B_SF + (it & 1)]);
       };
-      auto issue_dp = [&](int s) {  // dP^T = V dO_s^T
-        const uint64_t o = desc_adv(dOk, (uint32_t)(s * C::Q_TILE));
+      auto issue_dp = [&](int it) {  // dP^T(it) = V dO^T
+        const uint64_t o = desc_adv(dOk, (uint32_t)((it % C::NS) * C::Q_TILE));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + C::T_DP, desc_adv(dV, koff<D>(C::K_CHUNK_BYTES, kk)),
-                  desc_adv(o, koff<D>(C::Q_CHUNK_BYTES, kk)), C::IDESC_S, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + C::T_DP, desc_adv(dV, koff<D>(C::K_CHUNK_BYTES, kk)), desc_adv(o, koff<D>(C::Q_CHUNK_BYTES, kk)),
+                  C::IDESC_S, kk > 0 ? 1u : 0u);
         umma_commit(&bars[C::B_DPF]);
       };
-      bool ok = n_it > 0 && mbar_wait(&bars[C::B_KV], 0, wc, 32) && mbar_wait(&bars[C::B_QF], 0, wc, 33);
+      bool ok = mbar_wait(&bars[C::B_KV], 0, wc, 32) && mbar_wait(&bars[C::B_QF], 0, wc, 33);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        issue_dp(0);
       }
       for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % C::NS;
-        const int s1 = (it + 1) % C::NS;
-        const bool more = it + 1 < n_it;
-        const uint64_t qm = desc_adv(dQm, (uint32_t)(s * C::Q_TILE));
-        const uint64_t om = desc_adv(dOm, (uint32_t)(s * C::Q_TILE));
-        // dV += P^T dO_i once P^T is in TMEM
-        if (!(ok = mbar_wait(&bars[C::B_PF], it & 1, wc, 34))) break;
+        // dP^T(it) overwrites dS^T(it-1) in TMEM once dK(it-1) has read it (its stage is
+        // loaded: S^T(it) waited for it)
+        if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DKD], (it - 1) & 1, wc, 35))) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          umma_ts(tmem + C::T_DV, tmem + C::T_S + a_col(kk), desc_adv(om, mnoff<D>(kk)), C::IDESC_KV,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-        // S^T of the next tile overwrites P^T only after dV has read it (in-order UMMA)
-        if (more) {
-          if (!(ok = mbar_wait(&bars[C::B_QF + s1], ((it + 1) / C::NS) & 1, wc, 35))) break;
+        issue_dp(it);
+        // S^T(it+1) goes to the buffer that held P^T(it-1): after dV(it-1) read it
+        if (it + 1 < n_it) {
+          const int s1 = (it + 1) % C::NS, b1 = (it + 1) & 1;
+          if (!(ok = mbar_wait(&bars[C::B_QF + s1], ((it + 1) / C::NS) & 1, wc, 33))) break;
+          if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DVD + b1], ((it - 1) >> 1) & 1, wc, 49))) break;
           tc_fence_after();
-          issue_s(s1);
+          issue_s(it + 1);
         }
-        // dK += dS^T Q_i once dS^T is in TMEM (and in shared memory for dQ)
-        if (!(ok = mbar_wait(&bars[C::B_DSF], it & 1, wc, 36))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars[C::B_QE + s]);
-        // dQ_i^T = K^T dS^T (A = K^T from TMEM) once the dQ warpgroup drained the last one
-        const int b = it & 1;
-        if (it == 0 && !(ok = mbar_wait(&bars[C::B_KT], 0, wc, 47))) break;
-        if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DQE], (it - 1) & 1, wc, 37))) break;
-        tc_fence_after();
-        const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts(tmem + C::T_DQ, tmem + C::T_KT + kk * 8, desc_adv(ds, (uint32_t)(kk * 16 * 128)), C::IDESC_DQ,
-                  kk > 0 ? 1u : 0u);
-        umma_commit(&bars[C::B_DQF + b]);
-        umma_commit(&bars[C::B_DQR]);
-        // dP^T of the next tile overwrites dS^T only after dK has read it
-        if (more) issue_dp(s1);
       }
       umma_commit(&bars[C::B_DRAIN]);
       volatile int no_abort = 0;
       const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
       mbar_wait(&bars[C::B_DRAIN], 0, w2, 42);
+    }
+  } else if (warp == C::W_MMA_B) {
+    // ---------------------------------------------------------------- UMMA issuer B: dV, dK, dQ^T
+    if (lane == 0 && n_it > 0) {
+      const uint64_t dQm = sdesc(sbase + C::OFF_Q, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // MN-major
+      const uint64_t dOm = sdesc(sbase + C::OFF_DO, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);  // MN-major
+      const uint64_t dKt = sdesc(sbase + C::OFF_K, C::K_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // K^T, MN-major
+      const uint64_t dS0 = sdesc(sbase + C::OFF_DS, C::DS_BYTES, 1024, 2u);          // dS^T buffer 0, MN-major
+      bool ok = mbar_wait(&bars[C::B_KV], 0, wc, 32);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % C::NS, b = it & 1;
+        const uint64_t qm = desc_adv(dQm, (uint32_t)(s * C::Q_TILE));
+        const uint64_t om = desc_adv(dOm, (uint32_t)(s * C::Q_TILE));
+        // dV += P^T dO_i once P^T(it) is in TMEM buffer b
+        if (!(ok = mbar_wait(&bars[C::B_PF + b], (it >> 1) & 1, wc, 34))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          umma_ts(tmem + C::T_DV, tmem + C::T_S + (uint32_t)(b * 64) + a_col(kk), desc_adv(om, mnoff<D>(kk)),
+                  C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[C::B_DVD + b]);
+        // dK += dS^T Q_i and dQ_i^T = K^T dS^T once dS^T is in TMEM and shared memory
+        // and the dQ warpgroup drained the last dQ^T
+        if (!(ok = mbar_wait(&bars[C::B_DSF], it & 1, wc, 36))) break;
+        if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DQE], (it - 1) & 1, wc, 37))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[C::B_DKD]);
+        umma_commit(&bars[C::B_QE + s]);  // dK was the stage's last reader
+        const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          umma_ss(tmem + C::T_DQ, desc_adv(dKt, (uint32_t)(kk * 16 * C::ROWB)), desc_adv(ds, (uint32_t)(kk * 16 * 128)),
+                  C::IDESC_DQ, kk > 0 ? 1u : 0u);
+        umma_commit(&bars[C::B_DQF + b]);
+        umma_commit(&bars[C::B_DQR]);
+      }
+      umma_commit(&bars[C::B_DRAIN + 1]);
+      volatile int no_abort = 0;
+      const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+      mbar_wait(&bars[C::B_DRAIN + 1], 0, w2, 42);
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- compute warpgroups
@@ -320,13 +344,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     for (int it = 0; it < n_it && ok; ++it) {
       const int s = it % C::NS;
       const int i = qs.at(it);
-      if (!warp_wait(&bars[C::B_QF + s], (it / C::NS) & 1, wc, 38) || !warp_wait(&bars[C::B_SF], it & 1, wc, 39)) {
+      const uint32_t t_sb = (uint32_t)((it & 1) * 64);  // this step's S^T / P^T buffer
+      if (!warp_wait(&bars[C::B_QF + s], (it / C::NS) & 1, wc, 38) ||
+          !warp_wait(&bars[C::B_SF + (it & 1)], (it >> 1) & 1, wc, 39)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sreg[32];
-      tmem_ld32(t_lane + C::T_S + col0, sreg);
+      tmem_ld32(t_lane + C::T_S + t_sb + col0, sreg);
       tmem_wait_ld(sreg);
       const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * C::BM * 4) + col0;
       const float* dlt = reinterpret_cast<const float*>(smem + C::OFF_DLT + s * C::BM * 4) + col0;
@@ -353,10 +379,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       uint32_t pk[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
-      tmem_st16(t_lane + C::T_S + wg * 32, pk);
+      tmem_st16(t_lane + C::T_S + t_sb + wg * 32, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars[C::B_PF]);
+      mbar_arrive(&bars[C::B_PF + (it & 1)]);
 
       if (!warp_wait(&bars[C::B_DPF], it & 1, wc, 43)) {
         ok = false;
@@ -416,34 +442,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int d = warp * 32 + lane;  // TMEM lane = row d of dQ^T
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
     float* stg = reinterpret_cast<float*>(smem + C::OFF_STG);
-    // K^T into TMEM once per CTA: lane d holds K[key][d] for all 128 keys as bf16 pairs
-    // (the A operand of dQ^T = K^T dS^T).  Lanes d >= D (D < 128) hold zeros.
-    bool ok = n_it > 0 && named_bar_and(1, 128, warp_wait(&bars[C::B_KV], 0, wc, 48));
-    if (ok) {
-      const uint8_t* sK = smem + C::OFF_K;
-      const int dc = d < D ? d : 0;
-      const int chunk = dc / C::CHUNK, col = dc % C::CHUNK;
-      const uint8_t* base = sK + chunk * C::K_CHUNK_BYTES + (col % 8) * 2;
-      const int u = col / 8;
-      uint32_t kt[2][32];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        uint32_t pr = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = 2 * c + h;  // key row of the swizzled K-major tile
-          const int phys = u ^ ((r * C::ROWB >> 7) & (C::ROWB / 16 - 1));
-          const uint32_t e = *reinterpret_cast<const uint16_t*>(base + r * C::ROWB + phys * 16);
-          pr |= (d < D ? e : 0u) << (16 * h);
-        }
-        kt[c >> 5][c & 31] = pr;
-      }
-      tmem_st32(t_lane + C::T_KT, kt[0]);
-      tmem_st32(t_lane + C::T_KT + 32, kt[1]);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars[C::B_KT]);
-    }
+    bool ok = n_it > 0;
     for (int it = 0; ok && it < n_it; ++it) {
       // the four warps agree before any of them reaches the named barriers below
       if (!named_bar_and(1, 128, warp_wait(&bars[C::B_DQR], it & 1, wc, 46))) break;
@@ -477,7 +476,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == C::W_MMA) {
+  if (warp == C::W_MMA_A) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
