@@ -16,15 +16,18 @@
 //              dP^T = V dO_i^T           -> TMEM   dS^T = P^T o (dP^T - Dlt)
 //              dV  += P^T dO_i   (A = P^T from TMEM)
 //              dK  += dS^T Q_i   (A = dS^T from TMEM)
-//              dQ_i^T = K^T dS^T (both from shared memory)          -> TMEM
+//              dQ_i^T = K^T dS^T (A = K^T kept in TMEM, dS^T from shared memory)
+//                                   -> TMEM, into the S^T buffer dV has just consumed
 //            Two threads issue the UMMAs: one the score GEMMs S^T, dP^T (which need only
 //            loaded tiles and free TMEM), the other the gradient GEMMs dV, dK, dQ^T
 //            (which wait for the compute warps).  The tensor core keeps almost no queue,
 //            so a single issuing thread lets it run dry at every wait (~200 cycles each,
 //            measured); with two, one feeds it while the other waits.  S^T / P^T is
-//            double-buffered in TMEM so S(i+1) need not wait for dV(i).  A dQ warpgroup
-//            moves dQ_i^T from TMEM to shared memory and adds it into dq_accum with one
-//            TMA bulk reduce-add per tile.
+//            double-buffered in TMEM so S(i+1) need not wait for dV(i); dQ_i^T reuses
+//            step i's buffer, and S(i+2) waits until the dQ warpgroup has moved dQ_i^T
+//            from TMEM to shared memory and added it into dq_accum (one TMA bulk
+//            reduce-add per tile).  Shared-memory bandwidth is the next limit (~290 KB
+//            per step against 128 B/cycle), which is why K^T is kept in TMEM.
 //   convert  dq = bf16(dq_accum * scale).
 #include "fa_kernels.h"
 #include "ptx_sm103a.cuh"
@@ -66,26 +69,24 @@ struct Cfg {
   static constexpr int B_PF = 4 + 2 * NS;    // [2] P^T in TMEM buffer b (compute warps)
   static constexpr int B_DSF = 6 + 2 * NS;   // dS^T in TMEM and shared memory (compute warps)
   static constexpr int B_DQF = 7 + 2 * NS;   // [2] dQ^T MMA of a step done: its dS^T smem buffer is free
-  static constexpr int B_DQR = 9 + 2 * NS;   // dQ^T accumulator ready for the dQ warpgroup
-  static constexpr int B_DQE = 10 + 2 * NS;  // dQ^T accumulator drained
-  static constexpr int B_DVD = 11 + 2 * NS;  // [2] dV of the step using S buffer b done (buffer free)
-  static constexpr int B_DKD = 13 + 2 * NS;  // dK done (dP^T / dS^T TMEM free)
-  static constexpr int B_DRAIN = 14 + 2 * NS;  // [2] one per issuing thread
-  static constexpr int NBAR = 16 + 2 * NS;
+  static constexpr int B_DQR = 9 + 2 * NS;   // [2] dQ^T in TMEM buffer b, ready for the dQ warpgroup
+  static constexpr int B_DQE = 11 + 2 * NS;  // [2] dQ^T drained from TMEM buffer b (buffer free)
+  static constexpr int B_KT = 13 + 2 * NS;   // K^T written into TMEM
+  static constexpr int B_DKD = 14 + 2 * NS;  // dK done (dP^T / dS^T TMEM free)
+  static constexpr int B_DRAIN = 15 + 2 * NS;  // [2] one per issuing thread
+  static constexpr int NBAR = 17 + 2 * NS;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
   // warps 0-3: dQ warpgroup, 4-11: two compute warpgroups, 12: TMA producer,
   // 13: UMMA issuer for S^T, dP^T (and TMEM allocator), 14: UMMA issuer for dV, dK, dQ^T
   static constexpr int THREADS = 480;
   static constexpr int W_PRODUCER = 12, W_MMA_A = 13, W_MMA_B = 14;
-  // TMEM columns: S^T/P^T buffer 0 | buffer 1 | dP^T/dS^T | dQ^T | dV | dK
-  static constexpr int T_S = 0, T_DP = 128, T_DQ = 192, T_DV = 256, T_DK = 256 + D;
+  // TMEM columns: S^T/P^T/dQ^T buffer 0 | buffer 1 | dP^T/dS^T | K^T (bf16 pairs) | dV | dK
+  static constexpr int T_S = 0, T_DP = 128, T_KT = 192, T_DV = 256, T_DK = 256 + D;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, BM, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
-  // dQ^T: A = K^T, the K tile read MN-major (M = d; for D < 128 the rows d >= D read other
-  // tiles and are never used), B = dS^T MN-major
-  static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, true, true);
+  static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, false, true);   // dQ^T (A = K^T in TMEM, B MN-major)
   static_assert(Q_TILE % 1024 == 0 && KV_TILE % 1024 == 0 && OFF_STG % 128 == 0, "alignment");
 };
 
@@ -178,13 +179,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(&bars[C::B_SF + b], 1);
       mbar_init(&bars[C::B_PF + b], 256);
       mbar_init(&bars[C::B_DQF + b], 1);
-      mbar_init(&bars[C::B_DVD + b], 1);
+      mbar_init(&bars[C::B_DQR + b], 1);
+      mbar_init(&bars[C::B_DQE + b], 128);
       mbar_init(&bars[C::B_DRAIN + b], 1);
     }
     mbar_init(&bars[C::B_DPF], 1);
     mbar_init(&bars[C::B_DSF], 256);
-    mbar_init(&bars[C::B_DQR], 1);
-    mbar_init(&bars[C::B_DQE], 128);
+    mbar_init(&bars[C::B_KT], 128);
     mbar_init(&bars[C::B_DKD], 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -271,11 +272,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DKD], (it - 1) & 1, wc, 35))) break;
         tc_fence_after();
         issue_dp(it);
-        // S^T(it+1) goes to the buffer that held P^T(it-1): after dV(it-1) read it
+        // S^T(it+1) goes to the buffer that held P^T(it-1), then dQ^T(it-1): after the dQ
+        // warpgroup drained it (which follows dV(it-1) and dQ^T(it-1) in issuer B's order)
         if (it + 1 < n_it) {
           const int s1 = (it + 1) % C::NS, b1 = (it + 1) & 1;
           if (!(ok = mbar_wait(&bars[C::B_QF + s1], ((it + 1) / C::NS) & 1, wc, 33))) break;
-          if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DVD + b1], ((it - 1) >> 1) & 1, wc, 49))) break;
+          if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DQE + b1], ((it - 1) >> 1) & 1, wc, 49))) break;
           tc_fence_after();
           issue_s(it + 1);
         }
@@ -290,7 +292,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     if (lane == 0 && n_it > 0) {
       const uint64_t dQm = sdesc(sbase + C::OFF_Q, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // MN-major
       const uint64_t dOm = sdesc(sbase + C::OFF_DO, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);  // MN-major
-      const uint64_t dKt = sdesc(sbase + C::OFF_K, C::K_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // K^T, MN-major
       const uint64_t dS0 = sdesc(sbase + C::OFF_DS, C::DS_BYTES, 1024, 2u);          // dS^T buffer 0, MN-major
       bool ok = mbar_wait(&bars[C::B_KV], 0, wc, 32);
       for (int it = 0; ok && it < n_it; ++it) {
@@ -304,11 +305,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         for (int kk = 0; kk < C::BM / 16; ++kk)
           umma_ts(tmem + C::T_DV, tmem + C::T_S + (uint32_t)(b * 64) + a_col(kk), desc_adv(om, mnoff<D>(kk)),
                   C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars[C::B_DVD + b]);
         // dK += dS^T Q_i and dQ_i^T = K^T dS^T once dS^T is in TMEM and shared memory
-        // and the dQ warpgroup drained the last dQ^T
         if (!(ok = mbar_wait(&bars[C::B_DSF], it & 1, wc, 36))) break;
-        if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DQE], (it - 1) & 1, wc, 37))) break;
+        if (it == 0 && !(ok = mbar_wait(&bars[C::B_KT], 0, wc, 47))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
@@ -316,13 +315,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                   (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&bars[C::B_DKD]);
         umma_commit(&bars[C::B_QE + s]);  // dK was the stage's last reader
+        // dQ^T(it) into buffer b, which dV(it) (issued above: in-order) has finished reading
         const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ss(tmem + C::T_DQ, desc_adv(dKt, (uint32_t)(kk * 16 * C::ROWB)), desc_adv(ds, (uint32_t)(kk * 16 * 128)),
+          umma_ts(tmem + C::T_S + (uint32_t)(b * 64), tmem + C::T_KT + kk * 8, desc_adv(ds, (uint32_t)(kk * 16 * 128)),
                   C::IDESC_DQ, kk > 0 ? 1u : 0u);
         umma_commit(&bars[C::B_DQF + b]);
-        umma_commit(&bars[C::B_DQR]);
+        umma_commit(&bars[C::B_DQR + b]);
       }
       umma_commit(&bars[C::B_DRAIN + 1]);
       volatile int no_abort = 0;
@@ -442,18 +442,46 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int d = warp * 32 + lane;  // TMEM lane = row d of dQ^T
     const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
     float* stg = reinterpret_cast<float*>(smem + C::OFF_STG);
-    bool ok = n_it > 0;
+    // K^T into TMEM once per CTA: lane d holds K[key][d] for all 128 keys as bf16 pairs
+    // (the A operand of dQ^T = K^T dS^T).  Lanes d >= D (D < 128) hold zeros.
+    bool ok = n_it > 0 && named_bar_and(1, 128, warp_wait(&bars[C::B_KV], 0, wc, 48));
+    if (ok) {
+      const uint8_t* sK = smem + C::OFF_K;
+      const int dc = d < D ? d : 0;
+      const int chunk = dc / C::CHUNK, col = dc % C::CHUNK;
+      const uint8_t* base = sK + chunk * C::K_CHUNK_BYTES + (col % 8) * 2;
+      const int u = col / 8;
+      uint32_t kt[2][32];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        uint32_t pr = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = 2 * c + h;  // key row of the swizzled K-major tile
+          const int phys = u ^ ((r * C::ROWB >> 7) & (C::ROWB / 16 - 1));
+          const uint32_t e = *reinterpret_cast<const uint16_t*>(base + r * C::ROWB + phys * 16);
+          pr |= (d < D ? e : 0u) << (16 * h);
+        }
+        kt[c >> 5][c & 31] = pr;
+      }
+      tmem_st32(t_lane + C::T_KT, kt[0]);
+      tmem_st32(t_lane + C::T_KT + 32, kt[1]);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_KT]);
+    }
     for (int it = 0; ok && it < n_it; ++it) {
+      const int b = it & 1;
       // the four warps agree before any of them reaches the named barriers below
-      if (!named_bar_and(1, 128, warp_wait(&bars[C::B_DQR], it & 1, wc, 46))) break;
+      if (!named_bar_and(1, 128, warp_wait(&bars[C::B_DQR + b], (it >> 1) & 1, wc, 46))) break;
       tc_fence_after();
       uint32_t v0[32], v1[32];
-      tmem_ld32(t_lane + C::T_DQ, v0);
-      tmem_ld32(t_lane + C::T_DQ + 32, v1);
+      tmem_ld32(t_lane + C::T_S + (uint32_t)(b * 64), v0);
+      tmem_ld32(t_lane + C::T_S + (uint32_t)(b * 64) + 32, v1);
       tmem_wait_ld(v0);
       reg_tie(v1);
       tc_fence_before();
-      mbar_arrive(&bars[C::B_DQE]);
+      mbar_arrive(&bars[C::B_DQE + b]);
       // the previous bulk reduce must have finished reading the staging buffer
       if (threadIdx.x == 0) bulk_wait_read_all();
       named_bar_sync(1, 128);
