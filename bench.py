@@ -425,7 +425,7 @@ def run_table(args):
         print(f"| {p.name()} | {res[0]:.4f} | {tf:.1f} | {100 * tf / sustained:.1f}% | {res[1]:.4f} | {tb:.1f} | "
               f"{100 * tb / sustained:.1f}% | {gbs:.0f} ({100 * gbs / hbm:.1f}%) | {steps[0]:.4f} / {steps[1]:.4f} "
               f"| {'yes' if small else 'no'} |", flush=True)
-        del q, k, v, do, o, lse, dq, dk, dv, ws
+        del q, k, v, do, o, lse, dq, dk, dv, ws, fws
         torch.cuda.empty_cache()
     if args.fp8_only:
         _table_fp8(args, dev, sustained, hbm)
@@ -475,8 +475,10 @@ def _table_window(args, dev, sustained):
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws = torch.empty(_lib.fa_bwd_workspace_size(B, H, N, N, D), dtype=torch.uint8, device=dev)
-        fwd = lambda: _lib.fa_fwd_window(q, k, v, o, lse, causal, wl, wr, g, p.scale)  # noqa: E731
+        ws = torch.empty(_lib.fa_bwd_window_workspace_size(B, H, N, N, D, wl, wr, g), dtype=torch.uint8, device=dev)
+        fws = torch.empty(max(_lib.fa_fwd_window_workspace_size(B, H, N, N, D, causal, wl, wr, g), 256),
+                          dtype=torch.uint8, device=dev)
+        fwd = lambda: _lib.fa_fwd_window(q, k, v, o, lse, causal, wl, wr, g, p.scale, workspace=fws)  # noqa: E731
         bwd = lambda: _lib.fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, causal, wl, wr, g, p.scale,  # noqa: E731
                                          workspace=ws)
         res = []
@@ -499,7 +501,7 @@ def _table_window(args, dev, sustained):
         name = f"window B{B}H{H}N{N}D{D}{'c' if causal else 'n'} wl{wl} wr{wr} g{g}"
         print(f"| {name} | {res[0]:.4f} | {tf:.1f} | {100 * tf / sustained:.1f}% | {res[1]:.4f} | {tb:.1f} | "
               f"{100 * tb / sustained:.1f}% | {gbs:.0f} | {res[2]:.4f} / - | yes |", flush=True)
-        del q, k, v, do, o, lse, dq, dk, dv, ws
+        del q, k, v, do, o, lse, dq, dk, dv, ws, fws
         torch.cuda.empty_cache()
 
 

@@ -134,9 +134,23 @@ void fa_set_bwd_main_events(cudaEvent_t begin, cudaEvent_t end);
  * Layout, workspace (fa_bwd_workspace_size), ownership, asynchrony and errors as for
  * fa_fwd / fa_bwd.
  */
+/* Without the causal condition the global query rows see every key; when the key range is
+ * long (> 32 key tiles) their query tiles are split over chunks of 16 key tiles whose partial
+ * results (unnormalised O, running maximum and sums) go to `workspace` and are merged by a
+ * second kernel.  fa_fwd_window_workspace_size gives the bytes (0 when no split is needed;
+ * workspace may then be null); workspace 256-byte aligned, caller-owned, FA_ERR_WORKSPACE
+ * when missing or short. */
+size_t fa_fwd_window_workspace_size(int B, int H, int Nq, int Nk, int D, int causal, int window_left,
+                                    int window_right, int n_global);
 int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-                  int D, float scale, int causal, int window_left, int window_right, int n_global,
-                  cudaStream_t stream);
+                  int D, float scale, int causal, int window_left, int window_right, int n_global, void* workspace,
+                  size_t workspace_bytes, cudaStream_t stream);
+/* Key tiles that hold global keys are seen by every (later) query; when the query range is
+ * long (> 64 steps of 64 queries) they are split over chunks of 32 steps whose partial dK, dV
+ * go to an fp32 area after the usual workspace and are written out by a final kernel.
+ * fa_bwd_window_workspace_size gives the bytes (>= fa_bwd_workspace_size). */
+size_t fa_bwd_window_workspace_size(int B, int H, int Nq, int Nk, int D, int window_left, int window_right,
+                                    int n_global);
 int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                   void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal,
                   int window_left, int window_right, int n_global, void* workspace, size_t workspace_bytes,

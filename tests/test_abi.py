@@ -159,7 +159,7 @@ def test_window_validation_codes(L):
     vp = ctypes.c_void_p
     q, k, v, o, lse = (vp(x) for x in ptrs(5))
     call = lambda **kw: L.fa_fwd_window(kw.get("q", q), k, v, o, lse, 2, 3, 100, 77, kw.get("D", 64), 0.125, 1,  # noqa: E731
-                                        kw.get("wl", 16), -1, kw.get("g", 4), None)
+                                        kw.get("wl", 16), -1, kw.get("g", 4), None, 0, None)
     assert call(q=vp(0)) == _lib.FA_ERR_INVALID_ARG
     assert call(D=48) == _lib.FA_ERR_UNSUPPORTED_D
     assert call(q=vp(ptrs(1)[0] + 8)) == _lib.FA_ERR_MISALIGNED
@@ -205,3 +205,37 @@ def test_step_host_validation_codes(L):
     assert call(nbytes=need - 1) == _lib.FA_ERR_WORKSPACE
     assert call(dev=vp(ptrs(1)[0] + 16)) == _lib.FA_ERR_WORKSPACE
     assert call() == _lib.FA_ERR_DEVICE
+
+
+def test_window_split_workspace(L):
+    vp = ctypes.c_void_p
+    # causal or short key ranges need no split; non-causal long ones with global tokens do
+    assert L.fa_fwd_window_workspace_size(1, 2, 8192, 8192, 64, 1, 256, -1, 64) == 0
+    assert L.fa_fwd_window_workspace_size(1, 2, 4000, 4000, 64, 0, 256, 256, 64) == 0   # 32 key tiles
+    need = L.fa_fwd_window_workspace_size(1, 2, 5000, 5000, 64, 0, 100, 100, 40)
+    # 1 global pair x 256 rows x 3 chunks of 16 key tiles: O (64 fp32) and 4 floats per record
+    recs = 2 * 256 * 3
+    assert need == (recs * 64 * 4 + 255) // 256 * 256 + (recs * 16 + 255) // 256 * 256
+    assert L.fa_fwd_window_workspace_size(1, 2, 5000, 5000, 64, 0, 100, 100, 0) == 0   # no global tokens
+    q, k, v, o, lse, ws = (vp(x) for x in ptrs(6))
+    args = (q, k, v, o, lse, 1, 2, 5000, 5000, 64, 0.125, 0, 100, 100, 40)
+    assert L.fa_fwd_window(*args, None, 0, None) == _lib.FA_ERR_WORKSPACE
+    assert L.fa_fwd_window(*args, ws, need - 1, None) == _lib.FA_ERR_WORKSPACE
+    assert L.fa_fwd_window(*args, vp(ptrs(6)[5] + 16), need, None) == _lib.FA_ERR_WORKSPACE  # misaligned
+    assert L.fa_fwd_window(*args, ws, need, None) == _lib.FA_ERR_DEVICE
+
+
+def test_window_bwd_split_workspace(L):
+    base = L.fa_bwd_workspace_size(1, 2, 5000, 5000, 64)
+    assert L.fa_bwd_window_workspace_size(1, 2, 5000, 5000, 64, 100, 100, 0) == base     # no global tokens
+    assert L.fa_bwd_window_workspace_size(1, 2, 4000, 4000, 64, 100, 100, 40) == \
+        L.fa_bwd_workspace_size(1, 2, 4000, 4000, 64)                                      # 63 query steps
+    # 5000 queries = 79 steps > 64: one global key tile, dK and dV rows of 64 fp32
+    assert L.fa_bwd_window_workspace_size(1, 2, 5000, 5000, 64, 100, 100, 40) == base + (2 * 128 * 2 * 64 * 4)
+    need = base + 2 * 128 * 2 * 64 * 4
+    vp = ctypes.c_void_p
+    p = [vp(x) for x in ptrs(10)]
+    args = (*p[:9], 1, 2, 5000, 5000, 64, 0.125, 0, 100, 100, 40, p[9])
+    assert L.fa_bwd_window(*args, base, None) == _lib.FA_ERR_WORKSPACE      # split area missing
+    assert L.fa_bwd_window(*args, need - 1, None) == _lib.FA_ERR_WORKSPACE
+    assert L.fa_bwd_window(*args, need, None) == _lib.FA_ERR_DEVICE

@@ -188,3 +188,45 @@ def test_long_window_sampled():
     dkl, dvl, dol = dk.double().cpu(), dv.double().cpu(), do.double()
     assert ((dkl.sum(2).abs() / dkl.abs().sum(2).clamp_min(1e-30)).max() < 5e-3)
     assert (((dvl.sum(2) - dol.sum(2)).abs() / dol.abs().sum(2).clamp_min(1e-30)).max() < 5e-3)
+
+
+SPLIT_CASES = [
+    # non-causal, global tokens, key range > 32 tiles: the global query tiles split into
+    # chunks of 16 key tiles and merged (rows of the same tiles that are not global see
+    # nothing in far chunks)
+    (I.Problem(1, 2, 5000, 5000, 64, False), 100, 100, 40),
+    (I.Problem(1, 1, 4500, 4500, 128, False), 64, 0, 300),     # two global pairs
+    (I.Problem(2, 1, 600, 5000, 128, False), 50, 50, 17),      # Nq != Nk
+    (I.Problem(1, 1, 4300, 4300, 32, False), -1, 30, 129),     # look-back unbounded
+]
+
+
+@pytest.mark.parametrize("p,wl,wr,g", SPLIT_CASES, ids=[f"{c[0].name()}-wl{c[1]}-wr{c[2]}-g{c[3]}" for c in SPLIT_CASES])
+def test_window_split_global_rows(p, wl, wr, g):
+    assert _lib.fa_fwd_window_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D, p.causal, wl, wr, g) > 0
+    check_window(p, wl, wr, g)
+
+
+def test_window_split_large_logits():
+    p = I.Problem(1, 1, 4400, 4400, 128, False, qk_factor=8.0)
+    assert _lib.fa_fwd_window_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D, p.causal, 200, 200, 64) > 0
+    check_window(p, 200, 200, 64, seed=4)
+
+
+BWD_SPLIT_CASES = [
+    # more than 64 query steps with global keys: the global key tiles split into chunks
+    # of 32 query steps whose partial dK, dV add up in an fp32 workspace
+    (I.Problem(1, 2, 4500, 4500, 64, True), 200, -1, 40),      # causal, one global key tile
+    (I.Problem(1, 1, 4200, 4200, 128, True), 128, -1, 300),    # three global key tiles, ragged
+    (I.Problem(1, 1, 4200, 4500, 128, True), 300, -1, 130),    # causal, Nq < Nk
+    (I.Problem(1, 1, 5000, 2000, 64, False), 100, 100, 17),    # Nq > Nk
+    (I.Problem(1, 2, 4200, 200, 64, False), 10, 10, 500),      # every key global
+]
+
+
+@pytest.mark.parametrize("p,wl,wr,g", BWD_SPLIT_CASES,
+                         ids=[f"{c[0].name()}-wl{c[1]}-wr{c[2]}-g{c[3]}" for c in BWD_SPLIT_CASES])
+def test_window_split_global_keys(p, wl, wr, g):
+    assert (_lib.fa_bwd_window_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D, wl, wr, g) >
+            _lib.fa_bwd_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D))
+    check_window(p, wl, wr, g)

@@ -30,7 +30,8 @@ FA_ERR_SCRATCH_LIMIT = 8
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_device_status",
             "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
             "fa_graph_create", "fa_graph_launch", "fa_graph_destroy", "fa_fwd_varlen", "fa_bwd_varlen",
-            "fa_bwd_varlen_workspace_size", "fa_fwd_window", "fa_bwd_window", "fa_quantize_e4m3",
+            "fa_bwd_varlen_workspace_size", "fa_fwd_window", "fa_bwd_window", "fa_fwd_window_workspace_size", "fa_bwd_window_workspace_size",
+            "fa_quantize_e4m3",
             "fa_quantize_e4m3_transposed", "fa_fwd_fp8", "fa_step_host",
             "fa_step_host_device_bytes")
 
@@ -88,8 +89,12 @@ def lib() -> ctypes.CDLL:
     L.fa_quantize_e4m3_transposed.restype = i
     L.fa_fwd_fp8.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     L.fa_fwd_fp8.restype = i
-    L.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp]
+    L.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp, sz, vp]
     L.fa_fwd_window.restype = i
+    L.fa_fwd_window_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
+    L.fa_fwd_window_workspace_size.restype = sz
+    L.fa_bwd_window_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+    L.fa_bwd_window_workspace_size.restype = sz
     L.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp, sz, vp]
     L.fa_bwd_window.restype = i
     L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
@@ -307,18 +312,36 @@ def fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, m
 
 
 # ----------------------------------------------------------------------------- local window + global tokens
+def fa_fwd_window_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int, causal: bool, window_left: int,
+                                 window_right: int, n_global: int) -> int:
+    return int(lib().fa_fwd_window_workspace_size(B, H, Nq, Nk, D, int(bool(causal)), int(window_left),
+                                                  int(window_right), int(n_global)))
+
+
 def fa_fwd_window(q, k, v, o, lse, causal: bool, window_left: int, window_right: int, n_global: int,
-                  scale: float | None = None, stream=None) -> None:
-    """C ``fa_fwd_window`` on [B,H,N,D] bf16 tensors (negative window bound: unbounded)."""
+                  scale: float | None = None, workspace=None, stream=None) -> None:
+    """C ``fa_fwd_window`` on [B,H,N,D] bf16 tensors (negative window bound: unbounded);
+    allocates the split workspace with torch when it is needed and none is given."""
     B, H, Nq, D = q.shape
     Nk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    need = fa_fwd_window_workspace_size(B, H, Nq, Nk, D, causal, window_left, window_right, n_global)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wptr = 0 if workspace is None else _ptr(workspace, "workspace", torch.uint8)
+    wbytes = 0 if workspace is None else workspace.numel()
     rc = lib().fa_fwd_window(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
                              _ptr(v, "v", torch.bfloat16), _ptr(o, "o", torch.bfloat16),
                              _ptr(lse, "lse", torch.float32), B, H, Nq, Nk, D, float(scale), int(bool(causal)),
-                             int(window_left), int(window_right), int(n_global), _stream(stream))
+                             int(window_left), int(window_right), int(n_global), wptr, wbytes, _stream(stream))
     _check(rc, "fa_fwd_window")
+
+
+def fa_bwd_window_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int, window_left: int, window_right: int,
+                                 n_global: int) -> int:
+    return int(lib().fa_bwd_window_workspace_size(B, H, Nq, Nk, D, int(window_left), int(window_right),
+                                                  int(n_global)))
 
 
 def fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, causal: bool, window_left: int, window_right: int,
@@ -329,8 +352,8 @@ def fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, causal: bool, window_left: in
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if workspace is None:
-        workspace = torch.empty(max(fa_bwd_workspace_size(B, H, Nq, Nk, D), 256), dtype=torch.uint8,
-                                device=q.device)
+        workspace = torch.empty(max(fa_bwd_window_workspace_size(B, H, Nq, Nk, D, window_left, window_right,
+                                                                 n_global), 256), dtype=torch.uint8, device=q.device)
     rc = lib().fa_bwd_window(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
                              _ptr(v, "v", torch.bfloat16), _ptr(o, "o", torch.bfloat16),
                              _ptr(lse, "lse", torch.float32), _ptr(do, "do", torch.bfloat16),

@@ -142,7 +142,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   // Key tiles of one head are adjacent in launch order, so resident CTAs share the
   // Q, dO and dq_accum of a few heads in L2; causal: low key tiles see the most
   // queries and go first.
-  const int kt = blockIdx.x;
+  int kt = blockIdx.x;
+  int chunk = -1;  // >= 0: this CTA covers query steps [chunk*split_q, (chunk+1)*split_q) only
+  if (LOCAL && p.n_gk > 0) {
+    const int n_split_ctas = p.n_gk * p.n_qsplit;
+    if (kt < n_split_ctas) {
+      chunk = kt % p.n_qsplit;
+      kt = kt / p.n_qsplit;
+    } else {
+      kt = kt - n_split_ctas + p.n_gk;
+    }
+  }
   const int bh = blockIdx.y;
   const int k0 = kt * C::BN;
   const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, bh);
@@ -165,6 +175,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int qmax = min(sv.Nq - 1, ke + p.lm.win_l);
     qs = TileSet::make(qlo / C::BM, (p.lm.n_glob + C::BM - 1) / C::BM, max(qlo, k0 - p.lm.win_r) / C::BM,
                        qmax >= 0 ? qmax / C::BM + 1 : 0);
+  }
+  if (LOCAL && chunk >= 0) {
+    const int lo = chunk * p.split_q, hi = lo + p.split_q;
+    qs = TileSet::make(max(qs.a, lo), min(qs.g, hi), max(qs.L, lo), min(qs.hi, hi));
   }
   const int n_it = qs.count();
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
@@ -422,7 +436,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     // epilogue: WG0 writes dK = scale * acc, WG1 writes dV; the last dQ commit covers both
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) +
                          (VARLEN ? ((size_t)(sv.k_tok + key) * p.va.H + sv.h) * D : ((size_t)bh * sv.Nk + key) * D);
-    if (n_it == 0) {
+    if (LOCAL && chunk >= 0) {
+      // partial sums of a split global key tile: add (unscaled) into dkv_accum
+      if (n_it > 0 && ok && warp_wait(&bars[C::B_DQF + ((n_it - 1) & 1)], ((n_it - 1) >> 1) & 1, wc, 45)) {
+        tc_fence_after();
+        float* acc = p.dkv_accum + (((size_t)bh * (p.n_gk * C::BN) + (size_t)row + (size_t)kt * C::BN) * 2 + wg) * D;
+#pragma unroll
+        for (int g = 0; g < D / 16; ++g) {
+          uint32_t v[16];
+          tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + g * 16, v);
+          tmem_wait_ld(v);
+          if (key < sv.Nk) {
+#pragma unroll
+            for (int c = 0; c < 16; c += 4)
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(acc + g * 16 + c), "f"(as_f(v[c])),
+                           "f"(as_f(v[c + 1])), "f"(as_f(v[c + 2])), "f"(as_f(v[c + 3]))
+                           : "memory");
+          }
+        }
+      }
+    } else if (n_it == 0) {
       if (key < sv.Nk) {
         for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(dst + d) = make_uint4(0, 0, 0, 0);
       }
@@ -586,6 +619,28 @@ __global__ void __launch_bounds__(256) convert_kernel(const ConvParams p) {
   *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + tok * D + d) = w;
 }
 
+// dK = scale * dk_accum, dV = dv_accum (bf16) for the rows of split global key tiles.
+template <int D>
+__global__ void __launch_bounds__(256) kv_convert_kernel(const KvConvertParams p) {
+  constexpr int TPR = RowCfg<D>::TPR;
+  const int bh = blockIdx.y;
+  const int r = blockIdx.x * RowCfg<D>::ROWS + threadIdx.x / TPR;
+  if (r >= p.n_rows || r >= p.Nk) return;
+  const int d = (threadIdx.x % TPR) * 8;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const float4* src = reinterpret_cast<const float4*>(p.dkv_accum + (((size_t)bh * p.n_rows + r) * 2 + m) * D + d);
+    const float4 a = src[0], b = src[1];
+    const float mul = m == 0 ? p.scale : 1.f;
+    uint4 w;
+    w.x = pack_bf16(a.x * mul, a.y * mul);
+    w.y = pack_bf16(a.z * mul, a.w * mul);
+    w.z = pack_bf16(b.x * mul, b.y * mul);
+    w.w = pack_bf16(b.z * mul, b.w * mul);
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(m == 0 ? p.dk : p.dv) + ((size_t)bh * p.Nk + r) * D + d) = w;
+  }
+}
+
 template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                      const BwdParams& p, int BH, cudaStream_t st) {
@@ -593,7 +648,8 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   auto kern = bwd_kernel<D, CAUSAL, VARLEN, LOCAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.n_k_tiles, (unsigned)BH);
+  const int gx = (LOCAL && p.n_gk > 0) ? p.n_gk * p.n_qsplit + (p.n_k_tiles - p.n_gk) : p.n_k_tiles;
+  dim3 grid((unsigned)gx, (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
@@ -646,6 +702,17 @@ cudaError_t launch_bwd_prep(int D, const PrepParams& p, cudaStream_t st) {
 
 cudaError_t launch_bwd_convert(int D, const ConvParams& p, cudaStream_t st) {
   TA11_SWITCH_D(D, bwd::conv_t<DD>(p, st))
+}
+
+template <int D>
+cudaError_t kv_conv_t(const KvConvertParams& p, int BH, cudaStream_t st) {
+  dim3 grid((unsigned)((p.n_rows + bwd::RowCfg<D>::ROWS - 1) / bwd::RowCfg<D>::ROWS), (unsigned)BH);
+  bwd::kv_convert_kernel<D><<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_kv_convert(int D, const KvConvertParams& p, int BH, cudaStream_t st) {
+  TA11_SWITCH_D(D, kv_conv_t<DD>(p, BH, st))
 }
 
 }  // namespace ta11

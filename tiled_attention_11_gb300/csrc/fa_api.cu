@@ -231,8 +231,31 @@ ta11::LocalMask local_mask(int Nq, int Nk, int window_left, int window_right, in
   return m;
 }
 
+// Split of the global query rows' key range (local mask, non-causal, long key range):
+// see FwdParams.  Everything zero when no split is needed.
+struct FwdSplit {
+  int n_gp = 0, n_split = 0, split_t = 0;
+  size_t o_bytes = 0, ml_bytes = 0, total = 0;
+};
+constexpr int kSplitTiles = 16;  // key tiles per chunk: about one window CTA's work
+
+FwdSplit fwd_split(int B, int H, int Nq, int Nk, int D, int causal, const ta11::LocalMask& m) {
+  FwdSplit f;
+  const int nk_tiles = (Nk + 127) / 128, n_pairs = (Nq + 255) / 256;
+  if (causal || m.n_glob <= 0 || nk_tiles <= 2 * kSplitTiles) return f;
+  f.n_gp = (m.n_glob + 255) / 256 < n_pairs ? (m.n_glob + 255) / 256 : n_pairs;
+  f.split_t = kSplitTiles;
+  f.n_split = (nk_tiles + kSplitTiles - 1) / kSplitTiles;
+  const size_t recs = (size_t)B * H * f.n_gp * 256 * f.n_split;
+  f.o_bytes = (recs * D * 4 + 255) / 256 * 256;
+  f.ml_bytes = (recs * 16 + 255) / 256 * 256;
+  f.total = f.o_bytes + f.ml_bytes;
+  return f;
+}
+
 int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk, int D,
-              float scale, int causal, const ta11::LocalMask* lm, cudaStream_t stream) {
+              float scale, int causal, const ta11::LocalMask* lm, cudaStream_t stream, void* workspace = nullptr,
+              size_t workspace_bytes = 0) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   int rc = check_sizes(B, H, Nq, Nk, D, scale);
   if (rc != FA_OK) return rc;
@@ -245,6 +268,17 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
     for (Range in : {rq, rk, rv})
       if (overlap(out, in)) return FA_ERR_INVALID_ARG;
   if (overlap(ro, rl)) return FA_ERR_INVALID_ARG;
+
+  FwdSplit split;
+  if (lm) {
+    split = fwd_split(B, H, Nq, Nk, D, causal, *lm);
+    if (split.n_gp > 0) {
+      if (!workspace || !aligned(workspace, 256) || workspace_bytes < split.total) return FA_ERR_WORKSPACE;
+      const Range rw = rng(workspace, split.total);
+      for (Range r : {rq, rk, rv, ro, rl})
+        if (overlap(rw, r)) return FA_ERR_INVALID_ARG;
+    }
+  }
 
   unsigned* status = nullptr;
   rc = current_device(&status);
@@ -266,8 +300,39 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
   if (lm) {
     p.lm = *lm;
     p.local = 1;
+    if (split.n_gp > 0) {
+      p.n_gp = split.n_gp;
+      p.n_split = split.n_split;
+      p.split_t = split.split_t;
+      p.part_o = static_cast<float*>(workspace);
+      p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + split.o_bytes);
+    }
   }
-  return ta11::launch_fwd(D, causal != 0, tq, tk, tv, p, (int)BH, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  if (ta11::launch_fwd(D, causal != 0, tq, tk, tv, p, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (split.n_gp > 0) {
+    ta11::FwdCombineParams cp{p.part_o, p.part_ml, o, lse, Nq, split.n_gp * 256, split.n_split};
+    if (ta11::launch_fwd_combine(D, cp, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
+// Split of the global key tiles' query range (local mask with global tokens, long query
+// range): see BwdParams.  Everything zero when no split is needed.
+struct BwdSplit {
+  int n_gk = 0, n_qsplit = 0, split_q = 0;
+  size_t bytes = 0;
+};
+constexpr int kSplitSteps = 32;  // 64-query steps per chunk
+
+BwdSplit bwd_split(int B, int H, int Nq, int Nk, int D, const ta11::LocalMask& m) {
+  BwdSplit f;
+  const int nk_tiles = (Nk + 127) / 128, n_qt = (Nq + 63) / 64;
+  if (m.n_glob <= 0 || n_qt <= 2 * kSplitSteps) return f;
+  f.n_gk = (m.n_glob + 127) / 128 < nk_tiles ? (m.n_glob + 127) / 128 : nk_tiles;
+  f.split_q = kSplitSteps;
+  f.n_qsplit = (n_qt + kSplitSteps - 1) / kSplitSteps;
+  f.bytes = ((size_t)B * H * f.n_gk * 128 * 2 * D * 4 + 255) / 256 * 256;
+  return f;
 }
 
 int bwd_dense(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
@@ -280,11 +345,13 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return FA_ERR_MISALIGNED;
   const WsLayout w = ws_layout(B, H, Nq, D);
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < w.total) return FA_ERR_WORKSPACE;
+  const BwdSplit split = lm ? bwd_split(B, H, Nq, Nk, D, *lm) : BwdSplit{};
+  const size_t ws_need = w.total + split.bytes;
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < ws_need) return FA_ERR_WORKSPACE;
   const size_t BH = (size_t)B * H;
   const size_t nq_b = BH * Nq * D * 2, nk_b = BH * Nk * D * 2;
   const Range ins[] = {rng(q, nq_b), rng(k, nk_b), rng(v, nk_b), rng(o, nq_b), rng(lse, BH * Nq * 4), rng(dO, nq_b)};
-  const Range outs[] = {rng(dq, nq_b), rng(dk, nk_b), rng(dv, nk_b), rng(workspace, w.total)};
+  const Range outs[] = {rng(dq, nq_b), rng(dk, nk_b), rng(dv, nk_b), rng(workspace, ws_need)};
   for (int a = 0; a < 4; ++a) {
     for (const Range& in : ins)
       if (overlap(outs[a], in)) return FA_ERR_INVALID_ARG;
@@ -323,9 +390,18 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   bp.scale_log2 = scale * kLog2e;
   bp.wait_limit_ns = g_wait_limit_ns.load();
   bp.status = status;
+  float* dkv_accum = nullptr;
   if (lm) {
     bp.lm = *lm;
     bp.local = 1;
+    if (split.n_gk > 0) {
+      dkv_accum = reinterpret_cast<float*>(ws + w.total);
+      if (cudaMemsetAsync(dkv_accum, 0, split.bytes, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+      bp.n_gk = split.n_gk;
+      bp.n_qsplit = split.n_qsplit;
+      bp.split_q = split.split_q;
+      bp.dkv_accum = dkv_accum;
+    }
   }
   cudaEvent_t ev_b = nullptr, ev_e = nullptr;
   {
@@ -339,6 +415,10 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
 
   ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale};
   if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (split.n_gk > 0) {
+    ta11::KvConvertParams kp{dkv_accum, dk, dv, Nk, split.n_gk * 128, scale};
+    if (ta11::launch_bwd_kv_convert(D, kp, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  }
   return FA_OK;
 }
 
@@ -358,11 +438,23 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
                    workspace_bytes, stream);
 }
 
+size_t fa_fwd_window_workspace_size(int B, int H, int Nq, int Nk, int D, int causal, int window_left,
+                                    int window_right, int n_global) {
+  if (check_sizes(B, H, Nq, Nk, D, 1.f) != FA_OK) return 0;
+  return fwd_split(B, H, Nq, Nk, D, causal, local_mask(Nq, Nk, window_left, window_right, n_global)).total;
+}
+
 int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-                  int D, float scale, int causal, int window_left, int window_right, int n_global,
-                  cudaStream_t stream) {
+                  int D, float scale, int causal, int window_left, int window_right, int n_global, void* workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
   const ta11::LocalMask m = local_mask(Nq, Nk, window_left, window_right, n_global);
-  return fwd_dense(q, k, v, o, lse, B, H, Nq, Nk, D, scale, causal, &m, stream);
+  return fwd_dense(q, k, v, o, lse, B, H, Nq, Nk, D, scale, causal, &m, stream, workspace, workspace_bytes);
+}
+
+size_t fa_bwd_window_workspace_size(int B, int H, int Nq, int Nk, int D, int window_left, int window_right,
+                                    int n_global) {
+  if (check_sizes(B, H, Nq, Nk, D, 1.f) != FA_OK) return 0;
+  return ws_layout(B, H, Nq, D).total + bwd_split(B, H, Nq, Nk, D, local_mask(Nq, Nk, window_left, window_right, n_global)).bytes;
 }
 
 int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,

@@ -95,6 +95,23 @@ struct FwdParams {
   VarlenArgs va;
   LocalMask lm;         // used when `local` is set
   int local;            // 1: apply the local-window + global-token mask
+  // Local mask, non-causal: the first n_gp query-tile pairs hold global query rows, which
+  // see every key.  Each runs as n_split CTAs over key tiles [c*split_t, (c+1)*split_t)
+  // that write partial results (the unnormalised O accumulator, and per row the
+  // subtracted maximum m (base 2), the sum l and the sum of rounded weights lr);
+  // fwd_combine merges them.  n_gp == 0: no split.
+  int n_gp, n_split, split_t;
+  float* part_o;        // [B*H][n_gp*256][n_split][D]
+  float* part_ml;       // [B*H][n_gp*256][n_split][4]: m, l, lr, unused
+};
+
+struct FwdCombineParams {
+  const float* part_o;
+  const float* part_ml;
+  void* o;              // bf16 [B,H,Nq,D]
+  float* lse;           // fp32 [B,H,Nq]
+  int Nq, n_rows;       // n_rows = n_gp*256 (rows with partial records per head)
+  int n_split;
 };
 
 // Backward workspace rows: dense, head bh owns rows [bh*Nq_pad, bh*Nq_pad + Nq_pad);
@@ -120,6 +137,19 @@ struct BwdParams {
   VarlenArgs va;
   LocalMask lm;         // used when `local` is set
   int local;            // 1: apply the local-window + global-token mask
+  // Local mask: the first n_gk key tiles hold global keys, which every (later) query sees.
+  // Each runs as n_qsplit CTAs over query steps [c*split_q, (c+1)*split_q) that add their
+  // partial dK, dV (fp32, unscaled) into dkv_accum; bwd_kv_convert writes them out.
+  int n_gk, n_qsplit, split_q;
+  float* dkv_accum;     // [B*H][n_gk*128][2][D] (zeroed before the launch)
+};
+
+struct KvConvertParams {
+  const float* dkv_accum;
+  void* dk;             // bf16 [B,H,Nk,D]
+  void* dv;
+  int Nk, n_rows;       // n_rows = n_gk*128
+  float scale;
 };
 
 struct PrepParams {
@@ -159,10 +189,12 @@ struct Fp8FwdParams {
 // local-window + global-token mask (dense layout only).
 cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int BH, cudaStream_t st);
+cudaError_t launch_fwd_combine(int D, const FwdCombineParams& p, int BH, cudaStream_t st);
 cudaError_t launch_bwd_prep(int D, const PrepParams& p, cudaStream_t st);
 cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int BH, cudaStream_t st);
 cudaError_t launch_bwd_convert(int D, const ConvParams& p, cudaStream_t st);
+cudaError_t launch_bwd_kv_convert(int D, const KvConvertParams& p, int BH, cudaStream_t st);
 cudaError_t launch_fwd_fp8(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
                            const Fp8FwdParams& p, int BH, cudaStream_t st);
 // Per-tensor e4m3 quantisation: amax (device float, zeroed by the caller's stream

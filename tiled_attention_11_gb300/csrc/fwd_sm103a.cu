@@ -107,8 +107,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   // Query-tile pairs of one head are adjacent in launch order, so the CTAs resident at
   // any moment share the K/V of a few heads in L2; within a head the heaviest
   // (causal) pairs go first.
-  // (Local mask: pair 0 holds the global query rows, which see every key; it goes first.)
-  const int pair = LOCAL ? (int)blockIdx.x : (int)gridDim.x - 1 - (int)blockIdx.x;
+  // (Local mask: pairs holding global query rows, which see every key, go first; without
+  // the causal condition they are split over chunks of key tiles, see FwdParams.)
+  int pair = LOCAL ? (int)blockIdx.x : (int)gridDim.x - 1 - (int)blockIdx.x;
+  int chunk = -1;  // >= 0: this CTA covers key tiles [chunk*split_t, (chunk+1)*split_t) only
+  if (LOCAL && p.n_gp > 0) {
+    const int n_split_ctas = p.n_gp * p.n_split;
+    if (pair < n_split_ctas) {
+      chunk = pair % p.n_split;
+      pair = pair / p.n_split;
+    } else {
+      pair = pair - n_split_ctas + p.n_gp;
+    }
+  }
   const int bh = blockIdx.y;
   const int q0 = pair * 2 * C::BM;
   const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, bh);
@@ -136,7 +147,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     if (!LOCAL || qa < p.lm.n_glob) return TileSet::make(0, 0, 0, hi);
     return TileSet::make(0, (p.lm.n_glob + C::BN - 1) / C::BN, max(qa - p.lm.win_l, 0) / C::BN, hi);
   };
-  const TileSet ks0 = key_set(q0), ks1 = key_set(q0 + C::BM);
+  auto chunk_of = [&](const TileSet& k) -> TileSet {  // restrict to this CTA's key chunk
+    if (!LOCAL || chunk < 0) return k;
+    const int lo = chunk * p.split_t, hi = lo + p.split_t;
+    return TileSet::make(max(k.a, lo), min(k.g, hi), max(k.L, lo), min(k.hi, hi));
+  };
+  const TileSet ks0 = chunk_of(key_set(q0)), ks1 = chunk_of(key_set(q0 + C::BM));
   // The producer and the UMMA issuer walk the union of both sets in ascending order.
   auto next_kt = [&](int kt) { return min(ks0.next(kt), ks1.next(kt)); };
   // kNone when no row of the pair sees a key (a sequence without keys, or a local mask
@@ -482,7 +498,30 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       tc_fence_before();
       mbar_arrive(&bars[C::B_PF + t]);
     }
-    if (ok && n_kv == 0) {  // this tile's rows see no key: O = 0, L = -inf
+    if (LOCAL && chunk >= 0) {
+      // partial record of this key chunk: unnormalised O accumulator, m, l, lr
+      if (ok && n_kv > 0 && !warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8)) ok = false;
+      if (ok && q_idx < sv.Nq) {
+        const size_t rec = ((size_t)bh * (p.n_gp * 2 * C::BM) + q_idx) * p.n_split + chunk;
+        float* po = p.part_o + rec * D;
+        if (n_kv > 0) {
+          tc_fence_after();
+#pragma unroll
+          for (int g = 0; g < D / 16; ++g) {
+            uint32_t o[16];
+            tmem_ld16(t_o + g * 16, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int c = 0; c < 16; c += 4)
+              *reinterpret_cast<float4*>(po + g * 16 + c) = make_float4(as_f(o[c]), as_f(o[c + 1]), as_f(o[c + 2]), as_f(o[c + 3]));
+          }
+        } else {
+          for (int d = 0; d < D; d += 4) *reinterpret_cast<float4*>(po + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        *reinterpret_cast<float4*>(p.part_ml + rec * 4) =
+            n_kv > 0 ? make_float4(m, l, lr, 0.f) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+      }
+    } else if (ok && n_kv == 0) {  // this tile's rows see no key: O = 0, L = -inf
       if (q_idx < sv.Nq) {
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + o_row(q_idx);
         for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
@@ -525,6 +564,45 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   }
 }
 
+// Merge the per-chunk partial records of the split global query rows: with M = max_c m_c,
+// O = sum_c O_c 2^(m_c - M) / sum_c lr_c 2^(m_c - M) and L = (M + log2 sum_c l_c 2^(m_c - M)) ln 2,
+// the same result as one pass over every key tile (up to rounding order).  D/8 threads per row.
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const FwdCombineParams p) {
+  constexpr int TPR = D / 8, ROWS = 256 / TPR;
+  const int bh = blockIdx.y;
+  const int r = blockIdx.x * ROWS + threadIdx.x / TPR;
+  const int part = threadIdx.x % TPR;
+  if (r >= p.n_rows || r >= p.Nq) return;
+  const size_t rec0 = ((size_t)bh * p.n_rows + r) * p.n_split;
+  float M = -INFINITY;
+  for (int c = 0; c < p.n_split; ++c) M = fmaxf(M, p.part_ml[(rec0 + c) * 4]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float lsum = 0.f, lrsum = 0.f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < p.n_split; ++c) {
+      const float4 ml = *reinterpret_cast<const float4*>(p.part_ml + (rec0 + c) * 4);
+      if (ml.x == -INFINITY) continue;  // no visible key in this chunk
+      const float w = exp2f(ml.x - M);
+      lsum += w * ml.y;
+      lrsum += w * ml.z;
+      const float4* po = reinterpret_cast<const float4*>(p.part_o + (rec0 + c) * D + part * 8);
+      const float4 a = po[0], b = po[1];
+      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+      acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    }
+  }
+  const float inv = lrsum > 0.f ? 1.f / lrsum : 0.f;
+  uint4 wv;
+  wv.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  wv.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  wv.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  wv.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.Nq + r) * D + part * 8) = wv;
+  if (part == 0)
+    p.lse[(size_t)bh * p.Nq + r] = lsum > 0.f ? (M + log2f(lsum)) * 0.69314718055994530942f : -INFINITY;
+}
+
 template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                      int BH, cudaStream_t st) {
@@ -532,7 +610,9 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   auto kern = fwd_kernel<D, CAUSAL, VARLEN, LOCAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH);
+  const int n_pairs = (p.n_q_tiles + 1) / 2;
+  const int gx = (LOCAL && p.n_gp > 0) ? p.n_gp * p.n_split + (n_pairs - p.n_gp) : n_pairs;
+  dim3 grid((unsigned)gx, (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -577,6 +657,25 @@ cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensor
       return cudaErrorInvalidValue;
   }
 #undef TA11_FWD_CASE
+}
+
+cudaError_t launch_fwd_combine(int D, const FwdCombineParams& p, int BH, cudaStream_t st) {
+  constexpr int kRowsPerBlock = 256;  // rows per block at D/8 threads per row: 256 / (D / 8)
+  switch (D) {
+#define TA11_COMBINE_CASE(DD)                                                                   \
+  case DD: {                                                                                    \
+    dim3 grid((unsigned)((p.n_rows + (kRowsPerBlock / (DD / 8)) - 1) / (kRowsPerBlock / (DD / 8))), (unsigned)BH); \
+    fwd::combine_kernel<DD><<<grid, 256, 0, st>>>(p);                                           \
+    return cudaGetLastError();                                                                  \
+  }
+    TA11_COMBINE_CASE(16)
+    TA11_COMBINE_CASE(32)
+    TA11_COMBINE_CASE(64)
+    TA11_COMBINE_CASE(128)
+#undef TA11_COMBINE_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned* status, cudaStream_t st) {
