@@ -372,10 +372,16 @@ def run_table(args):
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    dense_rows = not (args.varlen_only or args.window_only or args.fp8_only)
+    ex2 = _lib.ex2_rate(dev) if dense_rows else 0.0
+    if dense_rows:
+        print(f"exp2 roof (fa_ex2_probe, special-function units): {ex2 / 1e12:.2f} T exp2/s")
     print("| workload | fwd ms | fwd TFLOP/s | fwd % peak | bwd ms | bwd TFLOP/s | bwd % peak | fwd GB/s (% HBM) "
-          "| step ms direct / CUDA graph | L2 flush |")
-    print("|---|---|---|---|---|---|---|---|---|---|")
-    for p in ([] if args.varlen_only or args.window_only or args.fp8_only else I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED]):
+          "| step ms direct / CUDA graph | L2 flush | exp2 % of roof fwd / bwd |")
+    print("|---|---|---|---|---|---|---|---|---|---|---|")
+    for p in (I.SWEEP + I.SWEEP_X8[-2:] + I.LONG + [I.LAYER, I.LONG_RAGGED] if dense_rows else []):
+        if args.only and p.name() != args.only:
+            continue
         q, k, v, do = (t.to(dev) for t in I.draw(p, 0))
         o = torch.empty_like(q)
         lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
@@ -422,11 +428,15 @@ def run_table(args):
         ff, fb = I.flops_fwd(p), I.flops_bwd(p)
         tf, tb = ff / res[0] / 1e9, fb / res[1] / 1e9
         gbs = in_bytes / res[0] / 1e6
+        exps = ff / (4.0 * p.D)  # one exp2 per unmasked score in each pass (same causal convention)
+        xf, xb = 100 * exps / (res[0] * 1e-3) / ex2, 100 * exps / (res[1] * 1e-3) / ex2
         print(f"| {p.name()} | {res[0]:.4f} | {tf:.1f} | {100 * tf / sustained:.1f}% | {res[1]:.4f} | {tb:.1f} | "
               f"{100 * tb / sustained:.1f}% | {gbs:.0f} ({100 * gbs / hbm:.1f}%) | {steps[0]:.4f} / {steps[1]:.4f} "
-              f"| {'yes' if small else 'no'} |", flush=True)
-        del q, k, v, do, o, lse, dq, dk, dv, ws, fws
+              f"| {'yes' if small else 'no'} | {xf:.1f}% / {xb:.1f}% |", flush=True)
+        del q, k, v, do, o, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()
+    if args.only:
+        return
     if args.fp8_only:
         _table_fp8(args, dev, sustained, hbm)
         return
@@ -643,6 +653,8 @@ def main(argv=None):
     ap.add_argument("--table", action="store_true", help="time every workload, print a markdown table")
     ap.add_argument("--varlen-only", action="store_true", help="with --table: only the packed variable-length row")
     ap.add_argument("--window-only", action="store_true", help="with --table: only the local-window rows")
+    ap.add_argument("--only", default="", help="with --table: only the dense row of this workload name "
+                                               "(e.g. B8H1q256k256D16n)")
     ap.add_argument("--fp8-only", action="store_true", help="with --table: only the FP8 forward rows")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps

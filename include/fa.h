@@ -111,6 +111,18 @@ void fa_set_wait_limit_ns(unsigned long long ns);
 int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
 
 /*
+ * Measurement hook (no counterpart on the pages): the rate of the special-function
+ * unit's exp2, the third roof of the softmax next to the tensor core and HBM.  Launches
+ * n_blocks blocks of 512 threads; each thread runs 8 independent chains of `iters`
+ * ex2.approx.ftz.f32, so the launch performs n_blocks * 512 * 8 * iters of them and
+ * its duration (CUDA events on `stream`) gives exp2 per second.  `out` (device, caller
+ * owned, n_blocks * 512 floats) receives each thread's chain sum.  Asynchronous.
+ * Returns FA_ERR_INVALID_ARG (null out, n_blocks outside [1, 65535], iters outside
+ * [1, 2^20]), FA_ERR_MISALIGNED, FA_ERR_DEVICE (not sm_103) or FA_ERR_LAUNCH.
+ */
+int fa_ex2_probe(float* out, int n_blocks, int iters, cudaStream_t stream);
+
+/*
  * Timing hook for measurement tools (no counterpart on the pages): while both
  * events are non-null, every fa_bwd records `begin` on its stream immediately
  * before launching its main tensor-core kernel and `end` immediately after it,

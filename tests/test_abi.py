@@ -239,3 +239,15 @@ def test_window_bwd_split_workspace(L):
     assert L.fa_bwd_window(*args, base, None) == _lib.FA_ERR_WORKSPACE      # split area missing
     assert L.fa_bwd_window(*args, need - 1, None) == _lib.FA_ERR_WORKSPACE
     assert L.fa_bwd_window(*args, need, None) == _lib.FA_ERR_DEVICE
+
+
+def test_ex2_probe_validation(L):
+    vp = ctypes.c_void_p
+    out = vp(ptrs(1)[0])
+    assert L.fa_ex2_probe(None, 4, 8, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_ex2_probe(out, 0, 8, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_ex2_probe(out, 65536, 8, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_ex2_probe(out, 4, 0, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_ex2_probe(out, 4, (1 << 20) + 1, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_ex2_probe(vp(ptrs(1)[0] + 2), 4, 8, None) == _lib.FA_ERR_MISALIGNED
+    assert L.fa_ex2_probe(out, 4, 8, None) == _lib.FA_ERR_DEVICE

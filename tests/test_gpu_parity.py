@@ -268,3 +268,18 @@ def test_binding_rejects_bad_tensors():
     with pytest.raises(_lib.FAError) as e:
         _lib.forward(q, q, q, causal=False)
     assert e.value.code == _lib.FA_ERR_UNSUPPORTED_D
+
+
+def test_ex2_probe_rate_and_values():
+    # every chain x <- 2^(-x) contracts to the fixed point x* = 2^(-x*) ~ 0.6412; the rate
+    # is the special-function units' (one 32-lane exp2 unit's worth per SM and clock
+    # is 32 x 152 x ~2 GHz ~ 1e13 per second; allow a wide band)
+    x = 0.5
+    for _ in range(200):
+        x = 2.0 ** -x
+    out = torch.empty(152 * 512, dtype=torch.float32, device="cuda")
+    _lib._check(_lib.lib().fa_ex2_probe(out.data_ptr(), 152, 256, torch.cuda.current_stream().cuda_stream), "probe")
+    torch.cuda.synchronize()
+    assert torch.allclose(out.double().cpu(), torch.full((152 * 512,), 8 * x, dtype=torch.float64), atol=1e-4)
+    rate = _lib.ex2_rate()
+    assert 1e12 < rate < 1e14, rate

@@ -67,12 +67,12 @@ struct Cfg {
   static constexpr int B_SF = 1 + 2 * NS;    // [2] S^T in TMEM buffer b
   static constexpr int B_DPF = 3 + 2 * NS;   // dP^T in TMEM
   static constexpr int B_PF = 4 + 2 * NS;    // [2] P^T in TMEM buffer b (compute warps)
-  static constexpr int B_DSF = 6 + 2 * NS;   // dS^T in TMEM and shared memory (compute warps)
+  static constexpr int B_DSF = 6 + 2 * NS;   // dS^T in shared memory (compute warps)
   static constexpr int B_DQF = 7 + 2 * NS;   // [2] dQ^T MMA of a step done: its dS^T smem buffer is free
   static constexpr int B_DQR = 9 + 2 * NS;   // [2] dQ^T in TMEM buffer b, ready for the dQ warpgroup
   static constexpr int B_DQE = 11 + 2 * NS;  // [2] dQ^T drained from TMEM buffer b (buffer free)
   static constexpr int B_KT = 13 + 2 * NS;   // K^T written into TMEM
-  static constexpr int B_DKD = 14 + 2 * NS;  // dK done (dP^T / dS^T TMEM free)
+  static constexpr int B_DPE = 14 + 2 * NS;  // dP^T loaded by the compute warps (its TMEM columns free)
   static constexpr int B_DRAIN = 15 + 2 * NS;  // [2] one per issuing thread
   static constexpr int NBAR = 17 + 2 * NS;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
@@ -81,7 +81,7 @@ struct Cfg {
   // 13: UMMA issuer for S^T, dP^T (and TMEM allocator), 14: UMMA issuer for dV, dK, dQ^T
   static constexpr int THREADS = 480;
   static constexpr int W_PRODUCER = 12, W_MMA_A = 13, W_MMA_B = 14;
-  // TMEM columns: S^T/P^T/dQ^T buffer 0 | buffer 1 | dP^T/dS^T | K^T (bf16 pairs) | dV | dK
+  // TMEM columns: S^T/P^T/dQ^T buffer 0 | buffer 1 | dP^T | K^T (bf16 pairs) | dV | dK
   static constexpr int T_S = 0, T_DP = 128, T_KT = 192, T_DV = 256, T_DK = 256 + D;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, BM, false, false);   // S^T, dP^T
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     mbar_init(&bars[C::B_DPF], 1);
     mbar_init(&bars[C::B_DSF], 256);
     mbar_init(&bars[C::B_KT], 128);
-    mbar_init(&bars[C::B_DKD], 1);
+    mbar_init(&bars[C::B_DPE], 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -281,9 +281,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         issue_s(0);
       }
       for (int it = 0; ok && it < n_it; ++it) {
-        // dP^T(it) overwrites dS^T(it-1) in TMEM once dK(it-1) has read it (its stage is
-        // loaded: S^T(it) waited for it)
-        if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DKD], (it - 1) & 1, wc, 35))) break;
+        // dP^T(it) overwrites dP^T(it-1) in TMEM once the compute warps have loaded it (its
+        // stage is loaded: S^T(it) waited for it)
+        if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DPE], (it - 1) & 1, wc, 35))) break;
         tc_fence_after();
         issue_dp(it);
         // S^T(it+1) goes to the buffer that held P^T(it-1), then dQ^T(it-1): after the dQ
@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const uint64_t dQm = sdesc(sbase + C::OFF_Q, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // MN-major
       const uint64_t dOm = sdesc(sbase + C::OFF_DO, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);  // MN-major
       const uint64_t dS0 = sdesc(sbase + C::OFF_DS, C::DS_BYTES, 1024, 2u);          // dS^T buffer 0, MN-major
+      const uint64_t dSa = sdesc(sbase + C::OFF_DS, 16, 1024, 2u);                   // the same, K-major A
       bool ok = mbar_wait(&bars[C::B_KV], 0, wc, 32);
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % C::NS, b = it & 1;
@@ -319,15 +320,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         for (int kk = 0; kk < C::BM / 16; ++kk)
           umma_ts(tmem + C::T_DV, tmem + C::T_S + (uint32_t)(b * 64) + a_col(kk), desc_adv(om, mnoff<D>(kk)),
                   C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q_i and dQ_i^T = K^T dS^T once dS^T is in TMEM and shared memory
+        // dK += dS^T Q_i and dQ_i^T = K^T dS^T once dS^T is in shared memory buffer b (one
+        // copy serves both: 128-byte swizzled rows of 64 queries per key are the K-major A
+        // layout of dK and the MN-major B layout of dQ^T)
         if (!(ok = mbar_wait(&bars[C::B_DSF], it & 1, wc, 36))) break;
         if (it == 0 && !(ok = mbar_wait(&bars[C::B_KT], 0, wc, 47))) break;
         tc_fence_after();
+        const uint64_t dsa = desc_adv(dSa, (uint32_t)(b * C::DS_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          umma_ts(tmem + C::T_DK, tmem + C::T_DP + a_col(kk), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
+          umma_ss(tmem + C::T_DK, desc_adv(dsa, (uint32_t)(kk * 32)), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
                   (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars[C::B_DKD]);
         umma_commit(&bars[C::B_QE + s]);  // dK was the stage's last reader
         // dQ^T(it) into buffer b, which dV(it) (issued above: in-order) has finished reading
         const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
@@ -406,6 +409,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       uint32_t dv[32];
       tmem_ld32(t_lane + C::T_DP + col0, dv);
       tmem_wait_ld(dv);
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_DPE]);  // dP^T(it+1) may overwrite it now
       uint32_t dk[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
@@ -413,12 +418,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const float d1 = pv[2 * c + 1] * (as_f(dv[2 * c + 1]) - dlt[2 * c + 1]);
         dk[c] = pack_bf16(d0, d1);
       }
-      tmem_st16(t_lane + C::T_DP + wg * 32, dk);
-      // dS^T row into shared memory (128-byte rows, 128B swizzle) for the dQ^T MMA, once the
-      // dQ^T MMA two tiles back has finished reading this buffer.
+      // dS^T row into shared memory (128-byte rows, 128B swizzle) for the dK and dQ^T MMAs,
+      // once the dQ^T MMA two tiles back (issued after that tile's dK) has finished reading
+      // this buffer.
       if (it >= 2 && !warp_wait(&bars[C::B_DQF + (it & 1)], ((it - 2) >> 1) & 1, wc, 44)) {
         ok = false;
-        tmem_wait_st();
         break;
       }
       uint8_t* dsrow = sds_row_base + (it & 1) * C::DS_BYTES;
@@ -428,8 +432,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         *reinterpret_cast<uint4*>(dsrow + phys * 16) = make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
       }
       fence_proxy_async_smem();
-      tmem_wait_st();
-      tc_fence_before();
       mbar_arrive(&bars[C::B_DSF]);
     }
 

@@ -494,6 +494,15 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream) {
   return ta11::launch_wait_probe(limit_ns, status, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+int fa_ex2_probe(float* out, int n_blocks, int iters, cudaStream_t stream) {
+  if (!out || n_blocks < 1 || n_blocks > 65535 || iters < 1 || iters > (1 << 20)) return FA_ERR_INVALID_ARG;
+  if (!aligned(out, 4)) return FA_ERR_MISALIGNED;
+  unsigned* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  return ta11::launch_ex2_probe(out, n_blocks, iters, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------------------------------
