@@ -117,11 +117,26 @@ def test_window_large_logits():
     check_window(p, 200, -1, 32, seed=3)
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_unbounded_mask_matches_plain_path_bitwise(causal):
+BITWISE_CASES = [
+    # (B, H, Nq, Nk, D, causal).  Causal grids of at most one wave fold their query-tile
+    # pairs in fa_fwd (tile t with tile n-1-t); the local-mask kernel never does, so these
+    # also check the fold bit for bit: odd tile counts (the middle tile alone), even ones,
+    # and Nq != Nk both ways.
+    (2, 2, 333, 333, 64, False),
+    (2, 2, 333, 333, 64, True),
+    (1, 2, 1100, 1100, 128, True),
+    (1, 2, 1536, 1536, 64, True),
+    (1, 1, 700, 1500, 128, True),
+    (1, 1, 1500, 700, 32, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,D,causal", BITWISE_CASES,
+                         ids=[f"B{c[0]}H{c[1]}q{c[2]}k{c[3]}D{c[4]}{'c' if c[5] else 'n'}" for c in BITWISE_CASES])
+def test_unbounded_mask_matches_plain_path_bitwise(B, H, Nq, Nk, D, causal):
     # window_left = window_right = -1 and no global tokens is the plain mask: the same
     # tiles in the same order, so the outputs agree bit for bit with fa_fwd / fa_bwd
-    p = I.Problem(2, 2, 333, 333, 64, causal)
+    p = I.Problem(B, H, Nq, Nk, D, causal)
     q, k, v, do = I.draw(p, 5)
     dev = torch.device("cuda")
     qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))

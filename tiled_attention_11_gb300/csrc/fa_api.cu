@@ -28,6 +28,7 @@ struct DeviceState {
   std::once_flag once;
   int ok = 0;               // 1: sm_103 and status word resolved
   unsigned* status = nullptr;
+  int n_sm = 0;             // streaming multiprocessors
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -53,11 +54,22 @@ int current_device(unsigned** status) {
       return;
     }
     s.status = static_cast<unsigned*>(p);
+    if (cudaDeviceGetAttribute(&s.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
     s.ok = 1;
   });
   if (!s.ok) return FA_ERR_DEVICE;
   *status = s.status;
   return FA_OK;
+}
+
+// SM count of the current device (after a successful current_device).
+int current_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return g_dev[dev].n_sm;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -297,6 +309,10 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = status;
+  // Causal launches that fit in one wave are bound by their heaviest CTA: fold the pairs
+  // (tile t with tile n-1-t) so that every CTA walks about the same number of key tiles.
+  const long long n_ctas = (long long)BH * ((p.n_q_tiles + 1) / 2);
+  p.fold = (!lm && causal && n_ctas <= current_sms()) ? 1 : 0;
   if (lm) {
     p.lm = *lm;
     p.local = 1;

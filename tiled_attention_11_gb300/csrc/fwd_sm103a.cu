@@ -91,7 +91,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-template <int D, bool CAUSAL, bool VARLEN, bool LOCAL>
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL, bool FOLD = false>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -124,6 +124,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   const int q0 = pair * 2 * C::BM;
   const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, bh);
   if (VARLEN && q0 >= sv.Nq) return;  // this sequence is shorter than the pair: nothing to do
+  // First rows of the two query tiles; folded causal pairs hold tiles pair and
+  // n_q_tiles-1-pair (tile 1 then has at least tile 0's key tiles, as the issuer expects).
+  static_assert(!FOLD || (CAUSAL && !VARLEN && !LOCAL), "folding is for causal dense plain masks");
+  int qa0 = q0, qa1 = q0 + C::BM;
+  bool keep1 = true;  // tile 1's rows are stored
+  if (FOLD) {
+    const int t1 = p.n_q_tiles - 1 - pair;
+    qa0 = pair * C::BM;
+    qa1 = t1 * C::BM;
+    keep1 = t1 != pair;
+  }
   auto o_row = [&](int q) -> size_t {  // element offset of output row q
     return (VARLEN ? ((size_t)(sv.q_tok + q) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + q)) * D;
   };
@@ -152,7 +163,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int lo = chunk * p.split_t, hi = lo + p.split_t;
     return TileSet::make(max(k.a, lo), min(k.g, hi), max(k.L, lo), min(k.hi, hi));
   };
-  const TileSet ks0 = chunk_of(key_set(q0)), ks1 = chunk_of(key_set(q0 + C::BM));
+  const TileSet ks0 = chunk_of(key_set(FOLD ? qa0 : q0)), ks1 = chunk_of(key_set(FOLD ? qa1 : q0 + C::BM));
   // The producer and the UMMA issuer walk the union of both sets in ascending order.
   auto next_kt = [&](int kt) { return min(ks0.next(kt), ks1.next(kt)); };
   // kNone when no row of the pair sees a key (a sequence without keys, or a local mask
@@ -206,7 +217,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
-                      c * C::CHUNK, ty(q0 + t * C::BM), tzq(q0 + t * C::BM));
+                      c * C::CHUNK, ty(FOLD ? (t == 0 ? qa0 : qa1) : q0 + t * C::BM),
+                      tzq(FOLD ? (t == 0 ? qa0 : qa1) : q0 + t * C::BM));
       }
       int issued = 0;
       int j = 0;
@@ -377,8 +389,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int t = warp >> 2;   // which query tile of the pair
     const int wq = warp & 3;   // TMEM lane quarter this warp may access
     const int row = wq * 32 + lane;
-    const int qt0 = q0 + t * C::BM;
+    const int qt0 = FOLD ? (t == 0 ? qa0 : qa1) : q0 + t * C::BM;
     const int q_idx = qt0 + row;
+    const bool keep = !FOLD || t == 0 || keep1;  // this tile's rows are stored
     const TileSet ks = t == 0 ? ks0 : ks1;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t t_s = t_lane + C::TMEM_S + t * 128;
@@ -501,7 +514,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     if (LOCAL && chunk >= 0) {
       // partial record of this key chunk: unnormalised O accumulator, m, l, lr
       if (ok && n_kv > 0 && !warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8)) ok = false;
-      if (ok && q_idx < sv.Nq) {
+      if (ok && keep && q_idx < sv.Nq) {
         const size_t rec = ((size_t)bh * (p.n_gp * 2 * C::BM) + q_idx) * p.n_split + chunk;
         float* po = p.part_o + rec * D;
         if (n_kv > 0) {
@@ -522,7 +535,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             n_kv > 0 ? make_float4(m, l, lr, 0.f) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
       }
     } else if (ok && n_kv == 0) {  // this tile's rows see no key: O = 0, L = -inf
-      if (q_idx < sv.Nq) {
+      if (keep && q_idx < sv.Nq) {
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + o_row(q_idx);
         for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
         p.lse[lse_idx(q_idx)] = -INFINITY;
@@ -546,12 +559,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         w1.y = pack_bf16(as_f(o[10]) * inv_l, as_f(o[11]) * inv_l);
         w1.z = pack_bf16(as_f(o[12]) * inv_l, as_f(o[13]) * inv_l);
         w1.w = pack_bf16(as_f(o[14]) * inv_l, as_f(o[15]) * inv_l);
-        if (q_idx < sv.Nq) {
+        if (keep && q_idx < sv.Nq) {
           reinterpret_cast<uint4*>(orow + g * 16)[0] = w0;
           reinterpret_cast<uint4*>(orow + g * 16)[1] = w1;
         }
       }
-      if (q_idx < sv.Nq)
+      if (keep && q_idx < sv.Nq)
         p.lse[lse_idx(q_idx)] = (LOCAL && l == 0.f) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
     }
   }
@@ -603,11 +616,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const FwdCombineParams p) 
     p.lse[(size_t)bh * p.Nq + r] = lsum > 0.f ? (M + log2f(lsum)) * 0.69314718055994530942f : -INFINITY;
 }
 
-template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false, bool FOLD = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                      int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL, VARLEN, LOCAL>;
+  auto kern = fwd_kernel<D, CAUSAL, VARLEN, LOCAL, FOLD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   const int n_pairs = (p.n_q_tiles + 1) / 2;
@@ -646,6 +659,7 @@ cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensor
     if (p.va.cu_q)                                                                                 \
       return causal ? fwd::launch_t<DD, true, true>(tq, tk, tv, p, BH, st)                         \
                     : fwd::launch_t<DD, false, true>(tq, tk, tv, p, BH, st);                       \
+    if (causal && p.fold) return fwd::launch_t<DD, true, false, false, true>(tq, tk, tv, p, BH, st); \
     return causal ? fwd::launch_t<DD, true, false>(tq, tk, tv, p, BH, st)                          \
                   : fwd::launch_t<DD, false, false>(tq, tk, tv, p, BH, st);
   switch (D) {
