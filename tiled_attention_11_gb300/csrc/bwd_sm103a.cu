@@ -67,14 +67,17 @@ struct Cfg {
   static constexpr int B_SF = 1 + 2 * NS;    // [2] S^T in TMEM buffer b
   static constexpr int B_DPF = 3 + 2 * NS;   // dP^T in TMEM
   static constexpr int B_PF = 4 + 2 * NS;    // [2] P^T in TMEM buffer b (compute warps)
-  static constexpr int B_DSF = 6 + 2 * NS;   // dS^T in shared memory (compute warps)
-  static constexpr int B_DQF = 7 + 2 * NS;   // [2] dQ^T MMA of a step done: its dS^T smem buffer is free
-  static constexpr int B_DQR = 9 + 2 * NS;   // [2] dQ^T in TMEM buffer b, ready for the dQ warpgroup
-  static constexpr int B_DQE = 11 + 2 * NS;  // [2] dQ^T drained from TMEM buffer b (buffer free)
-  static constexpr int B_KT = 13 + 2 * NS;   // K^T written into TMEM
-  static constexpr int B_DPE = 14 + 2 * NS;  // dP^T loaded by the compute warps (its TMEM columns free)
-  static constexpr int B_DRAIN = 15 + 2 * NS;  // [2] one per issuing thread
-  static constexpr int NBAR = 17 + 2 * NS;
+  // [2] dS^T in shared memory buffer b (compute warps).  One per buffer: dP^T(i+1) waits only
+  // for the compute warps to have loaded dP^T(i), so they can publish dS^T(i) and dS^T(i+1)
+  // before issuer B waits for dS^T(i); dS^T(i+2) needs dQ^T(i), which B issues after that wait.
+  static constexpr int B_DSF = 6 + 2 * NS;
+  static constexpr int B_DQF = 8 + 2 * NS;   // [2] dQ^T MMA of a step done: its dS^T smem buffer is free
+  static constexpr int B_DQR = 10 + 2 * NS;  // [2] dQ^T in TMEM buffer b, ready for the dQ warpgroup
+  static constexpr int B_DQE = 12 + 2 * NS;  // [2] dQ^T drained from TMEM buffer b (buffer free)
+  static constexpr int B_KT = 14 + 2 * NS;   // K^T written into TMEM
+  static constexpr int B_DPE = 15 + 2 * NS;  // dP^T loaded by the compute warps (its TMEM columns free)
+  static constexpr int B_DRAIN = 16 + 2 * NS;  // [2] one per issuing thread
+  static constexpr int NBAR = 18 + 2 * NS;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
   // warps 0-3: dQ warpgroup, 4-11: two compute warpgroups, 12: TMA producer,
@@ -192,13 +195,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars[C::B_SF + b], 1);
       mbar_init(&bars[C::B_PF + b], 256);
+      mbar_init(&bars[C::B_DSF + b], 256);
       mbar_init(&bars[C::B_DQF + b], 1);
       mbar_init(&bars[C::B_DQR + b], 1);
       mbar_init(&bars[C::B_DQE + b], 128);
       mbar_init(&bars[C::B_DRAIN + b], 1);
     }
     mbar_init(&bars[C::B_DPF], 1);
-    mbar_init(&bars[C::B_DSF], 256);
     mbar_init(&bars[C::B_KT], 128);
     mbar_init(&bars[C::B_DPE], 256);
     *abort_flag = 0;
@@ -323,7 +326,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // dK += dS^T Q_i and dQ_i^T = K^T dS^T once dS^T is in shared memory buffer b (one
         // copy serves both: 128-byte swizzled rows of 64 queries per key are the K-major A
         // layout of dK and the MN-major B layout of dQ^T)
-        if (!(ok = mbar_wait(&bars[C::B_DSF], it & 1, wc, 36))) break;
+        if (!(ok = mbar_wait(&bars[C::B_DSF + b], (it >> 1) & 1, wc, 36))) break;
         if (it == 0 && !(ok = mbar_wait(&bars[C::B_KT], 0, wc, 47))) break;
         tc_fence_after();
         const uint64_t dsa = desc_adv(dSa, (uint32_t)(b * C::DS_BYTES));
@@ -432,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         *reinterpret_cast<uint4*>(dsrow + phys * 16) = make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bars[C::B_DSF]);
+      mbar_arrive(&bars[C::B_DSF + (it & 1)]);
     }
 
     // epilogue: WG0 writes dK = scale * acc, WG1 writes dV; the last dQ commit covers both
