@@ -375,7 +375,10 @@ def run_table(args):
     dense_rows = not (args.varlen_only or args.window_only or args.fp8_only)
     ex2 = _lib.ex2_rate(dev) if dense_rows else 0.0
     if dense_rows:
-        print(f"exp2 roof (fa_ex2_probe, special-function units): {ex2 / 1e12:.2f} T exp2/s")
+        print(f"exp2 roof (fa_ex2_probe, special-function units): {ex2 / 1e12:.2f} T exp2/s; "
+              f"tensor roof for the score GEMM's UMMA shape (fa_umma_probe): {_lib.umma_rate(dev) / 1e12:.0f} "
+              f"TFLOP/s at the running clock; % peak columns use the measured sustained cuBLAS peak "
+              f"{sustained:.1f} TFLOP/s")
     print("| workload | fwd ms | fwd TFLOP/s | fwd % peak | bwd ms | bwd TFLOP/s | bwd % peak | fwd GB/s (% HBM) "
           "| step ms direct / CUDA graph | L2 flush | exp2 % of roof fwd / bwd |")
     print("|---|---|---|---|---|---|---|---|---|---|---|")

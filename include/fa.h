@@ -123,6 +123,18 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
 int fa_ex2_probe(float* out, int n_blocks, int iters, cudaStream_t stream);
 
 /*
+ * Measurement hook (no counterpart on the pages): the tensor core's rate for the score
+ * GEMM's UMMA shape (M = N = 128, K = 16, bf16 operands from 128-byte swizzled K-major
+ * shared-memory tiles, fp32 accumulate in TMEM).  Launches n_ctas CTAs (one per SM at
+ * most resident); each issues `iters` groups of 8 such UMMAs back to back from one
+ * thread, i.e. n_ctas * iters * 8 * 2*128*128*16 FLOPs, and waits (bounded, like every
+ * wait in this library) for them to complete.  Time it with CUDA events on `stream`.
+ * Returns FA_ERR_INVALID_ARG (n_ctas outside [1, 65535], iters outside [1, 65536]),
+ * FA_ERR_DEVICE (not sm_103) or FA_ERR_LAUNCH; a timeout is recorded in the status word.
+ */
+int fa_umma_probe(int n_ctas, int iters, cudaStream_t stream);
+
+/*
  * Timing hook for measurement tools (no counterpart on the pages): while both
  * events are non-null, every fa_bwd records `begin` on its stream immediately
  * before launching its main tensor-core kernel and `end` immediately after it,

@@ -251,3 +251,11 @@ def test_ex2_probe_validation(L):
     assert L.fa_ex2_probe(out, 4, (1 << 20) + 1, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_ex2_probe(vp(ptrs(1)[0] + 2), 4, 8, None) == _lib.FA_ERR_MISALIGNED
     assert L.fa_ex2_probe(out, 4, 8, None) == _lib.FA_ERR_DEVICE
+
+
+def test_umma_probe_validation(L):
+    assert L.fa_umma_probe(0, 8, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_umma_probe(65536, 8, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_umma_probe(4, 0, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_umma_probe(4, (1 << 16) + 1, None) == _lib.FA_ERR_INVALID_ARG
+    assert L.fa_umma_probe(4, 8, None) == _lib.FA_ERR_DEVICE

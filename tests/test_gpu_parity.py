@@ -310,3 +310,13 @@ def test_repeated_runs_are_identical(p):
         assert err <= 1e-2 * dq0.float().abs().max().item(), err
     torch.cuda.synchronize()
     assert _lib.fa_device_status()[0] == _lib.FA_OK
+
+
+def test_umma_probe_rate():
+    # the score GEMM's UMMA shape back to back on every SM: within the hardware's range
+    # (8192 bf16 FLOP per SM-clock x 152 SMs x ~2 GHz ~ 2.5 PFLOP/s), no timeout recorded
+    _lib.fa_device_status(reset=True)
+    rate = _lib.umma_rate(iters=256)
+    torch.cuda.synchronize()
+    assert _lib.fa_device_status()[0] == _lib.FA_OK
+    assert 1.0e15 < rate < 3.5e15, rate

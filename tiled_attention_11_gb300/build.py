@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libta11_fa.so")
-SOURCES = ["fa_api.cu", "fwd_sm103a.cu", "bwd_sm103a.cu", "fwd_fp8_sm103a.cu", "quant_sm103a.cu"]
+SOURCES = ["fa_api.cu", "fwd_sm103a.cu", "bwd_sm103a.cu", "fwd_fp8_sm103a.cu", "quant_sm103a.cu", "probe_sm103a.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]

@@ -510,6 +510,16 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream) {
   return ta11::launch_wait_probe(limit_ns, status, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+int fa_umma_probe(int n_ctas, int iters, cudaStream_t stream) {
+  if (n_ctas < 1 || n_ctas > 65535 || iters < 1 || iters > (1 << 16)) return FA_ERR_INVALID_ARG;
+  unsigned* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != FA_OK) return rc;
+  return ta11::launch_umma_probe(n_ctas, iters, g_wait_limit_ns.load(), status, stream) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_LAUNCH;
+}
+
 int fa_ex2_probe(float* out, int n_blocks, int iters, cudaStream_t stream) {
   if (!out || n_blocks < 1 || n_blocks > 65535 || iters < 1 || iters > (1 << 20)) return FA_ERR_INVALID_ARG;
   if (!aligned(out, 4)) return FA_ERR_MISALIGNED;
