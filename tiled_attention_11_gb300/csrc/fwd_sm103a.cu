@@ -91,7 +91,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-template <int D, bool CAUSAL, bool VARLEN, bool LOCAL, bool FOLD = false>
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -124,17 +124,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   const int q0 = pair * 2 * C::BM;
   const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, bh);
   if (VARLEN && q0 >= sv.Nq) return;  // this sequence is shorter than the pair: nothing to do
-  // First rows of the two query tiles; folded causal pairs hold tiles pair and
-  // n_q_tiles-1-pair (tile 1 then has at least tile 0's key tiles, as the issuer expects).
-  static_assert(!FOLD || (CAUSAL && !VARLEN && !LOCAL), "folding is for causal dense plain masks");
-  int qa0 = q0, qa1 = q0 + C::BM;
-  bool keep1 = true;  // tile 1's rows are stored
-  if (FOLD) {
-    const int t1 = p.n_q_tiles - 1 - pair;
-    qa0 = pair * C::BM;
-    qa1 = t1 * C::BM;
-    keep1 = t1 != pair;
-  }
   auto o_row = [&](int q) -> size_t {  // element offset of output row q
     return (VARLEN ? ((size_t)(sv.q_tok + q) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + q)) * D;
   };
@@ -163,7 +152,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int lo = chunk * p.split_t, hi = lo + p.split_t;
     return TileSet::make(max(k.a, lo), min(k.g, hi), max(k.L, lo), min(k.hi, hi));
   };
-  const TileSet ks0 = chunk_of(key_set(FOLD ? qa0 : q0)), ks1 = chunk_of(key_set(FOLD ? qa1 : q0 + C::BM));
+  const TileSet ks0 = chunk_of(key_set(q0)), ks1 = chunk_of(key_set(q0 + C::BM));
   // The producer and the UMMA issuer walk the union of both sets in ascending order.
   auto next_kt = [&](int kt) { return min(ks0.next(kt), ks1.next(kt)); };
   // kNone when no row of the pair sees a key (a sequence without keys, or a local mask
@@ -217,8 +206,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
-                      c * C::CHUNK, ty(FOLD ? (t == 0 ? qa0 : qa1) : q0 + t * C::BM),
-                      tzq(FOLD ? (t == 0 ? qa0 : qa1) : q0 + t * C::BM));
+                      c * C::CHUNK, ty(q0 + t * C::BM), tzq(q0 + t * C::BM));
       }
       int issued = 0;
       int j = 0;
@@ -389,9 +377,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int t = warp >> 2;   // which query tile of the pair
     const int wq = warp & 3;   // TMEM lane quarter this warp may access
     const int row = wq * 32 + lane;
-    const int qt0 = FOLD ? (t == 0 ? qa0 : qa1) : q0 + t * C::BM;
+    const int qt0 = q0 + t * C::BM;
     const int q_idx = qt0 + row;
-    const bool keep = !FOLD || t == 0 || keep1;  // this tile's rows are stored
     const TileSet ks = t == 0 ? ks0 : ks1;
     const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t t_s = t_lane + C::TMEM_S + t * 128;
@@ -514,7 +501,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     if (LOCAL && chunk >= 0) {
       // partial record of this key chunk: unnormalised O accumulator, m, l, lr
       if (ok && n_kv > 0 && !warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8)) ok = false;
-      if (ok && keep && q_idx < sv.Nq) {
+      if (ok && q_idx < sv.Nq) {
         const size_t rec = ((size_t)bh * (p.n_gp * 2 * C::BM) + q_idx) * p.n_split + chunk;
         float* po = p.part_o + rec * D;
         if (n_kv > 0) {
@@ -535,7 +522,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             n_kv > 0 ? make_float4(m, l, lr, 0.f) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
       }
     } else if (ok && n_kv == 0) {  // this tile's rows see no key: O = 0, L = -inf
-      if (keep && q_idx < sv.Nq) {
+      if (q_idx < sv.Nq) {
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + o_row(q_idx);
         for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
         p.lse[lse_idx(q_idx)] = -INFINITY;
@@ -559,12 +546,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         w1.y = pack_bf16(as_f(o[10]) * inv_l, as_f(o[11]) * inv_l);
         w1.z = pack_bf16(as_f(o[12]) * inv_l, as_f(o[13]) * inv_l);
         w1.w = pack_bf16(as_f(o[14]) * inv_l, as_f(o[15]) * inv_l);
-        if (keep && q_idx < sv.Nq) {
+        if (q_idx < sv.Nq) {
           reinterpret_cast<uint4*>(orow + g * 16)[0] = w0;
           reinterpret_cast<uint4*>(orow + g * 16)[1] = w1;
         }
       }
-      if (keep && q_idx < sv.Nq)
+      if (q_idx < sv.Nq)
         p.lse[lse_idx(q_idx)] = (LOCAL && l == 0.f) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
     }
   }
@@ -616,11 +603,365 @@ __global__ void __launch_bounds__(256) combine_kernel(const FwdCombineParams p) 
     p.lse[(size_t)bh * p.Nq + r] = lsum > 0.f ? (M + log2f(lsum)) * 0.69314718055994530942f : -INFINITY;
 }
 
-template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false, bool FOLD = false>
+// ------------------------------------------------------------------------------------
+// Plain masks, dense layout: the CTA's two query tiles one after the other, S double
+// buffered.  Step g of the CTA is (query tile t, key tile kt): tile 0's key tiles, then
+// tile 1's.  S(g) goes to TMEM buffer g & 1 and S(g+2) is issued right after P(g) V, so
+// the tensor core computes the next scores while one softmax warpgroup (one thread per
+// query row) works on the current ones; each tile keeps its own O accumulator, and the
+// epilogue of both comes at the end.  Barriers reuse the two-tile kernel's slots:
+//   Q[t] tile t loaded; KF/VF/KE/VE the K and V ring; SF[b] S in buffer b; PF[b] P in
+//   buffer b (128 arrivals); O[b] the P V of a step with buffer b done; drain.
+// ------------------------------------------------------------------------------------
+template <int D>
+struct SeqCfg {
+  static constexpr int THREADS = 192;        // softmax warpgroup, TMA warp, UMMA warp
+  static constexpr int W_PRODUCER = 4, W_MMA = 5;
+};
+
+template <int D, bool CAUSAL, bool FOLD>
+__global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
+    fwd_seq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = Cfg<D>;
+  using S = SeqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+  // heaviest pairs first; folded pairs hold tiles pair and n_q_tiles-1-pair
+  const int pair = (int)gridDim.x - 1 - (int)blockIdx.x;
+  const int bh = blockIdx.y;
+  int qa[2] = {pair * 2 * C::BM, pair * 2 * C::BM + C::BM};
+  if (FOLD) {
+    qa[0] = pair * C::BM;
+    qa[1] = (p.n_q_tiles - 1 - pair) * C::BM;
+  }
+  const int nkt = (p.Nk + C::BN - 1) / C::BN;
+  // key tiles of a query tile: [0, hi); none for a tile past the rows (or the folded
+  // middle tile's duplicate)
+  auto n_keys = [&](int t) -> int {
+    if (qa[t] >= p.Nq || (FOLD && t == 1 && qa[1] == qa[0])) return 0;
+    return CAUSAL ? min(nkt, qa[t] / C::BM + 1) : nkt;
+  };
+  const int n0 = n_keys(0), n1 = n_keys(1), N = n0 + n1;
+  auto tile_of = [&](int g) { return g < n0 ? 0 : 1; };
+  auto kt_of = [&](int g) { return g < n0 ? g : g - n0; };
+  const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars[C::B_Q + t], 1);
+      mbar_init(&bars[C::B_SF + t], 1);
+      mbar_init(&bars[C::B_PF + t], 128);
+      mbar_init(&bars[C::B_O + t], 1);
+    }
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bars[C::B_KF + s], 1);
+      mbar_init(&bars[C::B_VF + s], 1);
+      mbar_init(&bars[C::B_KE + s], 1);
+      mbar_init(&bars[C::B_VE + s], 1);
+    }
+    mbar_init(&bars[C::B_DRAIN], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == S::W_MMA) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == S::W_PRODUCER) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && N > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int t = 0; t < 2; ++t) {
+        if ((t == 0 ? n0 : n1) == 0) continue;
+        mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
+                      c * C::CHUNK, qa[t], bh);
+      }
+      int issued = 0;
+      for (int g = 0; g < N; ++g) {
+        const int s = g % C::NS, kt = kt_of(g);
+        if (g >= C::NS && !mbar_wait(&bars[C::B_KE + s], ((g / C::NS) - 1) & 1, wc, 1)) break;
+        mbar_arrive_expect_tx(&bars[C::B_KF + s], C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
+                      c * C::CHUNK, kt * C::BN, bh);
+        if (g >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((g / C::NS) - 1) & 1, wc, 1)) {
+          issued = g;  // K(g) is in flight; the drain below waits for it
+          mbar_wait(&bars[C::B_KF + s], (g / C::NS) & 1, wc, 24);
+          break;
+        }
+        mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
+                      c * C::CHUNK, kt * C::BN, bh);
+        issued = g + 1;
+      }
+      if (*abort_flag) {
+        // Let every copy already issued land before the CTA can exit.
+        volatile int no_abort = 0;
+        const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+        const int first = issued > C::NS ? issued - C::NS : 0;
+        for (int g = first; g < issued; ++g) {
+          const int s = g % C::NS;
+          mbar_wait(&bars[C::B_KF + s], (g / C::NS) & 1, w2, 20);
+          mbar_wait(&bars[C::B_VF + s], (g / C::NS) & 1, w2, 21);
+        }
+        for (int t = 0; t < 2; ++t)
+          if ((t == 0 ? n0 : n1) > 0) mbar_wait(&bars[C::B_Q + t], 0, w2, 22);
+      }
+    }
+  } else if (warp == S::W_MMA) {
+    // ---------------------------------------------------------------- UMMA issuer
+    if (lane == 0 && N > 0) {
+      const uint64_t dq0 = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);
+      const uint64_t dk0 = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);
+      const uint64_t dv0 = sdesc(sbase + C::OFF_V, C::CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);
+      auto issue_s = [&](int g) {  // S(g) = Q_t K_kt^T into buffer g & 1; K_kt read for the last time
+        const int s = g % C::NS;
+        const uint64_t dq = desc_adv(dq0, (uint32_t)(tile_of(g) * C::TILE_BYTES));
+        const uint64_t dk = desc_adv(dk0, (uint32_t)(s * C::TILE_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + C::TMEM_S + (uint32_t)((g & 1) * 128), desc_adv(dq, kmajor_off<D>(kk)),
+                  desc_adv(dk, kmajor_off<D>(kk)), C::IDESC_S, kk > 0 ? 1u : 0u);
+        umma_commit(&bars[C::B_SF + (g & 1)]);
+        umma_commit(&bars[C::B_KE + s]);
+      };
+      auto issue_pv = [&](int g) {  // O_t (+)= P(g) V_kt, P read from buffer g & 1
+        const int s = g % C::NS;
+        const uint64_t dv = desc_adv(dv0, (uint32_t)(s * C::TILE_BYTES));
+        const uint32_t o = tmem + C::TMEM_O + (uint32_t)(tile_of(g) * D);
+        const bool acc = kt_of(g) > 0;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          umma_ts(o, tmem + C::TMEM_S + (uint32_t)((g & 1) * 128) + kk * 8,
+                  desc_adv(dv, (uint32_t)(kk * 16 * C::ROWB)), C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[C::B_O + (g & 1)]);
+        umma_commit(&bars[C::B_VE + s]);
+      };
+      // S(g) needs its Q tile (waited once per tile) and K in ring slot g % NS
+      bool q_ready[2] = {false, false};
+      auto s_ready = [&](int g) -> bool {
+        const int t = tile_of(g);
+        if (!q_ready[t]) {
+          if (!mbar_wait(&bars[C::B_Q + t], 0, wc, 2)) return false;
+          q_ready[t] = true;
+        }
+        return mbar_wait(&bars[C::B_KF + g % C::NS], (g / C::NS) & 1, wc, 3);
+      };
+      bool ok = s_ready(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        if (N > 1 && (ok = s_ready(1))) {
+          tc_fence_after();
+          issue_s(1);
+        }
+      }
+      for (int g = 0; ok && g < N; ++g) {
+        // P(g) V: P from the softmax, V in slot g % NS
+        if (!(ok = mbar_wait(&bars[C::B_PF + (g & 1)], (g >> 1) & 1, wc, 4))) break;
+        if (!(ok = mbar_wait(&bars[C::B_VF + g % C::NS], (g / C::NS) & 1, wc, 5))) break;
+        tc_fence_after();
+        issue_pv(g);
+        // S(g+2) over buffer g & 1, after P(g) V has read it (in-order UMMA)
+        if (g + 2 < N) {
+          if (!(ok = s_ready(g + 2))) break;
+          tc_fence_after();
+          issue_s(g + 2);
+        }
+      }
+      umma_commit(&bars[C::B_DRAIN]);
+      volatile int no_abort = 0;
+      const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+      mbar_wait(&bars[C::B_DRAIN], 0, w2, 23);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax warpgroup
+    const int row = warp * 32 + lane;  // query row of the tile (TMEM lane)
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY, l = 0.f, lr = 0.f;  // the current tile's running state
+    float st_m[2] = {-INFINITY, -INFINITY}, st_l[2] = {0.f, 0.f}, st_lr[2] = {0.f, 0.f};
+    bool ok = true;
+    for (int g = 0; g < N; ++g) {
+      const int t = tile_of(g), kt = kt_of(g), b = g & 1;
+      if (kt == 0 && g > 0) {  // tile 0 done: keep its state for the epilogue
+        st_m[0] = m;
+        st_l[0] = l;
+        st_lr[0] = lr;
+        m = -INFINITY;
+        l = lr = 0.f;
+      }
+      const int qt0 = qa[t], q_idx = qt0 + row;
+      const uint32_t t_s = t_lane + C::TMEM_S + (uint32_t)(b * 128);
+      if (!warp_wait(&bars[C::B_SF + b], (g >> 1) & 1, wc, 6)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) tmem_ld32(t_s + gg * 32, s[gg]);
+      tmem_wait_ld(s[0]);
+      reg_tie(s[1]);
+      reg_tie(s[2]);
+      reg_tie(s[3]);
+      // mask keys past Nk and (causal) keys after this row's query index
+      const int ka = kt * C::BN;
+      if ((ka + C::BN > p.Nk) || (CAUSAL && (ka + C::BN - 1 > qt0))) {
+        int lim = p.Nk - 1 - ka;  // last visible column of this tile
+        if (CAUSAL) lim = min(lim, q_idx - ka);
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg)
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (gg * 32 + c > lim) s[gg][c] = __float_as_uint(-INFINITY);
+      }
+      // row max: eight independent chains of 3-input max, then a short tree
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t* v = &s[i >> 1][(i & 1) * 16];
+        float a = fmax3(as_f(v[0]), as_f(v[1]), as_f(v[2]));
+#pragma unroll
+        for (int e = 3; e < 15; e += 2) a = fmax3(a, as_f(v[e]), as_f(v[e + 1]));
+        mx8[i] = fmaxf(a, as_f(v[15]));
+      }
+      const float mx2 =
+          fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * sl2;
+      float alpha = 1.f;
+      if (mx2 > m + kTau) {  // also taken on a tile's first key tile, where m = -inf
+        alpha = ex2(m - mx2);
+        m = mx2;
+      }
+      // p = 2^(S*c - m) two lanes at a time; l and lr accumulate in packed pairs
+      const uint64_t c2 = f2pack(sl2, sl2), nm2 = f2pack(-m, -m);
+      uint64_t l2[4], lr2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) l2[i] = lr2[i] = 0ull;
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float x0, x1;
+          f2unpack(ffma2(f2pack(as_f(s[gg][c]), as_f(s[gg][c + 1])), c2, nm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          const uint32_t w = pack_bf16(p0, p1);
+          l2[(c >> 1) & 3] = fadd2(l2[(c >> 1) & 3], f2pack(p0, p1));
+          lr2[(c >> 1) & 3] = fadd2(lr2[(c >> 1) & 3], f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+          pk[c >> 1] = w;
+        }
+        tmem_st16(t_s + gg * 16, pk);
+      }
+      float la[8], lb[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f2unpack(l2[i], la[2 * i], la[2 * i + 1]);
+        f2unpack(lr2[i], lb[2 * i], lb[2 * i + 1]);
+      }
+      l = l * alpha + (((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7])));
+      lr = lr * alpha + (((lb[0] + lb[1]) + (lb[2] + lb[3])) + ((lb[4] + lb[5]) + (lb[6] + lb[7])));
+      // rows whose subtracted max moved rescale O, once P(g-1) V (the tile's previous step)
+      // has landed: it was issued before S(g+1), not before S(g), so it is waited for here
+      if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!warp_wait(&bars[C::B_O + ((g - 1) & 1)], ((g - 1) >> 1) & 1, wc, 7)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_o = t_lane + C::TMEM_O + (uint32_t)(t * D);
+#pragma unroll
+        for (int gg = 0; gg < D / 16; ++gg) {
+          uint32_t o[16];
+          tmem_ld16(t_o + gg * 16, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(as_f(o[c]) * alpha);
+          tmem_st16(t_o + gg * 16, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_PF + b]);
+    }
+    st_m[n1 > 0 ? 1 : 0] = m;
+    st_l[n1 > 0 ? 1 : 0] = l;
+    st_lr[n1 > 0 ? 1 : 0] = lr;
+    // epilogue: the last P V done means every earlier one is (in-order UMMA)
+    if (ok && N > 0 && warp_wait(&bars[C::B_O + ((N - 1) & 1)], ((N - 1) >> 1) & 1, wc, 8)) {
+      tc_fence_after();
+      for (int t = 0; t < 2; ++t) {
+        if ((t == 0 ? n0 : n1) == 0) continue;
+        const int q_idx = qa[t] + row;
+        const float inv_l = 1.f / st_lr[t];
+        const uint32_t t_o = t_lane + C::TMEM_O + (uint32_t)(t * D);
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.Nq + q_idx) * D;
+#pragma unroll
+        for (int gg = 0; gg < D / 16; ++gg) {
+          uint32_t o[16];
+          tmem_ld16(t_o + gg * 16, o);
+          tmem_wait_ld(o);
+          uint4 w0, w1;
+          w0.x = pack_bf16(as_f(o[0]) * inv_l, as_f(o[1]) * inv_l);
+          w0.y = pack_bf16(as_f(o[2]) * inv_l, as_f(o[3]) * inv_l);
+          w0.z = pack_bf16(as_f(o[4]) * inv_l, as_f(o[5]) * inv_l);
+          w0.w = pack_bf16(as_f(o[6]) * inv_l, as_f(o[7]) * inv_l);
+          w1.x = pack_bf16(as_f(o[8]) * inv_l, as_f(o[9]) * inv_l);
+          w1.y = pack_bf16(as_f(o[10]) * inv_l, as_f(o[11]) * inv_l);
+          w1.z = pack_bf16(as_f(o[12]) * inv_l, as_f(o[13]) * inv_l);
+          w1.w = pack_bf16(as_f(o[14]) * inv_l, as_f(o[15]) * inv_l);
+          if (q_idx < p.Nq) {
+            reinterpret_cast<uint4*>(orow + gg * 16)[0] = w0;
+            reinterpret_cast<uint4*>(orow + gg * 16)[1] = w1;
+          }
+        }
+        if (q_idx < p.Nq) p.lse[(size_t)bh * p.Nq + q_idx] = (st_m[t] + log2f(st_l[t])) * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == S::W_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool CAUSAL, bool FOLD>
+cudaError_t launch_seq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                         int BH, cudaStream_t st) {
+  using C = Cfg<D>;
+  auto kern = fwd_seq_kernel<D, CAUSAL, FOLD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH);
+  kern<<<grid, SeqCfg<D>::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                      int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = fwd_kernel<D, CAUSAL, VARLEN, LOCAL, FOLD>;
+  auto kern = fwd_kernel<D, CAUSAL, VARLEN, LOCAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   const int n_pairs = (p.n_q_tiles + 1) / 2;
@@ -659,7 +1000,7 @@ cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensor
     if (p.va.cu_q)                                                                                 \
       return causal ? fwd::launch_t<DD, true, true>(tq, tk, tv, p, BH, st)                         \
                     : fwd::launch_t<DD, false, true>(tq, tk, tv, p, BH, st);                       \
-    if (causal && p.fold) return fwd::launch_t<DD, true, false, false, true>(tq, tk, tv, p, BH, st); \
+    if (causal && p.fold) return fwd::launch_seq_t<DD, true, true>(tq, tk, tv, p, BH, st);         \
     return causal ? fwd::launch_t<DD, true, false>(tq, tk, tv, p, BH, st)                          \
                   : fwd::launch_t<DD, false, false>(tq, tk, tv, p, BH, st);
   switch (D) {
