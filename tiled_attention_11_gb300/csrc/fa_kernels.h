@@ -103,9 +103,9 @@ struct FwdParams {
   int n_gp, n_split, split_t;
   float* part_o;        // [B*H][n_gp*256][n_split][D]
   float* part_ml;       // [B*H][n_gp*256][n_split][4]: m, l, lr, unused
-  // Causal, dense layout, plain mask: CTA `pair` holds query tiles pair and
-  // n_q_tiles-1-pair instead of 2*pair and 2*pair+1, so every CTA walks about the same
-  // number of key tiles (the middle tile of an odd count is computed twice, stored once).
+  // Causal, dense layout, plain mask, launch of one wave: the sequential-tile kernel,
+  // whose CTA `pair` holds query tiles pair and n_q_tiles-1-pair instead of 2*pair and
+  // 2*pair+1, so every CTA walks about the same number of key tiles.
   int fold;
 };
 

@@ -26,6 +26,9 @@
 //              so the tensor core works on one tile while the other's softmax runs.
 //   TMEM (512 columns): S0 | S1 (128 fp32 each; P as bf16 overwrites the first 64)
 //                       | O0 | O1 (D fp32 each)
+// Causal launches that fit in one wave use fwd_seq_kernel instead (see there): the same
+// pair of tiles, folded (tile t with n-1-t) and walked one after the other by one softmax
+// warpgroup with S double-buffered, so no CTA is much longer than the others.
 // Every wait is bounded; a timeout records FA_ERR_TIMEOUT in the status word and
 // the CTA drains its in-flight copies and MMAs before freeing TMEM.
 #include "fa_kernels.h"
