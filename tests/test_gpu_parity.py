@@ -320,3 +320,33 @@ def test_umma_probe_rate():
     torch.cuda.synchronize()
     assert _lib.fa_device_status()[0] == _lib.FA_OK
     assert 1.0e15 < rate < 3.5e15, rate
+
+
+def test_tensors_beyond_2_31_elements():
+    # 65535 heads (the grid's maximum) x 260 rows x D = 128: 2.18e9 elements per tensor, so
+    # the last heads live past element 2^31 and every offset must be 64-bit.  Inputs are drawn
+    # on the device (seeded); the oracle checks the first, a middle and the last head.
+    B, H, N, D = 255, 257, 260, 128
+    assert B * H * N * D > 2 ** 31
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev).manual_seed(21)
+    q, k, v, do = (torch.randn((B, H, N, D), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                   for _ in range(4))
+    scale = D ** -0.5
+    o, lse = _lib.forward(q, k, v, True, scale)
+    dq, dk, dv = _lib.backward(q, k, v, o, lse, do, True, scale)
+    torch.cuda.synchronize()
+    assert _lib.fa_device_status()[0] == _lib.FA_OK
+    for bh in (0, (B * H) // 2, B * H - 1):
+        b, h = divmod(bh, H)
+        qh, kh, vh, doh = (f64(t[b, h])[None, None] for t in (q, k, v, do))
+        ro, rl = oracle.attention_forward(qh, kh, vh, scale, True)
+        rdq, rdk, rdv = oracle.attention_backward(qh, kh, vh, doh, scale, True)
+        tag = f"head {bh}"
+        assert_close(tag + " O", f64(o[b, h])[None, None], ro)
+        assert_lse(tag + " L", f64(lse[b, h])[None, None], rl)
+        assert_close(tag + " dQ", f64(dq[b, h])[None, None], rdq)
+        assert_close(tag + " dK", f64(dk[b, h])[None, None], rdk)
+        assert_close(tag + " dV", f64(dv[b, h])[None, None], rdv)
+    del q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
