@@ -297,38 +297,76 @@ def test_planted_mistakes_are_caught(name, old, new):
 # packed variable-length batches: each sequence attended on its own
 # --------------------------------------------------------------------------------------
 
-def test_varlen_equal_lengths_match_dense_layout():
+def pin_varlen_equal_lengths(ref):
+    # equal lengths: the packed layout of the dense oracle's result
     B, H, N, D = 3, 2, 11, 4
     q, k, v, do = (rnd((B, H, N, D), 90 + i) for i in range(4))
     cu = np.arange(B + 1) * N
     pack = lambda x: x.transpose(0, 2, 1, 3).reshape(B * N, H, D)  # noqa: E731
+    ok = True
     for causal in (False, True):
-        o, lse, dq, dk, dv = attn_ref.attention_varlen(pack(q), pack(k), pack(v), pack(do), cu, cu, 0.4, causal)
+        o, lse, dq, dk, dv = ref.attention_varlen(pack(q), pack(k), pack(v), pack(do), cu, cu, 0.4, causal)
         ro, rl = attn_ref.attention_forward(q, k, v, 0.4, causal)
         rdq, rdk, rdv = attn_ref.attention_backward(q, k, v, do, 0.4, causal)
-        assert np.allclose(o, pack(ro), atol=1e-13)
-        assert np.allclose(lse, rl.transpose(1, 0, 2).reshape(H, B * N), atol=1e-13)
-        for a, r in ((dq, rdq), (dk, rdk), (dv, rdv)):
-            assert np.allclose(a, pack(r), atol=1e-12)
+        ok &= bool(np.allclose(o, pack(ro), atol=1e-13))
+        ok &= bool(np.allclose(lse, rl.transpose(1, 0, 2).reshape(H, B * N), atol=1e-13))
+        for a_, r in ((dq, rdq), (dk, rdk), (dv, rdv)):
+            ok &= bool(np.allclose(a_, pack(r), atol=1e-12))
+    return ok
 
 
-def test_varlen_brute_force_ragged_and_cross_lengths():
+def pin_varlen_brute_force(ref):
+    # ragged and cross lengths with empty sequences, each (sequence, head) by brute force
     lens_q, lens_k = [3, 0, 5, 1], [4, 2, 5, 0]
     cu_q, cu_k = np.concatenate([[0], np.cumsum(lens_q)]), np.concatenate([[0], np.cumsum(lens_k)])
     H, D = 2, 3
     q, do = rnd((cu_q[-1], H, D), 95), rnd((cu_q[-1], H, D), 96)
     k, v = rnd((cu_k[-1], H, D), 97), rnd((cu_k[-1], H, D), 98)
+    ok = True
     for causal in (False, True):
-        o, lse, dq, dk, dv = attn_ref.attention_varlen(q, k, v, do, cu_q, cu_k, 0.6, causal)
+        o, lse, dq, dk, dv = ref.attention_varlen(q, k, v, do, cu_q, cu_k, 0.6, causal)
         for b in range(4):
             q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
             for h in range(H):
                 if q1 == q0:
                     continue
                 if k1 == k0:
-                    assert np.all(o[q0:q1, h] == 0) and np.all(np.isneginf(lse[h, q0:q1]))
+                    ok &= bool(np.all(o[q0:q1, h] == 0) and np.all(np.isneginf(lse[h, q0:q1])))
                     continue
                 O, L, dQ, dK, dV = _brute_head(q[q0:q1, h], k[k0:k1, h], v[k0:k1, h], do[q0:q1, h], 0.6, causal)
-                assert np.allclose(o[q0:q1, h], O, atol=1e-12) and np.allclose(lse[h, q0:q1], L, atol=1e-12)
-                assert np.allclose(dq[q0:q1, h], dQ, atol=1e-12) and np.allclose(dk[k0:k1, h], dK, atol=1e-12)
-                assert np.allclose(dv[k0:k1, h], dV, atol=1e-12)
+                ok &= bool(np.allclose(o[q0:q1, h], O, atol=1e-12) and np.allclose(lse[h, q0:q1], L, atol=1e-12))
+                ok &= bool(np.allclose(dq[q0:q1, h], dQ, atol=1e-12) and np.allclose(dk[k0:k1, h], dK, atol=1e-12))
+                ok &= bool(np.allclose(dv[k0:k1, h], dV, atol=1e-12))
+    return ok
+
+
+VARLEN_PINS = [pin_varlen_equal_lengths, pin_varlen_brute_force]
+
+
+@pytest.mark.parametrize("pin", VARLEN_PINS, ids=[p.__name__ for p in VARLEN_PINS])
+def test_varlen_oracle_pin(pin):
+    assert pin(attn_ref)
+
+
+VARLEN_MUTATIONS = [
+    ("keys of a sequence taken at the query offsets",
+     "q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])",
+     "q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_q[b]), int(cu_q[b + 1])"),
+    ("last sequence dropped", "for b in range(len(cu_q) - 1):", "for b in range(len(cu_q) - 2):"),
+    ("L of every head written to head 0", "o[q0:q1, h], lse[h, q0:q1] = oo, ll", "o[q0:q1, h], lse[0, q0:q1] = oo, ll"),
+    ("sequences without keys not skipped", "if q1 <= q0 or k1 <= k0:", "if q1 <= q0:"),
+    ("dK written to the query rows", "dq[q0:q1, h], dk[k0:k1, h], dv[k0:k1, h] = gq, gk, gv",
+     "dq[q0:q1, h], dk[q0:q0 + (k1 - k0), h], dv[k0:k1, h] = gq, gk, gv"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", VARLEN_MUTATIONS, ids=[m[0] for m in VARLEN_MUTATIONS])
+def test_varlen_planted_mistakes_are_caught(name, old, new):
+    mut = _mutant(open(attn_ref.__file__).read(), old, new)
+    results = {}
+    for pin in VARLEN_PINS:
+        try:
+            results[pin.__name__] = pin(mut)
+        except Exception:  # a crash is also a caught mistake
+            results[pin.__name__] = False
+    assert not all(results.values()), f"planted mistake '{name}' passed every varlen pin"
