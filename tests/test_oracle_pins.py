@@ -229,6 +229,46 @@ def test_tiled_online_softmax_matches_plain(Bq, Bk, causal):
         assert np.allclose(lse, l2, rtol=0, atol=1e-12)
 
 
+def pin_tiled(ref):
+    # the tiled online update equals the plain definition for any tile sizes
+    ok = True
+    for Bq, Bk in [(1, 1), (3, 3), (5, 16), (16, 7), (128, 128)]:
+        for causal in (False, True):
+            for (nq, nk) in [(37, 37), (37, 53), (53, 37)]:
+                q, k, v = rnd((nq, 8), 60, 3.0), rnd((nk, 8), 61, 3.0), rnd((nk, 8), 62)
+                o, lse = attn_ref.forward_head(q, k, v, 0.35, causal)
+                o2, l2 = ref.tiled_forward_head(q, k, v, 0.35, causal, Bq, Bk)
+                ok &= bool(np.allclose(o, o2, rtol=0, atol=1e-12) and np.allclose(lse, l2, rtol=0, atol=1e-12))
+    return ok
+
+
+TILED_MUTATIONS = [
+    ("alpha not applied to l", "l = alpha * l + P.sum(axis=1)", "l = l + P.sum(axis=1)"),
+    ("o_acc not rescaled", "o_acc = alpha[:, None] * o_acc + P @ v_j", "o_acc = o_acc + P @ v_j"),
+    ("running max not kept", "            m = m_new\n", "            m = S.max(axis=1)\n"),
+    ("causal mask off by one", "S = np.where(qi >= kj, S, -np.inf)", "S = np.where(qi > kj, S, -np.inf)"),
+    ("missing max term in L", "L[i:i + rows] = m + np.log(l)", "L[i:i + rows] = np.log(l)"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", TILED_MUTATIONS, ids=[m[0] for m in TILED_MUTATIONS])
+def test_tiled_planted_mistakes_are_caught(name, old, new):
+    src = open(tiled_ref.__file__).read()
+    assert old in src, f"mutation anchor not found: {old!r}"
+    mod = types.ModuleType("tiled_ref_mutant")
+    exec(compile(src.replace(old, new, 1), "tiled_ref_mutant", "exec"), mod.__dict__)
+    try:
+        with np.errstate(all="ignore"):  # a broken update may produce NaN: that is the point
+            caught = not pin_tiled(mod)
+    except Exception:  # a crash is also a caught mistake
+        caught = True
+    assert caught, f"planted mistake '{name}' passed the tiled pin"
+
+
+def test_tiled_pin_holds():
+    assert pin_tiled(tiled_ref)
+
+
 def test_tiled_matches_torch_library():
     q, k, v = rnd((1, 1, 40, 8), 70), rnd((1, 1, 40, 8), 71), rnd((1, 1, 40, 8), 72)
     to = torch.nn.functional.scaled_dot_product_attention(
