@@ -13,10 +13,10 @@
 //            a TMA ring (causal: starting at the diagonal).  Per query tile, all on
 //            tcgen05 (keys on the M=128 axis):
 //              S^T  = K Q_i^T            -> TMEM   P^T = 2^(S^T c - lse2)  (compute WGs)
-//              dP^T = V dO_i^T           -> TMEM   dS^T = P^T o (dP^T - Dlt)
+//              dP^T = V dO_i^T           -> TMEM   dS^T = P^T o (dP^T - Dlt) -> shared memory
 //              dV  += P^T dO_i   (A = P^T from TMEM)
-//              dK  += dS^T Q_i   (A = dS^T from TMEM)
-//              dQ_i^T = K^T dS^T (A = K^T kept in TMEM, dS^T from shared memory)
+//              dK  += dS^T Q_i   (A = dS^T from shared memory)
+//              dQ_i^T = K^T dS^T (A = K^T kept in TMEM, B = the same dS^T tile)
 //                                   -> TMEM, into the S^T buffer dV has just consumed
 //            Two threads issue the UMMAs: one the score GEMMs S^T, dP^T (which need only
 //            loaded tiles and free TMEM), the other the gradient GEMMs dV, dK, dQ^T
