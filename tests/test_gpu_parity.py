@@ -350,3 +350,12 @@ def test_tensors_beyond_2_31_elements():
         assert_close(tag + " dV", f64(dv[b, h])[None, None], rdv)
     del q, k, v, do, o, lse, dq, dk, dv
     torch.cuda.empty_cache()
+
+
+def test_binding_rejects_tensors_on_another_device(monkeypatch):
+    # the library runs on the current device; a tensor elsewhere is refused, not misused
+    q = torch.zeros(1, 1, 64, 64, dtype=torch.bfloat16, device="cuda")
+    here = torch.cuda.current_device()
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: here + 1)
+    with pytest.raises(ValueError, match="current device"):
+        _lib.forward(q, q, q, causal=False)

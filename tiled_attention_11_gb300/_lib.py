@@ -130,6 +130,9 @@ def _ptr(t: torch.Tensor | None, name: str, dtype) -> int:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if t.get_device() != torch.cuda.current_device():
+        raise ValueError(f"{name} is on cuda:{t.get_device()} but the library runs on the current device, "
+                         f"cuda:{torch.cuda.current_device()} (select it with torch.cuda.device)")
     return t.data_ptr()
 
 
