@@ -83,7 +83,8 @@ size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int D);
  *   workspace: >= fa_bwd_workspace_size(...) bytes of device memory, 256-byte
  *   aligned, owned by the caller, contents on entry ignored (overwritten).
  * o and lse must be the forward's outputs for the same q, k, v, scale, causal.
- * dQ accumulates with fp32 atomics, so it is not bitwise deterministic run to run.
+ * dQ adds every key tile's fp32 contribution in L2 (bulk reduce-adds) in no fixed order,
+ * so it is not bitwise deterministic run to run; dK and dV (and fa_fwd's O, L) are.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
            void* dk, void* dv, int B, int H, int Nq, int Nk, int D, float scale, int causal, void* workspace,
