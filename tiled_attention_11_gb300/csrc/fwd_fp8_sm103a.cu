@@ -133,31 +133,27 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_QK);
         tma_load_3d(smem + C::OFF_Q + t * C::TILE_QK, &tm_q, &bars[C::B_Q + t], 0, q0 + t * C::BM, bh);
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;  // K and V tiles whose copies were started
       for (int j = 0; j < n_kv1; ++j) {
         const int s = j % C::NS;
         if (j >= C::NS && !mbar_wait(&bars[C::B_KE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
         mbar_arrive_expect_tx(&bars[C::B_KF + s], C::TILE_QK);
         tma_load_3d(smem + C::OFF_K + s * C::TILE_QK, &tm_k, &bars[C::B_KF + s], 0, j * C::BN, bh);
-        if (j >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) {
-          issued = j;  // K_j is in flight; let the drain below wait for it
-          mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, wc, 24);
-          break;
-        }
+        k_issued = j + 1;
+        if (j >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
         mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_VT);
         tma_load_3d(smem + C::OFF_V + s * C::TILE_VT, &tm_vt, &bars[C::B_VF + s], j * C::BN, 0, bh);
-        issued = j + 1;
+        v_issued = j + 1;
       }
       if (*abort_flag) {
-        // Let every copy already issued land before the CTA can exit.
+        // Let every copy already started land before the CTA can exit: the last NS of
+        // each ring, one per slot, so that each wait is on its slot's newest phase.
         volatile int no_abort = 0;
         const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
-        const int first = issued > C::NS ? issued - C::NS : 0;
-        for (int j = first; j < issued; ++j) {
-          const int s = j % C::NS;
-          mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, w2, 20);
-          mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, w2, 21);
-        }
+        for (int j = k_issued > C::NS ? k_issued - C::NS : 0; j < k_issued; ++j)
+          mbar_wait(&bars[C::B_KF + j % C::NS], (j / C::NS) & 1, w2, 20);
+        for (int j = v_issued > C::NS ? v_issued - C::NS : 0; j < v_issued; ++j)
+          mbar_wait(&bars[C::B_VF + j % C::NS], (j / C::NS) & 1, w2, 21);
         mbar_wait(&bars[C::B_Q], 0, w2, 22);
         mbar_wait(&bars[C::B_Q + 1], 0, w2, 22);
       }

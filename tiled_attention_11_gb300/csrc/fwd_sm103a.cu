@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
                       c * C::CHUNK, ty(q0 + t * C::BM), tzq(q0 + t * C::BM));
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;  // K and V tiles whose copies were started
       int j = 0;
       for (int kt = first_kt; kt != TileSet::kNone; kt = next_kt(kt), ++j) {
         const int s = j % C::NS;
@@ -220,27 +220,23 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
                       c * C::CHUNK, ty(kt * C::BN), tzk(kt * C::BN));
-        if (j >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) {
-          issued = j;  // K_j is in flight; let the drain below wait for it
-          mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, wc, 24);
-          break;
-        }
+        k_issued = j + 1;
+        if (j >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
         mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
                       c * C::CHUNK, ty(kt * C::BN), tzk(kt * C::BN));
-        issued = j + 1;
+        v_issued = j + 1;
       }
       if (*abort_flag) {
-        // Let every copy already issued land before the CTA can exit.
+        // Let every copy already started land before the CTA can exit: the last NS of
+        // each ring, one per slot, so that each wait is on its slot's newest phase.
         volatile int no_abort = 0;
         const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
-        const int first = issued > C::NS ? issued - C::NS : 0;
-        for (int j = first; j < issued; ++j) {
-          const int s = j % C::NS;
-          mbar_wait(&bars[C::B_KF + s], (j / C::NS) & 1, w2, 20);
-          mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, w2, 21);
-        }
+        for (int j = k_issued > C::NS ? k_issued - C::NS : 0; j < k_issued; ++j)
+          mbar_wait(&bars[C::B_KF + j % C::NS], (j / C::NS) & 1, w2, 20);
+        for (int j = v_issued > C::NS ? v_issued - C::NS : 0; j < v_issued; ++j)
+          mbar_wait(&bars[C::B_VF + j % C::NS], (j / C::NS) & 1, w2, 21);
         for (int t = 0; t < 2; ++t)
           if (has_q[t]) mbar_wait(&bars[C::B_Q + t], 0, w2, 22);
       }
@@ -695,7 +691,7 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
           tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
                       c * C::CHUNK, qa[t], bh);
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;  // steps whose K and V copies were started
       for (int g = 0; g < N; ++g) {
         const int s = g % C::NS, kt = kt_of(g);
         if (g >= C::NS && !mbar_wait(&bars[C::B_KE + s], ((g / C::NS) - 1) & 1, wc, 1)) break;
@@ -703,27 +699,23 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
                       c * C::CHUNK, kt * C::BN, bh);
-        if (g >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((g / C::NS) - 1) & 1, wc, 1)) {
-          issued = g;  // K(g) is in flight; the drain below waits for it
-          mbar_wait(&bars[C::B_KF + s], (g / C::NS) & 1, wc, 24);
-          break;
-        }
+        k_issued = g + 1;
+        if (g >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((g / C::NS) - 1) & 1, wc, 1)) break;
         mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_3d(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
                       c * C::CHUNK, kt * C::BN, bh);
-        issued = g + 1;
+        v_issued = g + 1;
       }
       if (*abort_flag) {
-        // Let every copy already issued land before the CTA can exit.
+        // Let every copy already started land before the CTA can exit: the last NS of
+        // each ring, one per slot, so that each wait is on its slot's newest phase.
         volatile int no_abort = 0;
         const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
-        const int first = issued > C::NS ? issued - C::NS : 0;
-        for (int g = first; g < issued; ++g) {
-          const int s = g % C::NS;
-          mbar_wait(&bars[C::B_KF + s], (g / C::NS) & 1, w2, 20);
-          mbar_wait(&bars[C::B_VF + s], (g / C::NS) & 1, w2, 21);
-        }
+        for (int g = k_issued > C::NS ? k_issued - C::NS : 0; g < k_issued; ++g)
+          mbar_wait(&bars[C::B_KF + g % C::NS], (g / C::NS) & 1, w2, 20);
+        for (int g = v_issued > C::NS ? v_issued - C::NS : 0; g < v_issued; ++g)
+          mbar_wait(&bars[C::B_VF + g % C::NS], (g / C::NS) & 1, w2, 21);
         for (int t = 0; t < 2; ++t)
           if ((t == 0 ? n0 : n1) > 0) mbar_wait(&bars[C::B_Q + t], 0, w2, 22);
       }
