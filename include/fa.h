@@ -15,7 +15,8 @@
  *   - lse is fp32 [B, H, Nq]: the natural-log row logsumexp of the scaled
  *     scores, L_i = m_i + log(sum_j exp(S_ij - m_i)) ([FA2-impl] §3.1, L = m + log l).
  *   - Supported head dims: D in {16, 32, 64, 128}.  B, H, Nq, Nk >= 1;
- *     B*H <= 65535.  scale must be finite and > 0
+ *     B*H <= 65535; Nq, Nk (and the packed totals and maximum lengths of the
+ *     variable-length calls) <= 2^29.  scale must be finite and > 0
  *     (the usual value is 1/sqrt(D), [FA2-impl] §3.1).
  *   - causal != 0 keeps key j for query i iff j <= i on absolute indices
  *     (top-left alignment, [FA2-impl] §4.3), for any Nq, Nk.  Masked keys get

@@ -1,6 +1,9 @@
 """C-ABI checks that need no GPU: the library builds, loads, exports every symbol
 include/fa.h declares, and rejects bad arguments with the documented codes
-before touching a device.  No compute call is made here.
+before touching a device.  No compute call is made here: the pointers are fake,
+never-allocated addresses, so a call whose arguments all pass validation (it would
+go on to launch work) is made only where no CUDA device exists, and there it must
+fail with FA_ERR_DEVICE.
 """
 import ctypes
 import os
@@ -19,6 +22,21 @@ HEADER = os.path.join(ROOT, "include", "fa.h")
 def L():
     build()
     return _lib.lib()
+
+
+def _device_present() -> bool:
+    import torch
+    return torch.cuda.is_available() or os.path.exists("/dev/nvidiactl")
+
+
+DEVICE_PRESENT = _device_present()
+
+
+def reaches_device(call):
+    """Make a call that passes every host check only where no device can run it."""
+    if DEVICE_PRESENT:
+        return
+    assert call() == _lib.FA_ERR_DEVICE
 
 
 def declared_functions():
@@ -87,7 +105,7 @@ def test_fwd_validation_codes(L):
     assert fwd_call(L, q, k, v, q + 1024, lse) == _lib.FA_ERR_INVALID_ARG
     assert fwd_call(L, q, k, v, o, o + 16) == _lib.FA_ERR_INVALID_ARG
     # every argument valid: the only failure left is the missing sm_103 device
-    assert fwd_call(L, q, k, v, o, lse) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: fwd_call(L, q, k, v, o, lse))
 
 
 def test_bwd_validation_codes(L):
@@ -103,7 +121,7 @@ def test_bwd_validation_codes(L):
     assert bwd_call(L, p[:9] + [p[6] + 256]) == _lib.FA_ERR_INVALID_ARG
     # dk overlapping an input
     assert bwd_call(L, p[:7] + [p[0] + 64] + p[8:]) == _lib.FA_ERR_INVALID_ARG
-    assert bwd_call(L, p) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: bwd_call(L, p))
 
 
 def test_workspace_size_formula(L):
@@ -128,14 +146,14 @@ def test_binding_rejects_missing_gpu():
 
 
 def test_wait_probe_needs_device(L):
-    assert L.fa_wait_probe(1000, None) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: L.fa_wait_probe(1000, None))
 
 
 def test_noalloc_size_limit_checked_on_host(L):
     vp = ctypes.c_void_p
     p = [vp(x) for x in ptrs(9)]
     assert L.fa_bwd_noalloc(*p, 4, 32, 4096, 4096, 128, 0.088, 1, None) == _lib.FA_ERR_SCRATCH_LIMIT
-    assert L.fa_bwd_noalloc(*p, 2, 3, 100, 77, 64, 0.125, 1, None) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: L.fa_bwd_noalloc(*p, 2, 3, 100, 77, 64, 0.125, 1, None))
 
 
 def test_varlen_validation_codes(L):
@@ -148,7 +166,7 @@ def test_varlen_validation_codes(L):
     assert call(mq=0) == _lib.FA_ERR_INVALID_ARG
     assert call(D=80) == _lib.FA_ERR_UNSUPPORTED_D
     assert call(cq=vp(ptrs(1)[0] + 2)) == _lib.FA_ERR_MISALIGNED
-    assert call() == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: call())
     rows = 64 * ((100 + 63) // 64 + 3)
     def rnd(x):
         return (x + 255) // 256 * 256
@@ -165,11 +183,11 @@ def test_window_validation_codes(L):
     assert call(q=vp(ptrs(1)[0] + 8)) == _lib.FA_ERR_MISALIGNED
     # any window / global-token values are valid (negative: unbounded, large: clipped)
     for wl, g in ((-1, 0), (0, 0), (1 << 30, 1 << 30), (-5, -3)):
-        assert call(wl=wl, g=g) == _lib.FA_ERR_DEVICE
+        reaches_device(lambda: call(wl=wl, g=g))
     p = [vp(x) for x in ptrs(10)]
     need = L.fa_bwd_workspace_size(2, 3, 100, 77, 64)
     assert L.fa_bwd_window(*p[:9], 2, 3, 100, 77, 64, 0.125, 1, 16, -1, 4, p[9], need - 1, None) == _lib.FA_ERR_WORKSPACE
-    assert L.fa_bwd_window(*p[:9], 2, 3, 100, 77, 64, 0.125, 1, 16, -1, 4, p[9], need, None) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: L.fa_bwd_window(*p[:9], 2, 3, 100, 77, 64, 0.125, 1, 16, -1, 4, p[9], need, None))
 
 
 def test_fp8_validation_codes(L):
@@ -182,15 +200,15 @@ def test_fp8_validation_codes(L):
     assert call(ldv=100) == _lib.FA_ERR_INVALID_ARG     # not a multiple of 16
     assert call(o=vp(0)) == _lib.FA_ERR_INVALID_ARG
     assert call(o=vp(ptrs(1)[0] + 8)) == _lib.FA_ERR_MISALIGNED
-    assert call() == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: call())
     x, c, a, d = (vp(v) for v in ptrs(4))
     assert L.fa_quantize_e4m3(x, 0, c, a, d, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_quantize_e4m3(vp(ptrs(1)[0] + 2), 100, c, a, d, None) == _lib.FA_ERR_MISALIGNED
     assert L.fa_quantize_e4m3(x, 100, x, a, d, None) == _lib.FA_ERR_INVALID_ARG  # codes overlap x
-    assert L.fa_quantize_e4m3(x, 100, c, a, d, None) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: L.fa_quantize_e4m3(x, 100, c, a, d, None))
     assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 64, 100, c, a, d, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 48, 112, c, a, d, None) == _lib.FA_ERR_UNSUPPORTED_D
-    assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 64, 112, c, a, d, None) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 64, 112, c, a, d, None))
 
 
 def test_step_host_validation_codes(L):
@@ -204,7 +222,7 @@ def test_step_host_validation_codes(L):
     assert call(D=48) == _lib.FA_ERR_UNSUPPORTED_D
     assert call(nbytes=need - 1) == _lib.FA_ERR_WORKSPACE
     assert call(dev=vp(ptrs(1)[0] + 16)) == _lib.FA_ERR_WORKSPACE
-    assert call() == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: call())
 
 
 def test_window_split_workspace(L):
@@ -222,7 +240,7 @@ def test_window_split_workspace(L):
     assert L.fa_fwd_window(*args, None, 0, None) == _lib.FA_ERR_WORKSPACE
     assert L.fa_fwd_window(*args, ws, need - 1, None) == _lib.FA_ERR_WORKSPACE
     assert L.fa_fwd_window(*args, vp(ptrs(6)[5] + 16), need, None) == _lib.FA_ERR_WORKSPACE  # misaligned
-    assert L.fa_fwd_window(*args, ws, need, None) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: L.fa_fwd_window(*args, ws, need, None))
 
 
 def test_window_bwd_split_workspace(L):
@@ -238,7 +256,7 @@ def test_window_bwd_split_workspace(L):
     args = (*p[:9], 1, 2, 5000, 5000, 64, 0.125, 0, 100, 100, 40, p[9])
     assert L.fa_bwd_window(*args, base, None) == _lib.FA_ERR_WORKSPACE      # split area missing
     assert L.fa_bwd_window(*args, need - 1, None) == _lib.FA_ERR_WORKSPACE
-    assert L.fa_bwd_window(*args, need, None) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: L.fa_bwd_window(*args, need, None))
 
 
 def test_ex2_probe_validation(L):
@@ -250,7 +268,7 @@ def test_ex2_probe_validation(L):
     assert L.fa_ex2_probe(out, 4, 0, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_ex2_probe(out, 4, (1 << 20) + 1, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_ex2_probe(vp(ptrs(1)[0] + 2), 4, 8, None) == _lib.FA_ERR_MISALIGNED
-    assert L.fa_ex2_probe(out, 4, 8, None) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: L.fa_ex2_probe(out, 4, 8, None))
 
 
 def test_umma_probe_validation(L):
@@ -258,4 +276,35 @@ def test_umma_probe_validation(L):
     assert L.fa_umma_probe(65536, 8, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_umma_probe(4, 0, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_umma_probe(4, (1 << 16) + 1, None) == _lib.FA_ERR_INVALID_ARG
-    assert L.fa_umma_probe(4, 8, None) == _lib.FA_ERR_DEVICE
+    reaches_device(lambda: L.fa_umma_probe(4, 8, None))
+
+
+def test_length_limit(L):
+    """Sequence lengths (and packed totals) above 2^29 are rejected on the host: rows and
+    tiles are indexed with 32-bit ints, and an unbounded window side must reach past
+    every row."""
+    vp = ctypes.c_void_p
+    far = [vp((i + 1) << 40) for i in range(10)]  # 1 TiB apart: no overlap at these sizes
+    M = 1 << 29
+    bad = _lib.FA_ERR_INVALID_ARG
+    assert L.fa_bwd_workspace_size(1, 1, M, M, 16) > 0
+    assert L.fa_bwd_workspace_size(1, 1, M + 1, 16, 16) == 0
+    assert L.fa_bwd_workspace_size(1, 1, 16, M + 1, 16) == 0
+    assert L.fa_bwd_varlen_workspace_size(1, 1, M + 1, 16, 16) == 0
+    fwd = lambda nq, nk: L.fa_fwd(*far[:5], 1, 1, nq, nk, 16, 0.25, 1, None)  # noqa: E731
+    assert fwd(M + 1, 16) == bad
+    assert fwd(16, M + 1) == bad
+    assert fwd((1 << 31) - 1, 16) == bad
+    reaches_device(lambda: fwd(M, M))
+    assert L.fa_fwd_window(*far[:5], 1, 1, M + 1, 16, 16, 0.25, 0, -1, -1, 0, None, 0, None) == bad
+    assert L.fa_bwd(*far[:9], 1, 1, 16, M + 1, 16, 0.25, 1, far[9], 1 << 20, None) == bad
+    varlen = lambda tq, tk, mq, mk: L.fa_fwd_varlen(*far[:7], 1, 1, tq, tk, mq, mk, 16, 0.25, 1, None)  # noqa: E731
+    assert varlen(M + 1, 16, 16, 16) == bad
+    assert varlen(16, M + 1, 16, 16) == bad
+    assert varlen(16, 16, M + 1, 16) == bad
+    assert varlen(16, 16, 16, M + 1) == bad
+    reaches_device(lambda: varlen(M, M, M, M))
+    fp8 = lambda nq, nk, ldv: L.fa_fwd_fp8(*far[:3], ldv, *far[3:8], 1, 1, nq, nk, 64, 0.125, 1, None)  # noqa: E731
+    assert fp8(M + 1, 16, 16) == bad
+    assert fp8(16, M + 16, M + 16) == bad
+    assert L.fa_quantize_e4m3_transposed(far[0], 1, 1, M + 1, 64, M + 16, *far[1:4], None) == bad

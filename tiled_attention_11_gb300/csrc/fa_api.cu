@@ -153,9 +153,16 @@ bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 bool valid_d(int D) { return D == 16 || D == 32 || D == 64 || D == 128; }
 
+// Longest sequence (and packed total) accepted.  The kernels index rows and tiles with
+// 32-bit ints (row + tile size, tile counts, row + window extent), and an unbounded
+// window side is stored as kUnbounded, which must reach past every row.
+constexpr int kMaxLen = 1 << 29;
+static_assert(kMaxLen <= ta11::kUnbounded, "an unbounded window must cover every row");
+bool valid_len(int n) { return n >= 1 && n <= kMaxLen; }
+
 // Shared size checks; returns FA_OK or a code.
 int check_sizes(int B, int H, int Nq, int Nk, int D, float scale) {
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || !valid_len(Nq) || !valid_len(Nk)) return FA_ERR_INVALID_ARG;
   if ((long long)B * H > 65535) return FA_ERR_INVALID_ARG;  // grid.y
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (!valid_d(D)) return FA_ERR_UNSUPPORTED_D;
@@ -193,7 +200,8 @@ WsLayout ws_layout_varlen(int B, int H, int total_q, int D) {
 }
 
 int check_varlen(int B, int H, int total_q, int total_k, int max_q, int max_k, int D, float scale) {
-  if (B < 1 || H < 1 || total_q < 1 || total_k < 1 || max_q < 1 || max_k < 1) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || !valid_len(total_q) || !valid_len(total_k) || !valid_len(max_q) || !valid_len(max_k))
+    return FA_ERR_INVALID_ARG;
   if ((long long)B * H > 65535) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (!valid_d(D)) return FA_ERR_UNSUPPORTED_D;
@@ -823,7 +831,8 @@ extern "C" int fa_quantize_e4m3(const void* x, long long n, void* codes, float* 
 extern "C" int fa_quantize_e4m3_transposed(const void* x, int B, int H, int N, int D, int ldt, void* codes_t,
                                            float* amax, float* descale, cudaStream_t stream) {
   if (!x || !codes_t || !amax || !descale) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || (long long)B * H > 65535 || ldt < N || ldt % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || !valid_len(N) || (long long)B * H > 65535 || ldt < N || ldt % 16 != 0)
+    return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
   if (!aligned(x, 16) || !aligned(codes_t, 16) || !aligned(amax, 4) || !aligned(descale, 4)) return FA_ERR_MISALIGNED;
   const size_t BH = (size_t)B * H;
@@ -844,7 +853,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int l
                           const float* k_descale, const float* v_descale, void* o, float* lse, int B, int H, int Nq,
                           int Nk, int D, float scale, int causal, cudaStream_t stream) {
   if (!q8 || !k8 || !vt8 || !q_descale || !k_descale || !v_descale || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (long long)B * H > 65535) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || !valid_len(Nq) || !valid_len(Nk) || (long long)B * H > 65535) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
   if (ldv < Nk || ldv % 16 != 0) return FA_ERR_INVALID_ARG;
