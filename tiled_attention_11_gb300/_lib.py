@@ -141,14 +141,56 @@ def _check(rc: int, where: str):
         raise FAError(rc, where)
 
 
+# The C calls receive pointers and the sizes read from q and k, and the kernels index
+# every other tensor by those sizes: a tensor of another shape would be read or written
+# past its end.  So each wrapper first checks every tensor's shape against them.
+def _expect(t, name: str, shape) -> None:
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _dense_sizes(q, k, v, o=None, lse=None, do=None, dq=None, dk=None, dv=None):
+    """(B, H, Nq, Nk, D) of [B,H,N,D] tensors, after checking that the shapes agree."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError(f"q and k must be [B, H, N, D], got {tuple(q.shape)} and {tuple(k.shape)}")
+    B, H, Nq, D = q.shape
+    Nk = k.shape[2]
+    _expect(k, "k", (B, H, Nk, D))
+    _expect(v, "v", (B, H, Nk, D))
+    for t, name in ((o, "o"), (do, "do"), (dq, "dq")):
+        _expect(t, name, (B, H, Nq, D))
+    _expect(lse, "lse", (B, H, Nq))
+    _expect(dk, "dk", (B, H, Nk, D))
+    _expect(dv, "dv", (B, H, Nk, D))
+    return B, H, Nq, Nk, D
+
+
+def _packed_sizes(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, do=None, dq=None, dk=None, dv=None):
+    """(B, H, total_q, total_k, D) of packed [total, H, D] tensors, after checking shapes."""
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError(f"q and k must be [total, H, D], got {tuple(q.shape)} and {tuple(k.shape)}")
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    _expect(k, "k", (total_k, H, D))
+    _expect(v, "v", (total_k, H, D))
+    for t, name in ((o, "o"), (do, "do"), (dq, "dq")):
+        _expect(t, name, (total_q, H, D))
+    _expect(lse, "lse", (H, total_q))
+    _expect(dk, "dk", (total_k, H, D))
+    _expect(dv, "dv", (total_k, H, D))
+    if cu_seqlens_q.dim() != 1 or cu_seqlens_q.numel() < 2:
+        raise ValueError(f"cu_seqlens_q must hold B + 1 >= 2 offsets, got shape {tuple(cu_seqlens_q.shape)}")
+    _expect(cu_seqlens_k, "cu_seqlens_k", tuple(cu_seqlens_q.shape))
+    return cu_seqlens_q.numel() - 1, H, total_q, total_k, D
+
+
 def fa_bwd_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int) -> int:
     return int(lib().fa_bwd_workspace_size(B, H, Nq, Nk, D))
 
 
 def fa_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None) -> None:
     """C ``fa_fwd`` on [B,H,N,D] bf16 tensors; writes o (bf16) and lse (fp32 [B,H,Nq])."""
-    B, H, Nq, D = q.shape
-    Nk = k.shape[2]
+    B, H, Nq, Nk, D = _dense_sizes(q, k, v, o, lse)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     rc = lib().fa_fwd(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16), _ptr(v, "v", torch.bfloat16),
@@ -160,8 +202,7 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=Non
 def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None = None, workspace=None,
            stream=None) -> None:
     """C ``fa_bwd``; allocates the workspace with torch when none is given."""
-    B, H, Nq, D = q.shape
-    Nk = k.shape[2]
+    B, H, Nq, Nk, D = _dense_sizes(q, k, v, o, lse, do, dq, dk, dv)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     need = fa_bwd_workspace_size(B, H, Nq, Nk, D)
@@ -268,8 +309,7 @@ def fa_set_bwd_main_events(begin=None, end=None) -> None:
 def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None = None, stream=None) -> None:
     """C ``fa_bwd_noalloc``: the backward for callers that cannot allocate device
     memory; its scratch is a fixed 32 MiB array inside the library (see fa.h)."""
-    B, H, Nq, D = q.shape
-    Nk = k.shape[2]
+    B, H, Nq, Nk, D = _dense_sizes(q, k, v, o, lse, do, dq, dk, dv)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     rc = lib().fa_bwd_noalloc(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
@@ -287,8 +327,7 @@ class StepGraph:
     references to every tensor so none is freed while the graph exists."""
 
     def __init__(self, q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None = None, workspace=None):
-        B, H, Nq, D = q.shape
-        Nk = k.shape[2]
+        B, H, Nq, Nk, D = _dense_sizes(q, k, v, o, lse, do, dq, dk, dv)
         if scale is None:
             scale = 1.0 / math.sqrt(D)
         if workspace is None:
@@ -326,9 +365,7 @@ def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int
                   causal: bool, scale: float | None = None, stream=None) -> None:
     """C ``fa_fwd_varlen``: packed [total, H, D] bf16 tensors, lse [H, total_q] fp32,
     cu_seqlens int32 CUDA tensors of B + 1 offsets."""
-    total_q, H, D = q.shape
-    total_k = k.shape[0]
-    B = cu_seqlens_q.numel() - 1
+    B, H, total_q, total_k, D = _packed_sizes(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     rc = lib().fa_fwd_varlen(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
@@ -347,9 +384,7 @@ def fa_bwd_varlen_workspace_size(B: int, H: int, total_q: int, max_seqlen_q: int
 def fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                   max_seqlen_k: int, causal: bool, scale: float | None = None, workspace=None, stream=None) -> None:
     """C ``fa_bwd_varlen``; allocates the workspace with torch when none is given."""
-    total_q, H, D = q.shape
-    total_k = k.shape[0]
-    B = cu_seqlens_q.numel() - 1
+    B, H, total_q, total_k, D = _packed_sizes(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, do, dq, dk, dv)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if workspace is None:
@@ -377,8 +412,7 @@ def fa_fwd_window(q, k, v, o, lse, causal: bool, window_left: int, window_right:
                   scale: float | None = None, workspace=None, stream=None) -> None:
     """C ``fa_fwd_window`` on [B,H,N,D] bf16 tensors (negative window bound: unbounded);
     allocates the split workspace with torch when it is needed and none is given."""
-    B, H, Nq, D = q.shape
-    Nk = k.shape[2]
+    B, H, Nq, Nk, D = _dense_sizes(q, k, v, o, lse)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     need = fa_fwd_window_workspace_size(B, H, Nq, Nk, D, causal, window_left, window_right, n_global)
@@ -402,8 +436,7 @@ def fa_bwd_window_workspace_size(B: int, H: int, Nq: int, Nk: int, D: int, windo
 def fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, causal: bool, window_left: int, window_right: int,
                   n_global: int, scale: float | None = None, workspace=None, stream=None) -> None:
     """C ``fa_bwd_window``; allocates the workspace with torch when none is given."""
-    B, H, Nq, D = q.shape
-    Nk = k.shape[2]
+    B, H, Nq, Nk, D = _dense_sizes(q, k, v, o, lse, do, dq, dk, dv)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if workspace is None:
@@ -450,8 +483,11 @@ def quantize_e4m3_transposed(v, stream=None):
 def fa_fwd_fp8(q8, k8, vt8, ldv: int, q_descale, k_descale, v_descale, o, lse, causal: bool,
                scale: float | None = None, stream=None) -> None:
     """C ``fa_fwd_fp8``: q8, k8 uint8 [B,H,N,D]; vt8 uint8 [B,H,D,ldv]; descales float32 CUDA scalars."""
-    B, H, Nq, D = q8.shape
-    Nk = k8.shape[2]
+    B, H, Nq, Nk, D = _dense_sizes(q8, k8, None, o, lse)
+    _expect(vt8, "vt8", (B, H, D, int(ldv)))
+    for t, name in ((q_descale, "q_descale"), (k_descale, "k_descale"), (v_descale, "v_descale")):
+        if t.numel() < 1:
+            raise ValueError(f"{name} must hold one float32")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     rc = lib().fa_fwd_fp8(_ptr(q8, "q8", torch.uint8), _ptr(k8, "k8", torch.uint8), _ptr(vt8, "vt8", torch.uint8),
@@ -465,6 +501,7 @@ def fa_fwd_fp8(q8, k8, vt8, ldv: int, q_descale, k_descale, v_descale, o, lse, c
 def forward_fp8(q, k, v, causal: bool, scale: float | None = None, stream=None):
     """Quantise bf16 q, k, v per tensor (three kernels each side) and run the FP8 forward;
     returns (o bf16, lse float32)."""
+    _dense_sizes(q, k, v)
     q8, _, qd = quantize_e4m3(q, stream)
     k8, _, kd = quantize_e4m3(k, stream)
     vt8, ldv, _, vd = quantize_e4m3_transposed(v, stream)
@@ -494,8 +531,7 @@ def step_host(q, k, v, do, o, lse, dq, dk, dv, dev_buf, causal: bool, scale: flo
               stream=None) -> None:
     """C ``fa_step_host``: host (pinned) bf16 [B,H,N,D] inputs / outputs, lse float32 [B,H,Nq];
     dev_buf a uint8 CUDA tensor of step_host_device_bytes(...) bytes."""
-    B, H, Nq, D = q.shape
-    Nk = k.shape[2]
+    B, H, Nq, Nk, D = _dense_sizes(q, k, v, o=o, lse=lse, do=do, dq=dq, dk=dk, dv=dv)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     bf = torch.bfloat16
