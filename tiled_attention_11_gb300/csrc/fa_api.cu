@@ -397,7 +397,7 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   float* dlt = reinterpret_cast<float*>(ws + w.dlt_off);
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
 
-  ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, (int)BH, Nq, w.Nq_pad};
+  ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, (int)BH, Nq, w.Nq_pad, {}};  // dense: no varlen view
   if (ta11::launch_bwd_prep(D, pp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
 
   ta11::BwdParams bp{};
@@ -437,7 +437,7 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   if (ta11::launch_bwd(D, causal != 0, tq, tk, tv, tdo, bp, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   if (ev_b && ev_e && cudaEventRecord(ev_e, stream) != cudaSuccess) return FA_ERR_LAUNCH;
 
-  ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale};
+  ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale, {}};  // dense: no varlen view
   if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   if (split.n_gk > 0) {
     ta11::KvConvertParams kp{dkv_accum, dk, dv, Nk, split.n_gk * 128, scale};
@@ -684,7 +684,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
 
   // The preprocess kernel rewrites every scratch word this call reads (it zeroes
   // dq_accum and fills Dlt and L*log2(e)), so the previous call's contents never leak in.
-  ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, (int)BH, Nq, w.Nq_pad};
+  ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, (int)BH, Nq, w.Nq_pad, {}};  // dense: no varlen view
   if (ta11::launch_bwd_prep(D, pp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   ta11::BwdParams bp{};
   bp.dk = dk;
@@ -701,7 +701,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   bp.wait_limit_ns = g_wait_limit_ns.load();
   bp.status = status;
   if (ta11::launch_bwd(D, causal != 0, tq, tk, tv, tdo, bp, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
-  ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale};
+  ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale, {}};  // dense: no varlen view
   if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;
 }
