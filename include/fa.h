@@ -113,30 +113,6 @@ void fa_set_wait_limit_ns(unsigned long long ns);
 int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
 
 /*
- * Measurement hook (no counterpart on the pages): the rate of the special-function
- * unit's exp2, the third roof of the softmax next to the tensor core and HBM.  Launches
- * n_blocks blocks of 512 threads; each thread runs 8 independent chains of `iters`
- * ex2.approx.ftz.f32, so the launch performs n_blocks * 512 * 8 * iters of them and
- * its duration (CUDA events on `stream`) gives exp2 per second.  `out` (device, caller
- * owned, n_blocks * 512 floats) receives each thread's chain sum.  Asynchronous.
- * Returns FA_ERR_INVALID_ARG (null out, n_blocks outside [1, 65535], iters outside
- * [1, 2^20]), FA_ERR_MISALIGNED, FA_ERR_DEVICE (not sm_103) or FA_ERR_LAUNCH.
- */
-int fa_ex2_probe(float* out, int n_blocks, int iters, cudaStream_t stream);
-
-/*
- * Measurement hook (no counterpart on the pages): the tensor core's rate for the score
- * GEMM's UMMA shape (M = N = 128, K = 16, bf16 operands from 128-byte swizzled K-major
- * shared-memory tiles, fp32 accumulate in TMEM).  Launches n_ctas CTAs (one per SM at
- * most resident); each issues `iters` groups of 8 such UMMAs back to back from one
- * thread, i.e. n_ctas * iters * 8 * 2*128*128*16 FLOPs, and waits (bounded, like every
- * wait in this library) for them to complete.  Time it with CUDA events on `stream`.
- * Returns FA_ERR_INVALID_ARG (n_ctas outside [1, 65535], iters outside [1, 65536]),
- * FA_ERR_DEVICE (not sm_103) or FA_ERR_LAUNCH; a timeout is recorded in the status word.
- */
-int fa_umma_probe(int n_ctas, int iters, cudaStream_t stream);
-
-/*
  * Timing hook for measurement tools (no counterpart on the pages): while both
  * events are non-null, every fa_bwd records `begin` on its stream immediately
  * before launching its main tensor-core kernel and `end` immediately after it,
@@ -280,13 +256,17 @@ void fa_graph_destroy(fa_graph g);
  * Its scratch (dq_accum, Dlt, L*log2(e), laid out as fa_bwd's workspace) is a
  * fixed 32 MiB array in the library's device memory, which every GPU that
  * loads the library holds until the process exits.  Problems whose
- * fa_bwd_workspace_size(...) exceeds 32 MiB are rejected with
- * FA_ERR_SCRATCH_LIMIT before anything is launched (for D = 128 that is about
- * B*H*Nq <= 64k query rows).
+ * fa_bwd_workspace_size(B, H, Nq, Nk, D) exceeds 32 MiB (33554432 bytes) are
+ * rejected with FA_ERR_SCRATCH_LIMIT before anything is launched; that call is
+ * the exact test.  The scratch holds (4*D + 8) bytes per query row with each
+ * head's rows padded to a multiple of 64, so for D = 128 the limit is
+ * B*H*64*ceil(Nq/64) <= 64512 padded rows (e.g. 1008 heads of up to 64 queries):
+ * many short heads count as 64 rows each.
  *
- * The first call on a device looks up the array's device address (a one-time
- * set-up per device, done with that device current); make that first call
- * before any stream capture.  All calls share the one array and the kernels
+ * The first call on a device looks up the array's device address (a set-up per
+ * device, done with that device current); make that first call before any
+ * stream capture.  A lookup that fails (FA_ERR_DEVICE) is not remembered: the
+ * next call tries again.  All calls share the one array and the kernels
  * re-initialise what must start at zero, so calls that overlap on the GPU
  * (different streams, or different threads without ordering) race on it and
  * must be serialised by the caller.  Allocates nothing: no cudaMalloc,

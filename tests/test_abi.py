@@ -259,24 +259,17 @@ def test_window_bwd_split_workspace(L):
     reaches_device(lambda: L.fa_bwd_window(*args, need, None))
 
 
-def test_ex2_probe_validation(L):
+def test_noalloc_scratch_boundary(L):
+    """fa_bwd_noalloc's limit is fa_bwd_workspace_size <= 32 MiB, checked before launching:
+    at D = 128 and 64 queries per head, 1008 heads fit and 1009 do not."""
     vp = ctypes.c_void_p
-    out = vp(ptrs(1)[0])
-    assert L.fa_ex2_probe(None, 4, 8, None) == _lib.FA_ERR_INVALID_ARG
-    assert L.fa_ex2_probe(out, 0, 8, None) == _lib.FA_ERR_INVALID_ARG
-    assert L.fa_ex2_probe(out, 65536, 8, None) == _lib.FA_ERR_INVALID_ARG
-    assert L.fa_ex2_probe(out, 4, 0, None) == _lib.FA_ERR_INVALID_ARG
-    assert L.fa_ex2_probe(out, 4, (1 << 20) + 1, None) == _lib.FA_ERR_INVALID_ARG
-    assert L.fa_ex2_probe(vp(ptrs(1)[0] + 2), 4, 8, None) == _lib.FA_ERR_MISALIGNED
-    reaches_device(lambda: L.fa_ex2_probe(out, 4, 8, None))
-
-
-def test_umma_probe_validation(L):
-    assert L.fa_umma_probe(0, 8, None) == _lib.FA_ERR_INVALID_ARG
-    assert L.fa_umma_probe(65536, 8, None) == _lib.FA_ERR_INVALID_ARG
-    assert L.fa_umma_probe(4, 0, None) == _lib.FA_ERR_INVALID_ARG
-    assert L.fa_umma_probe(4, (1 << 16) + 1, None) == _lib.FA_ERR_INVALID_ARG
-    reaches_device(lambda: L.fa_umma_probe(4, 8, None))
+    p = [vp(x) for x in ptrs(9)]
+    limit = 32 << 20
+    assert L.fa_bwd_workspace_size(1, 1008, 64, 64, 128) <= limit < L.fa_bwd_workspace_size(1, 1009, 64, 64, 128)
+    assert L.fa_bwd_noalloc(*p, 1, 1009, 64, 64, 128, 0.088, 1, None) == _lib.FA_ERR_SCRATCH_LIMIT
+    # short heads count as 64 padded rows each
+    assert L.fa_bwd_noalloc(*p, 1, 1009, 1, 1, 128, 0.088, 1, None) == _lib.FA_ERR_SCRATCH_LIMIT
+    reaches_device(lambda: L.fa_bwd_noalloc(*p, 1, 1008, 64, 64, 128, 0.088, 1, None))
 
 
 def test_length_limit(L):

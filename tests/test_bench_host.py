@@ -50,6 +50,7 @@ def test_reference_arm_prints_the_contract_line():
         assert key in line, key
     assert line["impl"] == "reference" and line["value"] > 0 and line["warmup"] >= 3
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert isinstance(line["cpu_baseline"]["cpu_model"], str) and line["cpu_baseline"]["cpu_model"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["config"]["workload"].startswith("multi-head LLM-shaped attention layer")
 
@@ -61,3 +62,7 @@ def test_reference_arm_prints_on_rank_zero_only():
                          cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert out.returncode == 0, out.stderr[-2000:]
     assert out.stdout.strip() == ""
+
+
+def test_cpu_model_is_named():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()

@@ -104,7 +104,10 @@ def test_small_config(seed):
 
 
 # ---------------------------------------------------------------------------- sweep (+ x8)
-SWEEP_CASES = [(p, s) for p in I.SWEEP + I.SWEEP_X8 for s in ((0, 1, 2) if p.Nq <= 1024 else (0,))]
+# every seed for N <= 1024 and for the x8 stability rows (whose dQ margin is the tightest:
+# rel-L2 up to 9.5e-3 against 1e-2 at D = 16/32); seed 0 for the plain N = 4096 rows
+SWEEP_CASES = [(p, s) for p in I.SWEEP + I.SWEEP_X8
+               for s in ((0, 1, 2) if p.Nq <= 1024 or p.qk_factor != 1.0 else (0,))]
 
 
 @pytest.mark.parametrize("p,seed", SWEEP_CASES, ids=[f"{p.name()}-s{s}" for p, s in SWEEP_CASES])
@@ -164,6 +167,32 @@ def test_long_single_head(p):
 
 def test_multi_head_layer():
     check_heads(I.LAYER, 0, heads=[(0, 0), (1, 17), (3, 31)])
+
+
+def test_multi_head_layer_every_head_sampled():
+    # all 128 heads of the layer: O, L and dQ on 32 rows (the first and last eight, sixteen
+    # drawn), dK and dV on the last 64 keys (which the last 64 queries see) and on a 64-key
+    # range that moves with the head (every key tile is covered by some head)
+    p = I.LAYER
+    q, k, v, do = I.draw(p, 0)
+    o, lse, dq, dk, dv = run_gpu(p, q, k, v, do)
+    rng = np.random.default_rng(9)
+    rows = np.unique(np.concatenate([np.arange(8), np.arange(p.Nq - 8, p.Nq), rng.integers(0, p.Nq, 16)]))
+    o, lse, dq, dk, dv = (f64(t) for t in (o, lse, dq, dk, dv))
+    for b in range(p.B):
+        for h in range(p.H):
+            qd, kd, vd, dod = (I.as_f64(t[b, h]) for t in (q, k, v, do))
+            tag = f"layer b{b}h{h}"
+            ro, rl = oracle.forward_head(qd, kd, vd, p.scale, p.causal, rows=rows)
+            assert_close(tag + " O[rows]", o[b, h][rows], ro)
+            assert_lse(tag + " L[rows]", lse[b, h][rows], rl)
+            rdq, _, _ = oracle.backward_head(qd, kd, vd, dod, p.scale, p.causal, q_rows=rows)
+            assert_close(tag + " dQ[rows]", dq[b, h][rows], rdq)
+            k_mid = 64 * ((b * p.H + h) * 5 % 63)  # 0 .. 3968, step 64
+            for (k0, k1) in ((p.Nk - 64, p.Nk), (k_mid, k_mid + 64)):
+                _, rdk, rdv = oracle.backward_head(qd, kd, vd, dod, p.scale, p.causal, k_range=(k0, k1))
+                assert_close(tag + f" dK[{k0}:{k1}]", dk[b, h][k0:k1], rdk)
+                assert_close(tag + f" dV[{k0}:{k1}]", dv[b, h][k0:k1], rdv)
 
 
 def test_long_context_ragged_tail():
@@ -270,21 +299,6 @@ def test_binding_rejects_bad_tensors():
     assert e.value.code == _lib.FA_ERR_UNSUPPORTED_D
 
 
-def test_ex2_probe_rate_and_values():
-    # every chain x <- 2^(-x) contracts to the fixed point x* = 2^(-x*) ~ 0.6412; the rate
-    # is the special-function units' (one 32-lane exp2 unit's worth per SM and clock
-    # is 32 x 152 x ~2 GHz ~ 1e13 per second; allow a wide band)
-    x = 0.5
-    for _ in range(200):
-        x = 2.0 ** -x
-    out = torch.empty(152 * 512, dtype=torch.float32, device="cuda")
-    _lib._check(_lib.lib().fa_ex2_probe(out.data_ptr(), 152, 256, torch.cuda.current_stream().cuda_stream), "probe")
-    torch.cuda.synchronize()
-    assert torch.allclose(out.double().cpu(), torch.full((152 * 512,), 8 * x, dtype=torch.float64), atol=1e-4)
-    rate = _lib.ex2_rate()
-    assert 1e12 < rate < 1e14, rate
-
-
 REPEAT_CASES = [I.Problem(2, 8, 2048, 2048, 128, True), I.Problem(2, 8, 2048, 2048, 64, False),
                 I.Problem(1, 16, 1000, 1000, 32, True)]
 
@@ -310,16 +324,6 @@ def test_repeated_runs_are_identical(p):
         assert err <= 1e-2 * dq0.float().abs().max().item(), err
     torch.cuda.synchronize()
     assert _lib.fa_device_status()[0] == _lib.FA_OK
-
-
-def test_umma_probe_rate():
-    # the score GEMM's UMMA shape back to back on every SM: within the hardware's range
-    # (8192 bf16 FLOP per SM-clock x 152 SMs x ~2 GHz ~ 2.5 PFLOP/s), no timeout recorded
-    _lib.fa_device_status(reset=True)
-    rate = _lib.umma_rate(iters=256)
-    torch.cuda.synchronize()
-    assert _lib.fa_device_status()[0] == _lib.FA_OK
-    assert 1.0e15 < rate < 3.5e15, rate
 
 
 def test_tensors_beyond_2_31_elements():

@@ -4,9 +4,10 @@ Some callers cannot call cudaMalloc or hand the library a workspace: a serving
 process whose device memory budget is fixed at start-up, or a plug-in whose
 host framework owns the allocator and passes only input and output buffers.
 fa_bwd_noalloc serves them with a fixed 32 MiB scratch array inside the
-library.  These tests call it through the C ABI and check that it reproduces
-the workspace entry point fa_bwd, within the parity tolerances used by every
-GPU test here, on consecutive calls that reuse the shared scratch.
+library.  These tests call it through the C ABI and check it against the fp64
+oracle and against the workspace entry point fa_bwd, within the parity
+tolerances used by every GPU test here, on consecutive calls that reuse the
+shared scratch, up to a problem that fills it.
 
 This file is collected last on purpose, and passes both alone in a fresh
 process and after the rest of the GPU suite.
@@ -14,6 +15,8 @@ process and after the rest of the GPU suite.
 import ctypes
 
 import numpy as np
+
+import oracle
 import pytest
 import torch
 
@@ -36,26 +39,32 @@ def close(name, got, ref):
     assert rl2 <= REL_L2 and ma <= MAX_FRAC * np.abs(r).max(), f"{name}: rel_l2={rl2:.3e} max_abs={ma:.3e}"
 
 
-def test_noalloc_backward_matches_workspace_backward_on_consecutive_calls():
+def test_noalloc_backward_matches_oracle_and_workspace_backward_on_consecutive_calls():
     assert torch.cuda.is_available(), "needs a CUDA device"
     build()
     _lib.lib()
     dev = torch.device("cuda")
-    # consecutive calls of different sizes share the scratch; the third repeats
-    # the first after a smaller problem has overwritten part of it
+    # consecutive calls of different sizes share the scratch; the third repeats the first
+    # after a smaller problem has overwritten part of it, the last fills the array
+    # (1008 heads of 64 queries at D = 128: 33546240 of its 33554432 bytes)
     problems = [(I.Problem(2, 3, 300, 257, 64, True), 0), (I.Problem(1, 2, 200, 200, 128, False), 1),
-                (I.Problem(2, 3, 300, 257, 64, True), 0)]
+                (I.Problem(2, 3, 300, 257, 64, True), 0), (I.Problem(1, 1008, 64, 64, 128, True), 2)]
+    assert _lib.fa_bwd_workspace_size(1, 1008, 64, 64, 128) > 33_500_000
     for n, (p, seed) in enumerate(problems):
-        q, k, v, do = (t.to(dev) for t in I.draw(p, seed))
+        qc, kc, vc, doc = I.draw(p, seed)
+        q, k, v, do = (t.to(dev) for t in (qc, kc, vc, doc))
         o, lse = _lib.forward(q, k, v, p.causal, p.scale)
         dq_ref, dk_ref, dv_ref = _lib.backward(q, k, v, o, lse, do, p.causal, p.scale)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         _lib.fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, p.causal, p.scale)
         torch.cuda.synchronize()
         tag = f"call {n} {p.name()}"
-        close(tag + " dQ", dq, dq_ref)
-        close(tag + " dK", dk, dk_ref)
-        close(tag + " dV", dv, dv_ref)
+        close(tag + " dQ vs fa_bwd", dq, dq_ref)
+        close(tag + " dK vs fa_bwd", dk, dk_ref)
+        close(tag + " dV vs fa_bwd", dv, dv_ref)
+        odq, odk, odv = oracle.attention_backward(*(I.as_f64(t) for t in (qc, kc, vc, doc)), p.scale, p.causal)
+        for name, got, ref in (("dQ", dq, odq), ("dK", dk, odk), ("dV", dv, odv)):
+            close(tag + f" {name} vs oracle", got, torch.from_numpy(ref))
     assert _lib.fa_device_status()[0] == _lib.FA_OK
 
 

@@ -28,7 +28,7 @@ FA_ERR_TIMEOUT = 7
 FA_ERR_SCRATCH_LIMIT = 8
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_device_status",
-            "fa_set_wait_limit_ns", "fa_wait_probe", "fa_ex2_probe", "fa_umma_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
+            "fa_set_wait_limit_ns", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
             "fa_graph_create", "fa_graph_launch", "fa_graph_destroy", "fa_fwd_varlen", "fa_bwd_varlen",
             "fa_bwd_varlen_workspace_size", "fa_fwd_window", "fa_bwd_window", "fa_fwd_window_workspace_size", "fa_bwd_window_workspace_size",
             "fa_quantize_e4m3",
@@ -66,10 +66,6 @@ def lib() -> ctypes.CDLL:
     L.fa_device_status.restype = i
     L.fa_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     L.fa_set_wait_limit_ns.restype = None
-    L.fa_ex2_probe.argtypes = [vp, i, i, vp]
-    L.fa_ex2_probe.restype = i
-    L.fa_umma_probe.argtypes = [i, i, vp]
-    L.fa_umma_probe.restype = i
     L.fa_wait_probe.argtypes = [ctypes.c_ulonglong, vp]
     L.fa_wait_probe.restype = i
     L.fa_set_bwd_main_events.argtypes = [vp, vp]
@@ -248,54 +244,6 @@ def fa_set_wait_limit_ns(ns: int) -> None:
 
 def fa_wait_probe(limit_ns: int, stream=None) -> None:
     _check(lib().fa_wait_probe(int(limit_ns), _stream(stream)), "fa_wait_probe")
-
-
-def ex2_rate(device=None, iters: int = 2048, reps: int = 5) -> float:
-    """exp2 per second of the special-function units, from fa_ex2_probe timed with CUDA
-    events (median of ``reps`` after one warm-up); 4 blocks of 512 threads per SM."""
-    dev = torch.device("cuda") if device is None else torch.device(device)
-    n_blocks = 4 * torch.cuda.get_device_properties(dev).multi_processor_count
-    out = torch.empty(n_blocks * 512, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def run():
-        _check(lib().fa_ex2_probe(_ptr(out, "out", torch.float32), n_blocks, iters, stream.cuda_stream),
-               "fa_ex2_probe")
-
-    run()
-    ts = []
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        run()
-        e1.record(stream)
-        e1.synchronize()
-        ts.append(e0.elapsed_time(e1))
-    ts.sort()
-    return n_blocks * 512 * 8 * iters / (ts[len(ts) // 2] * 1e-3)
-
-
-def umma_rate(device=None, iters: int = 1024, reps: int = 5) -> float:
-    """bf16 FLOP/s of the tensor cores for the score GEMM's UMMA shape, from fa_umma_probe
-    timed with CUDA events (median of ``reps`` after one warm-up); one CTA per SM."""
-    dev = torch.device("cuda") if device is None else torch.device(device)
-    n = torch.cuda.get_device_properties(dev).multi_processor_count
-    stream = torch.cuda.current_stream(dev)
-
-    def run():
-        _check(lib().fa_umma_probe(n, iters, stream.cuda_stream), "fa_umma_probe")
-
-    run()
-    ts = []
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        run()
-        e1.record(stream)
-        e1.synchronize()
-        ts.append(e0.elapsed_time(e1))
-    ts.sort()
-    return n * iters * 8 * 2.0 * 128 * 128 * 16 / (ts[len(ts) // 2] * 1e-3)
 
 
 def fa_set_bwd_main_events(begin=None, end=None) -> None:

@@ -1,10 +1,13 @@
-"""In-tree build of the CUDA library ``libta11_fa.so`` for sm_103a.
+"""In-tree build of the CUDA libraries for sm_103a.
 
-Each ``csrc/*.cu`` translation unit is compiled by nvcc in parallel into
-``_build/``; the objects are linked into the package directory.  The CUDA
-runtime is linked statically; the driver's tensor-map encoder is resolved at
-run time, so the library loads on a machine without a GPU (it then reports
-FA_ERR_DEVICE on any compute call).
+``libta11_fa.so`` is the attention library (include/fa.h); ``libta11_probe.so``
+is the separate measurement library (csrc/probe.h: roof microbenchmarks and the
+exp2 accuracy check), used only by the benchmark's tables and the tests.  Every
+``csrc/*.cu`` translation unit is compiled by nvcc in parallel into ``_build/``;
+the objects are linked into the package directory.  The CUDA runtime is linked
+statically; the driver's tensor-map encoder is resolved at run time, so the
+libraries load on a machine without a GPU (they then report FA_ERR_DEVICE on any
+compute call).
 """
 from __future__ import annotations
 
@@ -19,7 +22,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libta11_fa.so")
-SOURCES = ["fa_api.cu", "fwd_sm103a.cu", "bwd_sm103a.cu", "fwd_fp8_sm103a.cu", "quant_sm103a.cu", "probe_sm103a.cu"]
+SOURCES = ["fa_api.cu", "fwd_sm103a.cu", "bwd_sm103a.cu", "fwd_fp8_sm103a.cu", "quant_sm103a.cu"]
+PROBE_LIB = os.path.join(PKG, "libta11_probe.so")
+PROBE_SOURCES = ["probe_sm103a.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
@@ -42,22 +47,25 @@ def _newest_input() -> float:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library if any source is newer than it; return its path."""
+    """Compile and link both libraries if any source is newer than them; return the
+    attention library's path."""
     os.makedirs(BUILD, exist_ok=True)
     newest = _newest_input()
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
+    targets = [(LIB, SOURCES), (PROBE_LIB, PROBE_SOURCES)]
+    stale = [(lib, srcs) for lib, srcs in targets
+             if force or not os.path.exists(lib) or os.path.getmtime(lib) < newest]
+    if not stale:
         return LIB
     nvcc = _nvcc()
     procs = []
-    objs = []
-    for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        objs.append(obj)
-        cmd = [nvcc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
-        if verbose:
-            cmd.insert(1, "-Xptxas=-v")
-            print(" ".join(cmd), file=sys.stderr)
-        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
+    for _, srcs in stale:
+        for src in srcs:
+            obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+            cmd = [nvcc, *ARCH, *CFLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+                print(" ".join(cmd), file=sys.stderr)
+            procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
     errors = []
     for src, p in procs:
         out, _ = p.communicate()
@@ -67,12 +75,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
             errors.append(f"--- {src} ---\n{out}")
     if errors:
         raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
-    tmp = LIB + ".tmp"
-    link = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
-    r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
-    if r.returncode != 0:
-        raise RuntimeError("link failed:\n" + r.stdout)
-    os.replace(tmp, LIB)
+    for lib, srcs in stale:
+        objs = [os.path.join(BUILD, src.replace(".cu", ".o")) for src in srcs]
+        tmp = lib + ".tmp"
+        link = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
+        r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("link failed:\n" + r.stdout)
+        os.replace(tmp, lib)
     return LIB
 
 

@@ -518,25 +518,6 @@ int fa_wait_probe(unsigned long long limit_ns, cudaStream_t stream) {
   return ta11::launch_wait_probe(limit_ns, status, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-int fa_umma_probe(int n_ctas, int iters, cudaStream_t stream) {
-  if (n_ctas < 1 || n_ctas > 65535 || iters < 1 || iters > (1 << 16)) return FA_ERR_INVALID_ARG;
-  unsigned* status = nullptr;
-  int rc = current_device(&status);
-  if (rc != FA_OK) return rc;
-  return ta11::launch_umma_probe(n_ctas, iters, g_wait_limit_ns.load(), status, stream) == cudaSuccess
-             ? FA_OK
-             : FA_ERR_LAUNCH;
-}
-
-int fa_ex2_probe(float* out, int n_blocks, int iters, cudaStream_t stream) {
-  if (!out || n_blocks < 1 || n_blocks > 65535 || iters < 1 || iters > (1 << 20)) return FA_ERR_INVALID_ARG;
-  if (!aligned(out, 4)) return FA_ERR_MISALIGNED;
-  unsigned* status = nullptr;
-  int rc = current_device(&status);
-  if (rc != FA_OK) return rc;
-  return ta11::launch_ex2_probe(out, n_blocks, iters, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
-}
-
 }  // extern "C"
 
 // ------------------------------------------------------------------------------------
@@ -619,12 +600,14 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB, held by ev
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 struct NoAllocDevice {
-  std::once_flag once;
-  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  std::mutex mu;
+  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device (null: not looked up yet)
 };
 NoAllocDevice g_noalloc_dev[kMaxDevices];
 
-// One-time set-up per device, run with that device current.
+// Set-up per device, run with that device current: the array's device address.  A
+// failed lookup is not remembered, so a later call (outside a stream capture, say)
+// tries again.
 void* noalloc_scratch_for_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -632,15 +615,15 @@ void* noalloc_scratch_for_current_device() {
     return nullptr;
   }
   NoAllocDevice& s = g_noalloc_dev[dev];
-  std::call_once(s.once, [&]() {
+  std::lock_guard<std::mutex> lk(s.mu);
+  if (!s.scratch) {
     void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess) {
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
       cudaGetLastError();
-      return;
+      return nullptr;
     }
     s.scratch = ptr;
-  });
+  }
   return s.scratch;
 }
 
@@ -655,55 +638,17 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
       !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return FA_ERR_MISALIGNED;
-  const WsLayout w = ws_layout(B, H, Nq, D);
-  if (w.total > kNoAllocScratchBytes) return FA_ERR_SCRATCH_LIMIT;
-  const size_t BH = (size_t)B * H;
-  const size_t nq_b = BH * Nq * D * 2, nk_b = BH * Nk * D * 2;
-  const Range ins[] = {rng(q, nq_b), rng(k, nk_b), rng(v, nk_b), rng(o, nq_b), rng(lse, BH * Nq * 4), rng(dO, nq_b)};
-  const Range outs[] = {rng(dq, nq_b), rng(dk, nk_b), rng(dv, nk_b)};
-  for (int a = 0; a < 3; ++a) {
-    for (const Range& in : ins)
-      if (overlap(outs[a], in)) return FA_ERR_INVALID_ARG;
-    for (int b = a + 1; b < 3; ++b)
-      if (overlap(outs[a], outs[b])) return FA_ERR_INVALID_ARG;
-  }
-
+  if (ws_layout(B, H, Nq, D).total > kNoAllocScratchBytes) return FA_ERR_SCRATCH_LIMIT;
   unsigned* status = nullptr;
   rc = current_device(&status);
   if (rc != FA_OK) return rc;
-  char* ws = static_cast<char*>(noalloc_scratch_for_current_device());
+  void* ws = noalloc_scratch_for_current_device();
   if (!ws) return FA_ERR_DEVICE;
-
-  CUtensorMap tq, tk, tv, tdo;
-  if (!make_map(&tq, q, D, Nq, (int)BH, 64) || !make_map(&tk, k, D, Nk, (int)BH, 128) ||
-      !make_map(&tv, v, D, Nk, (int)BH, 128) || !make_map(&tdo, dO, D, Nq, (int)BH, 64))
-    return FA_ERR_LAUNCH;
-  float* dq_accum = reinterpret_cast<float*>(ws + w.dq_off);
-  float* dlt = reinterpret_cast<float*>(ws + w.dlt_off);
-  float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
-
-  // The preprocess kernel rewrites every scratch word this call reads (it zeroes
-  // dq_accum and fills Dlt and L*log2(e)), so the previous call's contents never leak in.
-  ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, (int)BH, Nq, w.Nq_pad, {}};  // dense: no varlen view
-  if (ta11::launch_bwd_prep(D, pp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
-  ta11::BwdParams bp{};
-  bp.dk = dk;
-  bp.dv = dv;
-  bp.dq_accum = dq_accum;
-  bp.lse2 = lse2;
-  bp.dlt = dlt;
-  bp.Nq = Nq;
-  bp.Nk = Nk;
-  bp.Nq_pad = w.Nq_pad;
-  bp.n_k_tiles = (Nk + 127) / 128;
-  bp.scale = scale;
-  bp.scale_log2 = scale * kLog2e;
-  bp.wait_limit_ns = g_wait_limit_ns.load();
-  bp.status = status;
-  if (ta11::launch_bwd(D, causal != 0, tq, tk, tv, tdo, bp, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
-  ta11::ConvParams cp{dq_accum, dq, (int)BH, Nq, w.Nq_pad, scale, {}};  // dense: no varlen view
-  if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
-  return FA_OK;
+  // The same launch sequence as fa_bwd, with the fixed array as its workspace.  Its
+  // preprocess kernel rewrites every scratch word the call reads (it zeroes dq_accum and
+  // fills Dlt and L*log2(e)), so the previous call's contents never leak in.
+  return bwd_dense(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, D, scale, causal, nullptr, ws,
+                   kNoAllocScratchBytes, stream);
 }
 
 // ------------------------------------------------------------------------------------

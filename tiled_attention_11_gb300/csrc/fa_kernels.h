@@ -209,10 +209,5 @@ cudaError_t launch_quant_e4m3(const void* x, long long n, const float* amax, voi
 cudaError_t launch_quant_e4m3_t(const void* x, int BH, int N, int D, int ldt, const float* amax, void* codes_t,
                                 float* descale, cudaStream_t st);
 cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned* status, cudaStream_t st);
-// n_ctas CTAs, each `iters` groups of 8 bf16 UMMAs (M = N = 128, K = 16) issued by one thread.
-cudaError_t launch_umma_probe(int n_ctas, int iters, unsigned long long limit_ns, unsigned* status,
-                              cudaStream_t st);
-// n_blocks x 512 threads, each 8 * iters ex2.approx; out holds n_blocks * 512 floats.
-cudaError_t launch_ex2_probe(float* out, int n_blocks, int iters, cudaStream_t st);
 
 }  // namespace ta11

@@ -81,6 +81,27 @@ struct Cfg {
 
 constexpr float kTau = 8.0f;  // base-2 growth of a row max that forces a rescale
 
+// The weights of one 32-column group of a row: p = 2^(S*c - m) two lanes at a time on
+// the special-function unit, packed to bf16 (RN) into pk; l2 accumulates the fp32
+// weights (packed pairs), lra / lrb the bf16-rounded ones (even / odd columns, added
+// straight from their bf16 halves), each over four independent chains.
+__device__ __forceinline__ void softmax_weights32(const uint32_t (&s)[32], uint64_t c2, uint64_t nm2,
+                                                  uint32_t (&pk)[16], uint64_t (&l2)[4], float (&lra)[4],
+                                                  float (&lrb)[4]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    const int q = c >> 1;
+    float x0, x1;
+    f2unpack(ffma2(f2pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c2, nm2), x0, x1);
+    const float p0 = ex2(x0), p1 = ex2(x1);
+    const uint32_t w = pack_bf16(p0, p1);
+    l2[q & 3] = fadd2(l2[q & 3], f2pack(p0, p1));
+    lra[q & 3] = add_bf16_lo(lra[q & 3], w);
+    lrb[q & 3] = add_bf16_hi(lrb[q & 3], w);
+    pk[q] = w;
+  }
+}
+
 // Byte offset of the kk-th 16-wide K slice inside a K-major tile (rows x D, D in
 // CHUNK-wide swizzled column blocks of CHUNK_BYTES each).
 template <int D>
@@ -449,33 +470,29 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         alpha = ex2(m - mx2);
         m = mx2;
       }
-      // p = 2^(S*c - m) two lanes at a time; l and lr accumulate in packed pairs.  (Local
-      // mask: a row whose keys so far were all masked keeps m = -inf; subtract 0 instead.)
+      // p = 2^(S*c - m) two lanes at a time; l and lr accumulate over four chains each.
+      // (Local mask: a row whose keys so far were all masked keeps m = -inf; subtract 0.)
       const float msub = (LOCAL && m == -INFINITY) ? 0.f : m;
       const uint64_t c2 = f2pack(sl2, sl2), nm2 = f2pack(-msub, -msub);
-      uint64_t l2[4], lr2[4];
+      uint64_t l2[4];
+      float lra[4], lrb[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) l2[i] = lr2[i] = 0ull;
+      for (int i = 0; i < 4; ++i) {
+        l2[i] = 0ull;
+        lra[i] = lrb[i] = 0.f;
+      }
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float x0, x1;
-          f2unpack(ffma2(f2pack(as_f(s[g][c]), as_f(s[g][c + 1])), c2, nm2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          const uint32_t w = pack_bf16(p0, p1);
-          l2[(c >> 1) & 3] = fadd2(l2[(c >> 1) & 3], f2pack(p0, p1));
-          lr2[(c >> 1) & 3] = fadd2(lr2[(c >> 1) & 3], f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
-          pk[c >> 1] = w;
-        }
+        softmax_weights32(s[g], c2, nm2, pk, l2, lra, lrb);
         tmem_st16(t_s + g * 16, pk);
       }
       float la[8], lb[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         f2unpack(l2[i], la[2 * i], la[2 * i + 1]);
-        f2unpack(lr2[i], lb[2 * i], lb[2 * i + 1]);
+        lb[2 * i] = lra[i];
+        lb[2 * i + 1] = lrb[i];
       }
       l = l * alpha + (((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7])));
       lr = lr * alpha + (((lb[0] + lb[1]) + (lb[2] + lb[3])) + ((lb[4] + lb[5]) + (lb[6] + lb[7])));
@@ -845,31 +862,27 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
         alpha = ex2(m - mx2);
         m = mx2;
       }
-      // p = 2^(S*c - m) two lanes at a time; l and lr accumulate in packed pairs
+      // p = 2^(S*c - m) two lanes at a time; l and lr accumulate over four chains each
       const uint64_t c2 = f2pack(sl2, sl2), nm2 = f2pack(-m, -m);
-      uint64_t l2[4], lr2[4];
+      uint64_t l2[4];
+      float lra[4], lrb[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) l2[i] = lr2[i] = 0ull;
+      for (int i = 0; i < 4; ++i) {
+        l2[i] = 0ull;
+        lra[i] = lrb[i] = 0.f;
+      }
 #pragma unroll
       for (int gg = 0; gg < 4; ++gg) {
         uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float x0, x1;
-          f2unpack(ffma2(f2pack(as_f(s[gg][c]), as_f(s[gg][c + 1])), c2, nm2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          const uint32_t w = pack_bf16(p0, p1);
-          l2[(c >> 1) & 3] = fadd2(l2[(c >> 1) & 3], f2pack(p0, p1));
-          lr2[(c >> 1) & 3] = fadd2(lr2[(c >> 1) & 3], f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
-          pk[c >> 1] = w;
-        }
+        softmax_weights32(s[gg], c2, nm2, pk, l2, lra, lrb);
         tmem_st16(t_s + gg * 16, pk);
       }
       float la[8], lb[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         f2unpack(l2[i], la[2 * i], la[2 * i + 1]);
-        f2unpack(lr2[i], lb[2 * i], lb[2 * i + 1]);
+        lb[2 * i] = lra[i];
+        lb[2 * i + 1] = lrb[i];
       }
       l = l * alpha + (((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7])));
       lr = lr * alpha + (((lb[0] + lb[1]) + (lb[2] + lb[3])) + ((lb[4] + lb[5]) + (lb[6] + lb[7])));

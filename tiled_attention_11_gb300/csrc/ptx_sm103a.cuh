@@ -433,6 +433,22 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// acc + (the bf16 in the low / high half of w) in fp32, in one mixed-precision add (the
+// bf16 operand is widened exactly), without unpacking it first.
+__device__ __forceinline__ float add_bf16_lo(float acc, uint32_t w) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+      : "=f"(d)
+      : "r"(w), "f"(acc));
+  return d;
+}
+__device__ __forceinline__ float add_bf16_hi(float acc, uint32_t w) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+      : "=f"(d)
+      : "r"(w), "f"(acc));
+  return d;
+}
 // max of three floats in one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

@@ -111,30 +111,7 @@ int grid_for(long long n8) {
   return g < 1 ? 1 : (int)g;
 }
 
-// Special-function-unit rate: every thread runs 8 independent chains x <- 2^(-x)
-// (values stay in [0.5, 1], no subnormals or overflow), so the exp2 pipe, not the
-// chains' latency, sets the time.  out[i] keeps the chains' sum so nothing is elided.
-constexpr int kEx2Threads = 512, kEx2Chains = 8;
-__global__ void __launch_bounds__(kEx2Threads) ex2_probe_kernel(float* out, int iters) {
-  float x[kEx2Chains];
-#pragma unroll
-  for (int c = 0; c < kEx2Chains; ++c) x[c] = 0.03125f * (float)((threadIdx.x + c) & 31);
-  for (int it = 0; it < iters; ++it) {
-#pragma unroll
-    for (int c = 0; c < kEx2Chains; ++c) asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(x[c]) : "f"(-x[c]));
-  }
-  float s = 0.f;
-#pragma unroll
-  for (int c = 0; c < kEx2Chains; ++c) s += x[c];
-  out[(size_t)blockIdx.x * kEx2Threads + threadIdx.x] = s;
-}
-
 }  // namespace quant
-
-cudaError_t launch_ex2_probe(float* out, int n_blocks, int iters, cudaStream_t st) {
-  quant::ex2_probe_kernel<<<n_blocks, quant::kEx2Threads, 0, st>>>(out, iters);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_amax_bf16(const void* x, long long n, float* amax, cudaStream_t st) {
   quant::amax_kernel<<<quant::grid_for(n / 8 + 1), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), n,
