@@ -106,6 +106,19 @@ int fa_device_status(unsigned* site, int reset);
 void fa_set_wait_limit_ns(unsigned long long ns);
 
 /*
+ * Schedule of fa_fwd's kernel for the dense layout without a window mask, when its
+ * (query-tile pair, head) units are more than the SMs can hold at once (no counterpart
+ * on the pages; a scheduling choice, not a change of the result):
+ *   1 (default)  persistent CTAs: a CTA that finishes a unit takes over the next CTA of
+ *                its grid that has not started, so one CTA's pipelines run on across
+ *                units (the next unit's loads and first score GEMMs overlap the current
+ *                unit's end);
+ *   0            one CTA per unit.
+ * Both compute every output bitwise the same.  Process-wide; returns the previous value.
+ */
+int fa_set_fwd_persistent(int on);
+
+/*
  * Self-test hook for the timeout path: launches a one-warp kernel that waits,
  * with the given limit, on a barrier nothing ever arrives on; it then records
  * FA_ERR_TIMEOUT in the status word and exits normally (no trap, no hang).

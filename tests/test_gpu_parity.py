@@ -300,7 +300,7 @@ def test_binding_rejects_bad_tensors():
 
 
 REPEAT_CASES = [I.Problem(2, 8, 2048, 2048, 128, True), I.Problem(2, 8, 2048, 2048, 64, False),
-                I.Problem(1, 16, 1000, 1000, 32, True)]
+                I.Problem(1, 16, 1000, 1000, 32, True), I.Problem(4, 16, 2048, 2048, 128, True)]
 
 
 @pytest.mark.parametrize("p", REPEAT_CASES, ids=[p.name() for p in REPEAT_CASES])
@@ -324,6 +324,36 @@ def test_repeated_runs_are_identical(p):
         assert err <= 1e-2 * dq0.float().abs().max().item(), err
     torch.cuda.synchronize()
     assert _lib.fa_device_status()[0] == _lib.FA_OK
+
+
+# more (query-tile pair, head) units than SMs: the forward runs persistent CTAs by default
+PERSIST_CASES = [I.Problem(2, 16, 2048, 2048, 128, True), I.Problem(2, 16, 2048, 2048, 64, False),
+                 I.Problem(4, 16, 1100, 1100, 32, True), I.Problem(4, 16, 1000, 1500, 16, True),
+                 I.Problem(4, 16, 1500, 1000, 128, False), I.Problem(8, 32, 300, 300, 64, True)]
+
+
+@pytest.mark.parametrize("p", PERSIST_CASES, ids=[p.name() for p in PERSIST_CASES])
+def test_persistent_forward_equals_one_cta_per_unit(p):
+    # the persistent schedule changes which SM runs a unit, never the arithmetic: O and L
+    # are bitwise those of one CTA per unit, and both match the oracle on sampled heads
+    assert p.B * p.H * ((p.Nq + 255) // 256) > 152
+    q, k, v, _ = I.draw(p, 12)
+    dev = torch.device("cuda")
+    qg, kg, vg = (t.to(dev) for t in (q, k, v))
+    prev = _lib.fa_set_fwd_persistent(False)
+    try:
+        o1, l1 = _lib.forward(qg, kg, vg, p.causal, p.scale)
+        _lib.fa_set_fwd_persistent(True)
+        o2, l2 = _lib.forward(qg, kg, vg, p.causal, p.scale)
+        torch.cuda.synchronize()
+    finally:
+        _lib.fa_set_fwd_persistent(prev)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for (b, h) in ((0, 0), (p.B - 1, p.H - 1)):
+        qd, kd, vd = (I.as_f64(t[b, h]) for t in (q, k, v))
+        ro, rl = oracle.forward_head(qd, kd, vd, p.scale, p.causal)
+        assert_close(f"{p.name()} b{b}h{h} O", f64(o2[b, h]), ro)
+        assert_lse(f"{p.name()} b{b}h{h} L", f64(l2[b, h]), rl)
 
 
 def test_tensors_beyond_2_31_elements():

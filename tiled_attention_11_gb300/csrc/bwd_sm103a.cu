@@ -218,34 +218,34 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 
   if (warp == C::W_PRODUCER) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0 && n_it > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(&bars[C::B_KV], 2 * C::KV_TILE);
+    if (n_it > 0) {
+      if (lane == 0) tma_prefetch_desc(&tm_q);
+      if (lane == 0) tma_prefetch_desc(&tm_k);
+      if (lane == 0) tma_prefetch_desc(&tm_v);
+      if (lane == 0) tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx_w(&bars[C::B_KV], 2 * C::KV_TILE);
       for (int c = 0; c < C::NCHUNK; ++c) {
-        tma_load_3d(smem + C::OFF_K + c * C::K_CHUNK_BYTES, &tm_k, &bars[C::B_KV], c * C::CHUNK, ty(k0), tzk(k0));
-        tma_load_3d(smem + C::OFF_V + c * C::K_CHUNK_BYTES, &tm_v, &bars[C::B_KV], c * C::CHUNK, ty(k0), tzk(k0));
+        tma_load_3d_w(smem + C::OFF_K + c * C::K_CHUNK_BYTES, &tm_k, &bars[C::B_KV], c * C::CHUNK, ty(k0), tzk(k0));
+        tma_load_3d_w(smem + C::OFF_V + c * C::K_CHUNK_BYTES, &tm_v, &bars[C::B_KV], c * C::CHUNK, ty(k0), tzk(k0));
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % C::NS;
         const int i = qs.at(it);
-        if (it >= C::NS && !mbar_wait(&bars[C::B_QE + s], ((it / C::NS) - 1) & 1, wc, 31)) break;
-        mbar_arrive_expect_tx(&bars[C::B_QF + s], 2 * C::Q_TILE + 2 * C::BM * 4);
+        if (it >= C::NS && !mbar_wait_w(&bars[C::B_QE + s], ((it / C::NS) - 1) & 1, wc, 31)) break;
+        mbar_arrive_expect_tx_w(&bars[C::B_QF + s], 2 * C::Q_TILE + 2 * C::BM * 4);
         for (int c = 0; c < C::NCHUNK; ++c) {
-          tma_load_3d(smem + C::OFF_Q + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_q, &bars[C::B_QF + s],
+          tma_load_3d_w(smem + C::OFF_Q + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_q, &bars[C::B_QF + s],
                       c * C::CHUNK, ty(i * C::BM), tzq(i * C::BM));
-          tma_load_3d(smem + C::OFF_DO + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_do, &bars[C::B_QF + s],
+          tma_load_3d_w(smem + C::OFF_DO + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_do, &bars[C::B_QF + s],
                       c * C::CHUNK, ty(i * C::BM), tzq(i * C::BM));
         }
         const size_t roff = (size_t)wrow0 + (size_t)i * C::BM;
-        bulk_load(smem + C::OFF_LSE + s * C::BM * 4, p.lse2 + roff, C::BM * 4, &bars[C::B_QF + s]);
-        bulk_load(smem + C::OFF_DLT + s * C::BM * 4, p.dlt + roff, C::BM * 4, &bars[C::B_QF + s]);
+        bulk_load_w(smem + C::OFF_LSE + s * C::BM * 4, p.lse2 + roff, C::BM * 4, &bars[C::B_QF + s]);
+        bulk_load_w(smem + C::OFF_DLT + s * C::BM * 4, p.dlt + roff, C::BM * 4, &bars[C::B_QF + s]);
         issued = it + 1;
       }
-      if (*abort_flag) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         volatile int no_abort = 0;
         const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
         mbar_wait(&bars[C::B_KV], 0, w2, 40);
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     }
   } else if (warp == C::W_MMA_A) {
     // ---------------------------------------------------------------- UMMA issuer A: S^T, dP^T
-    if (lane == 0 && n_it > 0) {
+    if (n_it > 0) {
       const uint64_t dK = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);       // K, K-major
       const uint64_t dV = sdesc(sbase + C::OFF_V, 16, 8 * C::ROWB, C::LAYOUT);       // V, K-major
       const uint64_t dQk = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);      // Q stage 0, K-major
@@ -266,19 +266,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const uint32_t d = tmem + C::T_S + (uint32_t)((it & 1) * 64);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(d, desc_adv(dK, koff<D>(C::K_CHUNK_BYTES, kk)), desc_adv(q, koff<D>(C::Q_CHUNK_BYTES, kk)),
+          umma_ss_w(d, desc_adv(dK, koff<D>(C::K_CHUNK_BYTES, kk)), desc_adv(q, koff<D>(C::Q_CHUNK_BYTES, kk)),
                   C::IDESC_S, kk > 0 ? 1u : 0u);
-        umma_commit(&bars[C::B_SF + (it & 1)]);
+        umma_commit_w(&bars[C::B_SF + (it & 1)]);
       };
       auto issue_dp = [&](int it) {  // dP^T(it) = V dO^T
         const uint64_t o = desc_adv(dOk, (uint32_t)((it % C::NS) * C::Q_TILE));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + C::T_DP, desc_adv(dV, koff<D>(C::K_CHUNK_BYTES, kk)), desc_adv(o, koff<D>(C::Q_CHUNK_BYTES, kk)),
+          umma_ss_w(tmem + C::T_DP, desc_adv(dV, koff<D>(C::K_CHUNK_BYTES, kk)), desc_adv(o, koff<D>(C::Q_CHUNK_BYTES, kk)),
                   C::IDESC_S, kk > 0 ? 1u : 0u);
-        umma_commit(&bars[C::B_DPF]);
+        umma_commit_w(&bars[C::B_DPF]);
       };
-      bool ok = mbar_wait(&bars[C::B_KV], 0, wc, 32) && mbar_wait(&bars[C::B_QF], 0, wc, 33);
+      bool ok = mbar_wait_w(&bars[C::B_KV], 0, wc, 32) && mbar_wait_w(&bars[C::B_QF], 0, wc, 33);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -286,65 +286,65 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       for (int it = 0; ok && it < n_it; ++it) {
         // dP^T(it) overwrites dP^T(it-1) in TMEM once the compute warps have loaded it (its
         // stage is loaded: S^T(it) waited for it)
-        if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DPE], (it - 1) & 1, wc, 35))) break;
+        if (it >= 1 && !(ok = mbar_wait_w(&bars[C::B_DPE], (it - 1) & 1, wc, 35))) break;
         tc_fence_after();
         issue_dp(it);
         // S^T(it+1) goes to the buffer that held P^T(it-1), then dQ^T(it-1): after the dQ
         // warpgroup drained it (which follows dV(it-1) and dQ^T(it-1) in issuer B's order)
         if (it + 1 < n_it) {
           const int s1 = (it + 1) % C::NS, b1 = (it + 1) & 1;
-          if (!(ok = mbar_wait(&bars[C::B_QF + s1], ((it + 1) / C::NS) & 1, wc, 33))) break;
-          if (it >= 1 && !(ok = mbar_wait(&bars[C::B_DQE + b1], ((it - 1) >> 1) & 1, wc, 49))) break;
+          if (!(ok = mbar_wait_w(&bars[C::B_QF + s1], ((it + 1) / C::NS) & 1, wc, 33))) break;
+          if (it >= 1 && !(ok = mbar_wait_w(&bars[C::B_DQE + b1], ((it - 1) >> 1) & 1, wc, 49))) break;
           tc_fence_after();
           issue_s(it + 1);
         }
       }
-      umma_commit(&bars[C::B_DRAIN]);
+      umma_commit_w(&bars[C::B_DRAIN]);
       volatile int no_abort = 0;
       const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
       mbar_wait(&bars[C::B_DRAIN], 0, w2, 42);
     }
   } else if (warp == C::W_MMA_B) {
     // ---------------------------------------------------------------- UMMA issuer B: dV, dK, dQ^T
-    if (lane == 0 && n_it > 0) {
+    if (n_it > 0) {
       const uint64_t dQm = sdesc(sbase + C::OFF_Q, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // MN-major
       const uint64_t dOm = sdesc(sbase + C::OFF_DO, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);  // MN-major
       const uint64_t dS0 = sdesc(sbase + C::OFF_DS, C::DS_BYTES, 1024, 2u);          // dS^T buffer 0, MN-major
       const uint64_t dSa = sdesc(sbase + C::OFF_DS, 16, 1024, 2u);                   // the same, K-major A
-      bool ok = mbar_wait(&bars[C::B_KV], 0, wc, 32);
+      bool ok = mbar_wait_w(&bars[C::B_KV], 0, wc, 32);
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % C::NS, b = it & 1;
         const uint64_t qm = desc_adv(dQm, (uint32_t)(s * C::Q_TILE));
         const uint64_t om = desc_adv(dOm, (uint32_t)(s * C::Q_TILE));
         // dV += P^T dO_i once P^T(it) is in TMEM buffer b
-        if (!(ok = mbar_wait(&bars[C::B_PF + b], (it >> 1) & 1, wc, 34))) break;
+        if (!(ok = mbar_wait_w(&bars[C::B_PF + b], (it >> 1) & 1, wc, 34))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          umma_ts(tmem + C::T_DV, tmem + C::T_S + (uint32_t)(b * 64) + a_col(kk), desc_adv(om, mnoff<D>(kk)),
+          umma_ts_w(tmem + C::T_DV, tmem + C::T_S + (uint32_t)(b * 64) + a_col(kk), desc_adv(om, mnoff<D>(kk)),
                   C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q_i and dQ_i^T = K^T dS^T once dS^T is in shared memory buffer b (one
         // copy serves both: 128-byte swizzled rows of 64 queries per key are the K-major A
         // layout of dK and the MN-major B layout of dQ^T)
-        if (!(ok = mbar_wait(&bars[C::B_DSF + b], (it >> 1) & 1, wc, 36))) break;
-        if (it == 0 && !(ok = mbar_wait(&bars[C::B_KT], 0, wc, 47))) break;
+        if (!(ok = mbar_wait_w(&bars[C::B_DSF + b], (it >> 1) & 1, wc, 36))) break;
+        if (it == 0 && !(ok = mbar_wait_w(&bars[C::B_KT], 0, wc, 47))) break;
         tc_fence_after();
         const uint64_t dsa = desc_adv(dSa, (uint32_t)(b * C::DS_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          umma_ss(tmem + C::T_DK, desc_adv(dsa, (uint32_t)(kk * 32)), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
+          umma_ss_w(tmem + C::T_DK, desc_adv(dsa, (uint32_t)(kk * 32)), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
                   (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&bars[C::B_QE + s]);  // dK was the stage's last reader
+        umma_commit_w(&bars[C::B_QE + s]);  // dK was the stage's last reader
         // dQ^T(it) into buffer b, which dV(it) (issued above: in-order) has finished reading
         const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts(tmem + C::T_S + (uint32_t)(b * 64), tmem + C::T_KT + kk * 8, desc_adv(ds, (uint32_t)(kk * 16 * 128)),
+          umma_ts_w(tmem + C::T_S + (uint32_t)(b * 64), tmem + C::T_KT + kk * 8, desc_adv(ds, (uint32_t)(kk * 16 * 128)),
                   C::IDESC_DQ, kk > 0 ? 1u : 0u);
-        umma_commit(&bars[C::B_DQF + b]);
-        umma_commit(&bars[C::B_DQR + b]);
+        umma_commit_w(&bars[C::B_DQF + b]);
+        umma_commit_w(&bars[C::B_DQR + b]);
       }
-      umma_commit(&bars[C::B_DRAIN + 1]);
+      umma_commit_w(&bars[C::B_DRAIN + 1]);
       volatile int no_abort = 0;
       const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
       mbar_wait(&bars[C::B_DRAIN + 1], 0, w2, 42);

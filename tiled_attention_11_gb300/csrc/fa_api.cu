@@ -18,6 +18,10 @@ __device__ unsigned g_fa_status[2];
 
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 
+// Forward kernel choice for the dense layout with plain masks beyond one wave: 1 the
+// persistent kernel, 0 one CTA per unit (the persistent kernel's parity tests compare the two).
+std::atomic<int> g_fwd_persist{1};
+
 // Optional events recorded around the main backward kernel (timing hook).
 std::mutex g_ev_mu;
 cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
@@ -231,6 +235,8 @@ const char* fa_strerror(int status) {
 
 void fa_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns : 1ull); }
 
+int fa_set_fwd_persistent(int on) { return g_fwd_persist.exchange(on ? 1 : 0); }
+
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int D) {
   if (check_sizes(B, H, Nq, Nk, D, 1.f) != FA_OK) return 0;
   return ws_layout(B, H, Nq, D).total;
@@ -304,9 +310,9 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
   rc = current_device(&status);
   if (rc != FA_OK) return rc;
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_map(&tq, q, D, Nq, (int)BH, 128) || !make_map(&tk, k, D, Nk, (int)BH, 128) ||
-      !make_map(&tv, v, D, Nk, (int)BH, 128))
+      !make_map(&tv, v, D, Nk, (int)BH, 128) || !make_map(&to, o, D, Nq, (int)BH, 128))
     return FA_ERR_LAUNCH;
   ta11::FwdParams p{};
   p.o = o;
@@ -321,6 +327,7 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
   // (tile t with tile n-1-t) so that every CTA walks about the same number of key tiles.
   const long long n_ctas = (long long)BH * ((p.n_q_tiles + 1) / 2);
   p.fold = (!lm && causal && n_ctas <= current_sms()) ? 1 : 0;
+  p.persist = (!lm && !p.fold && n_ctas > current_sms()) ? g_fwd_persist.load() : 0;
   if (lm) {
     p.lm = *lm;
     p.local = 1;
@@ -332,7 +339,7 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
       p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + split.o_bytes);
     }
   }
-  if (ta11::launch_fwd(D, causal != 0, tq, tk, tv, p, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (ta11::launch_fwd(D, causal != 0, tq, tk, tv, to, p, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   if (split.n_gp > 0) {
     ta11::FwdCombineParams cp{p.part_o, p.part_ml, o, lse, Nq, split.n_gp * 256, split.n_split};
     if (ta11::launch_fwd_combine(D, cp, (int)BH, stream) != cudaSuccess) return FA_ERR_LAUNCH;
@@ -677,6 +684,8 @@ extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* 
   if (!make_map_packed(&tq, q, D, H, total_q, 128) || !make_map_packed(&tk, k, D, H, total_k, 128) ||
       !make_map_packed(&tv, v, D, H, total_k, 128))
     return FA_ERR_LAUNCH;
+  // (the packed layout stores O row by row: a bulk store of a tile would write past a
+  // sequence's end into the next one; its O map argument is unused)
   ta11::FwdParams p{};
   p.o = o;
   p.lse = lse;
@@ -687,7 +696,7 @@ extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* 
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = status;
   p.va = ta11::VarlenArgs{cu_seqlens_q, cu_seqlens_k, H, total_q, total_k};
-  return ta11::launch_fwd(D, causal != 0, tq, tk, tv, p, B * H, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  return ta11::launch_fwd(D, causal != 0, tq, tk, tv, tq, p, B * H, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 extern "C" size_t fa_bwd_varlen_workspace_size(int B, int H, int total_q, int max_seqlen_q, int D) {

@@ -107,6 +107,9 @@ struct FwdParams {
   // whose CTA `pair` holds query tiles pair and n_q_tiles-1-pair instead of 2*pair and
   // 2*pair+1, so every CTA walks about the same number of key tiles.
   int fold;
+  // Dense layout, plain masks, more units than one wave: the persistent kernel (a CTA
+  // takes over not-yet-started CTAs of its grid instead of exiting).
+  int persist;
 };
 
 struct FwdCombineParams {
@@ -191,8 +194,9 @@ struct Fp8FwdParams {
 // Host launchers (return cudaError_t of the launch).
 // Launchers; p.va.cu_q != nullptr selects the variable-length layout, p.local the
 // local-window + global-token mask (dense layout only).
+// `to` maps O for the dense layout's bulk-store epilogue (unused by the packed layout).
 cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int BH, cudaStream_t st);
+                       const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t st);
 cudaError_t launch_fwd_combine(int D, const FwdCombineParams& p, int BH, cudaStream_t st);
 cudaError_t launch_bwd_prep(int D, const PrepParams& p, cudaStream_t st);
 cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -125,27 +125,27 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 
   if (warp == C::W_PRODUCER) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_vt);
+    {
+      if (lane == 0) tma_prefetch_desc(&tm_q);
+      if (lane == 0) tma_prefetch_desc(&tm_k);
+      if (lane == 0) tma_prefetch_desc(&tm_vt);
       for (int t = 0; t < 2; ++t) {
-        mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_QK);
-        tma_load_3d(smem + C::OFF_Q + t * C::TILE_QK, &tm_q, &bars[C::B_Q + t], 0, q0 + t * C::BM, bh);
+        mbar_arrive_expect_tx_w(&bars[C::B_Q + t], C::TILE_QK);
+        tma_load_3d_w(smem + C::OFF_Q + t * C::TILE_QK, &tm_q, &bars[C::B_Q + t], 0, q0 + t * C::BM, bh);
       }
       int k_issued = 0, v_issued = 0;  // K and V tiles whose copies were started
       for (int j = 0; j < n_kv1; ++j) {
         const int s = j % C::NS;
-        if (j >= C::NS && !mbar_wait(&bars[C::B_KE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
-        mbar_arrive_expect_tx(&bars[C::B_KF + s], C::TILE_QK);
-        tma_load_3d(smem + C::OFF_K + s * C::TILE_QK, &tm_k, &bars[C::B_KF + s], 0, j * C::BN, bh);
+        if (j >= C::NS && !mbar_wait_w(&bars[C::B_KE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
+        mbar_arrive_expect_tx_w(&bars[C::B_KF + s], C::TILE_QK);
+        tma_load_3d_w(smem + C::OFF_K + s * C::TILE_QK, &tm_k, &bars[C::B_KF + s], 0, j * C::BN, bh);
         k_issued = j + 1;
-        if (j >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
-        mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_VT);
-        tma_load_3d(smem + C::OFF_V + s * C::TILE_VT, &tm_vt, &bars[C::B_VF + s], j * C::BN, 0, bh);
+        if (j >= C::NS && !mbar_wait_w(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
+        mbar_arrive_expect_tx_w(&bars[C::B_VF + s], C::TILE_VT);
+        tma_load_3d_w(smem + C::OFF_V + s * C::TILE_VT, &tm_vt, &bars[C::B_VF + s], j * C::BN, 0, bh);
         v_issued = j + 1;
       }
-      if (*abort_flag) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         // Let every copy already started land before the CTA can exit: the last NS of
         // each ring, one per slot, so that each wait is on its slot's newest phase.
         volatile int no_abort = 0;
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     }
   } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------------- UMMA issuer
-    if (lane == 0) {
+    {
       // K-major descriptors for Q, the K ring and the V^T ring; a 32-byte K slice is a
       // 32-byte step inside the swizzled row.
       const uint64_t dq0 = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT_QK);
@@ -171,50 +171,50 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const uint64_t dk = desc_adv(dk0, (uint32_t)(slot * C::TILE_QK));
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk)
-          umma_ss_f8(tmem + C::TMEM_S + t * 128, desc_adv(dq, (uint32_t)(kk * 32)), desc_adv(dk, (uint32_t)(kk * 32)),
+          umma_ss_f8_w(tmem + C::TMEM_S + t * 128, desc_adv(dq, (uint32_t)(kk * 32)), desc_adv(dk, (uint32_t)(kk * 32)),
                      C::IDESC_S, kk > 0 ? 1u : 0u);
-        umma_commit(&bars[C::B_SF + t]);
+        umma_commit_w(&bars[C::B_SF + t]);
       };
       auto issue_pv = [&](int t, int slot, bool acc) {  // O_t (+)= P_t V  (A = P in TMEM, 4 per column)
         const uint64_t dv = desc_adv(dv0, (uint32_t)(slot * C::TILE_VT));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 32; ++kk)
-          umma_ts_f8(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * 128 + kk * 8, desc_adv(dv, (uint32_t)(kk * 32)),
+          umma_ts_f8_w(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * 128 + kk * 8, desc_adv(dv, (uint32_t)(kk * 32)),
                      C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-        umma_commit(&bars[C::B_O + t]);
+        umma_commit_w(&bars[C::B_O + t]);
       };
-      bool ok = mbar_wait(&bars[C::B_Q], 0, wc, 2) && mbar_wait(&bars[C::B_KF], 0, wc, 3);
+      bool ok = mbar_wait_w(&bars[C::B_Q], 0, wc, 2) && mbar_wait_w(&bars[C::B_KF], 0, wc, 3);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
-        if ((ok = mbar_wait(&bars[C::B_Q + 1], 0, wc, 2))) {
+        if ((ok = mbar_wait_w(&bars[C::B_Q + 1], 0, wc, 2))) {
           tc_fence_after();
           issue_s(1, 0);
-          umma_commit(&bars[C::B_KE]);
+          umma_commit_w(&bars[C::B_KE]);
         }
       }
       for (int j = 0; ok && j < n_kv1; ++j) {
         const int s = j % C::NS, s1 = (j + 1) % C::NS;
-        if (!(ok = mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
+        if (!(ok = mbar_wait_w(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
         const bool next_k = j + 1 < n_kv1;
-        if (next_k && !(ok = mbar_wait(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
+        if (next_k && !(ok = mbar_wait_w(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
         if (j < n_kv0) {
-          if (!(ok = mbar_wait(&bars[C::B_PF], j & 1, wc, 4))) break;
+          if (!(ok = mbar_wait_w(&bars[C::B_PF], j & 1, wc, 4))) break;
           tc_fence_after();
           issue_pv(0, s, j > 0);
           if (j + 1 < n_kv0) issue_s(0, s1);
         }
-        if (!(ok = mbar_wait(&bars[C::B_PF + 1], j & 1, wc, 4))) break;
+        if (!(ok = mbar_wait_w(&bars[C::B_PF + 1], j & 1, wc, 4))) break;
         tc_fence_after();
         issue_pv(1, s, j > 0);
-        umma_commit(&bars[C::B_VE + s]);
+        umma_commit_w(&bars[C::B_VE + s]);
         if (next_k) {
           issue_s(1, s1);
-          umma_commit(&bars[C::B_KE + s1]);
+          umma_commit_w(&bars[C::B_KE + s1]);
         }
       }
       // Every MMA issued so far must complete before TMEM is freed.
-      umma_commit(&bars[C::B_DRAIN]);
+      umma_commit_w(&bars[C::B_DRAIN]);
       volatile int no_abort = 0;
       const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
       mbar_wait(&bars[C::B_DRAIN], 0, w2, 23);

@@ -54,10 +54,12 @@ struct Cfg {
   static constexpr int OFF_Q = 0;                      // 2 tiles
   static constexpr int OFF_K = 2 * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NS * TILE_BYTES;
+  // O staging tile for the bulk tensor store of the epilogue (bf16, the TMA box layout)
+  static constexpr int OFF_STG = OFF_V + NS * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_STG + TILE_BYTES;
   // barriers: q_full[2], k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2],
-  // o_done[2], drain.  K and V stages are released separately: K_j is dead once both S
-  // MMAs that read it finish, long before P V_j, so its refill starts earlier.
+  // o_done[2], drain, staging free.  K and V stages are released separately: K_j is dead once
+  // both S MMAs that read it finish, long before P V_j, so its refill starts earlier.
   static constexpr int B_Q = 0;
   static constexpr int B_KF = 2;
   static constexpr int B_VF = 2 + NS;
@@ -67,8 +69,20 @@ struct Cfg {
   static constexpr int B_PF = 4 + 4 * NS;
   static constexpr int B_O = 6 + 4 * NS;
   static constexpr int B_DRAIN = 8 + 4 * NS;
-  static constexpr int NBAR = 9 + 4 * NS;
-  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int B_STG = 9 + 4 * NS;   // tile 0's store has read the staging tile
+  // persistent kernel only: tile 1's store has read the staging tile; Q tile t free (the last
+  // S MMA of a unit that reads it is done); work-unit ring slots full / empty; the answer of
+  // a launch-control request landed
+  static constexpr int B_STG1 = 10 + 4 * NS;
+  static constexpr int B_QE = 11 + 4 * NS;
+  static constexpr int NU = 4;               // work-unit ring slots
+  static constexpr int B_UF = 13 + 4 * NS;
+  static constexpr int B_UE = B_UF + NU;
+  static constexpr int B_CLC = B_UE + NU;
+  static constexpr int NBAR = B_CLC + 1;
+  static constexpr int OFF_CLC = OFF_BAR + ((NBAR * 8 + 16 + 15) / 16) * 16;  // 16-byte launch-control answer
+  static constexpr int OFF_UNITS = OFF_CLC + 16;                               // NU x int2 work units
+  static constexpr int SMEM_USED = OFF_UNITS + NU * 8;
   // At least ~120 KB so only one CTA (and one 512-column TMEM allocation) fits per SM.
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
   static constexpr int THREADS = 320;
@@ -115,10 +129,51 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
+// Epilogue of one query row on the bulk-store path: O (TMEM lane `row`, columns from t_o)
+// times inv_l, rounded to bf16, into the staging tile in the layout of the TMA box that
+// stores it (NCHUNK column chunks of 128 rows x ROWB bytes, 16-byte units swizzled by
+// row like every tile here).  Two TMEM loads in flight per wait.
+template <int D>
+__device__ __forceinline__ void stage_o_row(uint8_t* stg, int row, uint32_t t_o, float inv_l) {
+  using C = Cfg<D>;
+  constexpr int G = D / 16;  // groups of 16 columns
+  uint8_t* rbase = stg + row * C::ROWB;
+  const uint32_t sw = (uint32_t)((row * C::ROWB) >> 7) & (uint32_t)(C::ROWB / 16 - 1);
+#pragma unroll
+  for (int g = 0; g < G; g += 2) {
+    uint32_t a[2][16];
+    tmem_ld16(t_o + g * 16, a[0]);
+    if (g + 1 < G) tmem_ld16(t_o + (g + 1) * 16, a[1]);
+    tmem_wait_ld(a[0]);
+    if (g + 1 < G) reg_tie(a[1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (g + h >= G) break;
+      const int col = (g + h) * 16;
+      const int chunk = col / C::CHUNK, u = (col % C::CHUNK) / 8;  // first of two 16-byte units
+      uint8_t* cbase = rbase + chunk * C::CHUNK_BYTES;
+      const uint32_t* v = a[h];
+      uint4 w0, w1;
+      w0.x = pack_bf16(as_f(v[0]) * inv_l, as_f(v[1]) * inv_l);
+      w0.y = pack_bf16(as_f(v[2]) * inv_l, as_f(v[3]) * inv_l);
+      w0.z = pack_bf16(as_f(v[4]) * inv_l, as_f(v[5]) * inv_l);
+      w0.w = pack_bf16(as_f(v[6]) * inv_l, as_f(v[7]) * inv_l);
+      w1.x = pack_bf16(as_f(v[8]) * inv_l, as_f(v[9]) * inv_l);
+      w1.y = pack_bf16(as_f(v[10]) * inv_l, as_f(v[11]) * inv_l);
+      w1.z = pack_bf16(as_f(v[12]) * inv_l, as_f(v[13]) * inv_l);
+      w1.w = pack_bf16(as_f(v[14]) * inv_l, as_f(v[15]) * inv_l);
+      *reinterpret_cast<uint4*>(cbase + ((uint32_t)u ^ sw) * 16) = w0;
+      *reinterpret_cast<uint4*>(cbase + ((uint32_t)(u + 1) ^ sw) * 16) = w1;
+    }
+  }
+}
+
+
 template <int D, bool CAUSAL, bool VARLEN, bool LOCAL>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -207,6 +262,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(&bars[C::B_VE + s], 1);
     }
     mbar_init(&bars[C::B_DRAIN], 1);
+    mbar_init(&bars[C::B_STG], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -221,35 +277,35 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 
   if (warp == C::W_PRODUCER) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+    {
+      if (lane == 0) tma_prefetch_desc(&tm_q);
+      if (lane == 0) tma_prefetch_desc(&tm_k);
+      if (lane == 0) tma_prefetch_desc(&tm_v);
       for (int t = 0; t < 2; ++t) {
         if (!has_q[t]) continue;  // a tile without keys is never read
-        mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_BYTES);
+        mbar_arrive_expect_tx_w(&bars[C::B_Q + t], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
+          tma_load_3d_w(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
                       c * C::CHUNK, ty(q0 + t * C::BM), tzq(q0 + t * C::BM));
       }
       int k_issued = 0, v_issued = 0;  // K and V tiles whose copies were started
       int j = 0;
       for (int kt = first_kt; kt != TileSet::kNone; kt = next_kt(kt), ++j) {
         const int s = j % C::NS;
-        if (j >= C::NS && !mbar_wait(&bars[C::B_KE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
-        mbar_arrive_expect_tx(&bars[C::B_KF + s], C::TILE_BYTES);
+        if (j >= C::NS && !mbar_wait_w(&bars[C::B_KE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
+        mbar_arrive_expect_tx_w(&bars[C::B_KF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
+          tma_load_3d_w(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
                       c * C::CHUNK, ty(kt * C::BN), tzk(kt * C::BN));
         k_issued = j + 1;
-        if (j >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
-        mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_BYTES);
+        if (j >= C::NS && !mbar_wait_w(&bars[C::B_VE + s], ((j / C::NS) - 1) & 1, wc, 1)) break;
+        mbar_arrive_expect_tx_w(&bars[C::B_VF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
+          tma_load_3d_w(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
                       c * C::CHUNK, ty(kt * C::BN), tzk(kt * C::BN));
         v_issued = j + 1;
       }
-      if (*abort_flag) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         // Let every copy already started land before the CTA can exit: the last NS of
         // each ring, one per slot, so that each wait is on its slot's newest phase.
         volatile int no_abort = 0;
@@ -264,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     }
   } else if (warp == C::W_MMA) {
     // ---------------------------------------------------------------- UMMA issuer
-    if (lane == 0 && first_kt != TileSet::kNone) {
+    if (first_kt != TileSet::kNone) {
       // Base descriptors, built once: Q tiles and the K ring K-major, the V ring MN-major.
       const uint64_t dq0 = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);
       const uint64_t dk0 = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);
@@ -274,17 +330,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const uint64_t dk = desc_adv(dk0, (uint32_t)(slot * C::TILE_BYTES));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + C::TMEM_S + t * 128, desc_adv(dq, kmajor_off<D>(kk)), desc_adv(dk, kmajor_off<D>(kk)),
+          umma_ss_w(tmem + C::TMEM_S + t * 128, desc_adv(dq, kmajor_off<D>(kk)), desc_adv(dk, kmajor_off<D>(kk)),
                   C::IDESC_S, kk > 0 ? 1u : 0u);
-        umma_commit(&bars[C::B_SF + t]);
+        umma_commit_w(&bars[C::B_SF + t]);
       };
       auto issue_pv = [&](int t, int slot, bool acc) {  // O_t (+)= P_t V   (A = P from TMEM)
         const uint64_t dv = desc_adv(dv0, (uint32_t)(slot * C::TILE_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * 128 + kk * 8,
+          umma_ts_w(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * 128 + kk * 8,
                   desc_adv(dv, (uint32_t)(kk * 16 * C::ROWB)), C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-        umma_commit(&bars[C::B_O + t]);
+        umma_commit_w(&bars[C::B_O + t]);
       };
       // Position j of the walk holds key tile kt in ring slot j % NS; query tile t takes
       // part when its set has kt.  S_t of a position is issued one position ahead, after
@@ -297,44 +353,44 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // sits on the critical path (a general walk here cost 2% of the forward), so it
         // stays this lean.
         const int n_kv0 = ks0.count(), n_kv1 = ks1.count();
-        ok = mbar_wait(&bars[C::B_Q], 0, wc, 2) && mbar_wait(&bars[C::B_KF], 0, wc, 3);
+        ok = mbar_wait_w(&bars[C::B_Q], 0, wc, 2) && mbar_wait_w(&bars[C::B_KF], 0, wc, 3);
         if (ok) {
           tc_fence_after();
           issue_s(0, 0);
-          if ((ok = mbar_wait(&bars[C::B_Q + 1], 0, wc, 2))) {
+          if ((ok = mbar_wait_w(&bars[C::B_Q + 1], 0, wc, 2))) {
             tc_fence_after();
             issue_s(1, 0);
-            umma_commit(&bars[C::B_KE]);
+            umma_commit_w(&bars[C::B_KE]);
           }
         }
         for (int j = 0; ok && j < n_kv1; ++j) {
           const int s = j % C::NS, s1 = (j + 1) % C::NS;
-          if (!(ok = mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
+          if (!(ok = mbar_wait_w(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
           const bool next_k = j + 1 < n_kv1;
-          if (next_k && !(ok = mbar_wait(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
+          if (next_k && !(ok = mbar_wait_w(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
           // tile 0: P0_j -> O0, then S0 of the next key tile over the consumed P0
           if (j < n_kv0) {
-            if (!(ok = mbar_wait(&bars[C::B_PF], j & 1, wc, 4))) break;
+            if (!(ok = mbar_wait_w(&bars[C::B_PF], j & 1, wc, 4))) break;
             tc_fence_after();
             issue_pv(0, s, j > 0);
             if (j + 1 < n_kv0) issue_s(0, s1);
           }
           // tile 1
-          if (!(ok = mbar_wait(&bars[C::B_PF + 1], j & 1, wc, 4))) break;
+          if (!(ok = mbar_wait_w(&bars[C::B_PF + 1], j & 1, wc, 4))) break;
           tc_fence_after();
           issue_pv(1, s, j > 0);
-          umma_commit(&bars[C::B_VE + s]);
+          umma_commit_w(&bars[C::B_VE + s]);
           if (next_k) {
             issue_s(1, s1);
-            umma_commit(&bars[C::B_KE + s1]);
+            umma_commit_w(&bars[C::B_KE + s1]);
           }
         }
       } else {
-        ok = mbar_wait(&bars[C::B_KF], 0, wc, 3);
+        ok = mbar_wait_w(&bars[C::B_KF], 0, wc, 3);
         bool q0_ready = false, q1_ready = false;
         auto wait_q = [&](int t, bool& ready) {  // Q_t lands once; wait before its first S
           if (!ready) {
-            if (!mbar_wait(&bars[C::B_Q + t], 0, wc, 2)) return false;
+            if (!mbar_wait_w(&bars[C::B_Q + t], 0, wc, 2)) return false;
             ready = true;
           }
           tc_fence_after();
@@ -342,7 +398,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         };
         if (ok && ks0.has(first_kt) && (ok = wait_q(0, q0_ready))) issue_s(0, 0);
         if (ok && ks1.has(first_kt) && (ok = wait_q(1, q1_ready))) issue_s(1, 0);
-        if (ok) umma_commit(&bars[C::B_KE]);
+        if (ok) umma_commit_w(&bars[C::B_KE]);
         int n_pv0 = 0, n_pv1 = 0;
         int j = 0;
         for (int kt = first_kt; ok && kt != TileSet::kNone; ++j) {
@@ -351,11 +407,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           const bool next_k = kn != TileSet::kNone;
           const bool a0 = ks0.has(kt), a1 = ks1.has(kt);            // tiles taking part now
           const bool n0 = next_k && ks0.has(kn), n1 = next_k && ks1.has(kn);  // and at the next position
-          if (!(ok = mbar_wait(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
-          if (next_k && !(ok = mbar_wait(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
+          if (!(ok = mbar_wait_w(&bars[C::B_VF + s], (j / C::NS) & 1, wc, 5))) break;
+          if (next_k && !(ok = mbar_wait_w(&bars[C::B_KF + s1], ((j + 1) / C::NS) & 1, wc, 3))) break;
           // tile 0: P0 -> O0, then S0 of its next key tile over the consumed P0
           if (a0) {
-            if (!(ok = mbar_wait(&bars[C::B_PF], n_pv0 & 1, wc, 4))) break;
+            if (!(ok = mbar_wait_w(&bars[C::B_PF], n_pv0 & 1, wc, 4))) break;
             tc_fence_after();
             issue_pv(0, s, n_pv0 > 0);
             ++n_pv0;
@@ -368,12 +424,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           }
           // tile 1
           if (a1) {
-            if (!(ok = mbar_wait(&bars[C::B_PF + 1], n_pv1 & 1, wc, 4))) break;
+            if (!(ok = mbar_wait_w(&bars[C::B_PF + 1], n_pv1 & 1, wc, 4))) break;
             tc_fence_after();
             issue_pv(1, s, n_pv1 > 0);
             ++n_pv1;
           }
-          umma_commit(&bars[C::B_VE + s]);
+          umma_commit_w(&bars[C::B_VE + s]);
           if (next_k) {
             if (n1) {
               if (!a1 || !q1_ready) {
@@ -381,13 +437,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
               }
               issue_s(1, s1);
             }
-            umma_commit(&bars[C::B_KE + s1]);
+            umma_commit_w(&bars[C::B_KE + s1]);
           }
           kt = kn;
         }
       }
       // Every MMA issued so far must complete before TMEM is freed.
-      umma_commit(&bars[C::B_DRAIN]);
+      umma_commit_w(&bars[C::B_DRAIN]);
       volatile int no_abort = 0;
       const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
       mbar_wait(&bars[C::B_DRAIN], 0, w2, 23);
@@ -537,12 +593,36 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         *reinterpret_cast<float4*>(p.part_ml + rec * 4) =
             n_kv > 0 ? make_float4(m, l, lr, 0.f) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
       }
-    } else if (ok && n_kv == 0) {  // this tile's rows see no key: O = 0, L = -inf
+    } else if (n_kv_all == 0) {  // this tile's rows see no key: O = 0, L = -inf
       if (q_idx < sv.Nq) {
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + o_row(q_idx);
         for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
         p.lse[lse_idx(q_idx)] = -INFINITY;
       }
+    } else if (!VARLEN) {  // (every branch so far is uniform over the warpgroup)
+      // Dense layout: O goes through the staging tile and one bulk tensor store per column
+      // chunk (rows past Nq are clipped by the tensor map), so the warps do not wait on
+      // scattered 16-byte global stores.  Tile 1 takes the staging tile after tile 0's store
+      // has read it.  The four warps agree on the outcome of their waits first, so all of
+      // them meet at the named barrier.
+      bool go = ok && warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8);
+      if (t == 1) go = warp_wait(&bars[C::B_STG], 0, wc, 9) && go;
+      go = named_bar_and(1 + t, 128, go);
+      if (go) {
+        tc_fence_after();
+        // (local mask: a row with no visible key has lr = l = 0 and gets O = 0, L = -inf)
+        stage_o_row<D>(smem + C::OFF_STG, row, t_o, (LOCAL && lr == 0.f) ? 0.f : 1.f / lr);
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1 + t, 128);
+      if (go && row == 0 && qt0 < sv.Nq) {  // (a tile wholly past the rows stores nothing)
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_store_3d(&tm_o, smem + C::OFF_STG + c * C::CHUNK_BYTES, c * C::CHUNK, qt0, bh);
+        bulk_commit_group();
+        bulk_wait_read_all();  // the staging tile is free again (and may be released before exit)
+      }
+      if (go && q_idx < sv.Nq)
+        p.lse[lse_idx(q_idx)] = (LOCAL && l == 0.f) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
     } else if (ok && warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8)) {
       tc_fence_after();
       // (local mask: a row with no visible key has lr = l = 0 and gets O = 0, L = -inf)
@@ -569,6 +649,373 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
       if (q_idx < sv.Nq)
         p.lse[lse_idx(q_idx)] = (LOCAL && l == 0.f) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+    }
+    // Tile 0 hands the staging tile to tile 1 whatever path its epilogue took (its own
+    // store, if any, has been read: the issuing thread waited above).
+    if (t == 0 && row == 0) mbar_arrive(&bars[C::B_STG]);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::W_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Persistent form of the two-tile kernel for the dense layout with the plain masks.  The
+// grid still has one CTA per (query-tile pair, batch*head) in the same order, but a
+// running CTA takes over the next CTA that has not started yet (cluster launch control)
+// instead of exiting, so the hardware keeps handing out units heaviest-first to whichever
+// SM frees up, while the CTA's pipelines run on across units: the producer loads the
+// next unit's Q tiles as soon as the current unit's last S MMAs have read the old ones,
+// and the issuer computes the next unit's first S tiles while the softmax warpgroups are
+// still in the current unit's epilogue.  Per-CTA set-up (barriers, TMEM, descriptor
+// prefetch) is paid once per SM instead of once per unit.
+//   warp 8 lane 0  publishes each unit in a 4-slot ring (unit_full / unit_empty
+//                  barriers), issues the copies, and asks for the next unit once the
+//                  current one's last copies are started;
+//   warp 9 lane 0  issues the UMMAs exactly as the two-tile kernel, with ring positions
+//                  and barrier phases counted across units;
+//   warps 0-7      the two softmax warpgroups; each unit's epilogue stores O through the
+//                  staging tile, which the two tiles hand to each other (B_STG / B_STG1).
+// ------------------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
+    fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       const FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  void* clc_resp = smem + C::OFF_CLC;
+  int2* units = reinterpret_cast<int2*>(smem + C::OFF_UNITS);
+
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+  const int nkt = (p.Nk + C::BN - 1) / C::BN;
+  // key tiles of the query tile starting at row qa: [0, hi); a tile past the rows is
+  // computed and never stored, as in the two-tile kernel
+  auto n_keys = [&](int qa) { return CAUSAL ? min(nkt, qa / C::BM + 1) : nkt; };
+  const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars[C::B_Q + t], 1);
+      mbar_init(&bars[C::B_SF + t], 1);
+      mbar_init(&bars[C::B_PF + t], 128);
+      mbar_init(&bars[C::B_O + t], 1);
+      mbar_init(&bars[C::B_QE + t], 1);
+    }
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bars[C::B_KF + s], 1);
+      mbar_init(&bars[C::B_VF + s], 1);
+      mbar_init(&bars[C::B_KE + s], 1);
+      mbar_init(&bars[C::B_VE + s], 1);
+    }
+    for (int u = 0; u < C::NU; ++u) {
+      mbar_init(&bars[C::B_UF + u], 1);
+      mbar_init(&bars[C::B_UE + u], 9);  // the issuing thread and one lane of each softmax warp
+    }
+    mbar_init(&bars[C::B_DRAIN], 1);
+    mbar_init(&bars[C::B_STG], 1);
+    mbar_init(&bars[C::B_STG1], 1);
+    mbar_init(&bars[C::B_CLC], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::W_MMA) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::W_PRODUCER) {
+    // ---------------------------------------------------------------- scheduler + TMA producer
+    {
+      if (lane == 0) tma_prefetch_desc(&tm_q);
+      if (lane == 0) tma_prefetch_desc(&tm_k);
+      if (lane == 0) tma_prefetch_desc(&tm_v);
+      if (lane == 0) tma_prefetch_desc(&tm_o);
+      int ux = (int)blockIdx.x, uy = (int)blockIdx.y;  // the unit to publish next (ux < 0: none)
+      int jg = 0, k_issued = 0, v_issued = 0, q_units = 0;  // copies started (ring positions, Q pairs)
+      bool asked = false;  // a launch-control answer is pending
+      int n_asked = 0;
+      for (int i = 0;; ++i) {
+        const int us = i % C::NU;
+        if (i >= C::NU && !mbar_wait_w(&bars[C::B_UE + us], ((i / C::NU) - 1) & 1, wc, 10)) break;
+        units[us] = make_int2(ux, uy);
+        mbar_arrive_w(&bars[C::B_UF + us]);
+        if (ux < 0) break;
+        const int q0 = ((int)gridDim.x - 1 - ux) * 2 * C::BM, bh = uy;
+        const int n_kv = n_keys(q0 + C::BM);  // tile 1's walk contains tile 0's
+        bool ok = true;
+        for (int t = 0; t < 2 && ok; ++t) {  // Q_t is free once the last S MMA reading it is done
+          if (i >= 1 && !(ok = mbar_wait_w(&bars[C::B_QE + t], (i - 1) & 1, wc, 11))) break;
+          mbar_arrive_expect_tx_w(&bars[C::B_Q + t], C::TILE_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d_w(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
+                        c * C::CHUNK, q0 + t * C::BM, bh);
+        }
+        if (!ok) break;
+        q_units = i + 1;
+        for (int j = 0; j < n_kv && ok; ++j, ++jg) {
+          const int s = jg % C::NS;
+          if (jg >= C::NS && !(ok = mbar_wait_w(&bars[C::B_KE + s], ((jg / C::NS) - 1) & 1, wc, 1))) break;
+          mbar_arrive_expect_tx_w(&bars[C::B_KF + s], C::TILE_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d_w(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
+                        c * C::CHUNK, j * C::BN, bh);
+          k_issued = jg + 1;
+          if (jg >= C::NS && !(ok = mbar_wait_w(&bars[C::B_VE + s], ((jg / C::NS) - 1) & 1, wc, 1))) break;
+          mbar_arrive_expect_tx_w(&bars[C::B_VF + s], C::TILE_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d_w(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
+                        c * C::CHUNK, j * C::BN, bh);
+          v_issued = jg + 1;
+        }
+        if (!ok) break;
+        // Ask for the next unit only now, with this unit's last copies started (NS key tiles
+        // before its end): a unit claimed earlier would sit behind the whole current one
+        // while other SMs go idle, which unbalances launches of very uneven units.
+        mbar_arrive_expect_tx_w(&bars[C::B_CLC], 16);
+        clc_try_cancel_w(clc_resp, &bars[C::B_CLC]);
+        asked = true;
+        if (!mbar_wait_w(&bars[C::B_CLC], n_asked & 1, wc, 12)) break;
+        asked = false;
+        ++n_asked;
+        int cx, cy;
+        const bool taken = clc_taken(clc_resp, cx, cy);
+        ux = (taken && cx >= 0 && cx < (int)gridDim.x && cy >= 0 && cy < (int)gridDim.y) ? cx : -1;
+        uy = cy;
+      }
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+        // Let every copy already started land before the CTA can exit: the newest phase of
+        // each ring slot, the last Q pair and a pending launch-control answer.
+        volatile int no_abort = 0;
+        const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+        for (int j = k_issued > C::NS ? k_issued - C::NS : 0; j < k_issued; ++j)
+          mbar_wait(&bars[C::B_KF + j % C::NS], (j / C::NS) & 1, w2, 20);
+        for (int j = v_issued > C::NS ? v_issued - C::NS : 0; j < v_issued; ++j)
+          mbar_wait(&bars[C::B_VF + j % C::NS], (j / C::NS) & 1, w2, 21);
+        if (q_units > 0)
+          for (int t = 0; t < 2; ++t) mbar_wait(&bars[C::B_Q + t], (q_units - 1) & 1, w2, 22);
+        if (asked) mbar_wait(&bars[C::B_CLC], n_asked & 1, w2, 24);
+      }
+    }
+  } else if (warp == C::W_MMA) {
+    // ---------------------------------------------------------------- UMMA issuer
+    {
+      const uint64_t dq0 = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);
+      const uint64_t dk0 = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);
+      const uint64_t dv0 = sdesc(sbase + C::OFF_V, C::CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);
+      auto issue_s = [&](int t, int slot) {  // S_t = Q_t K^T (K in ring slot `slot`)
+        const uint64_t dq = desc_adv(dq0, (uint32_t)(t * C::TILE_BYTES));
+        const uint64_t dk = desc_adv(dk0, (uint32_t)(slot * C::TILE_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss_w(tmem + C::TMEM_S + t * 128, desc_adv(dq, kmajor_off<D>(kk)), desc_adv(dk, kmajor_off<D>(kk)),
+                  C::IDESC_S, kk > 0 ? 1u : 0u);
+        umma_commit_w(&bars[C::B_SF + t]);
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {  // O_t (+)= P_t V   (A = P from TMEM)
+        const uint64_t dv = desc_adv(dv0, (uint32_t)(slot * C::TILE_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          umma_ts_w(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * 128 + kk * 8,
+                  desc_adv(dv, (uint32_t)(kk * 16 * C::ROWB)), C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        umma_commit_w(&bars[C::B_O + t]);
+      };
+      int jg = 0;                // ring position of the unit's first key tile
+      int npf[2] = {0, 0};       // P tiles consumed per query tile (phases of p_full)
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        const int us = i % C::NU;
+        if (!(ok = mbar_wait_w(&bars[C::B_UF + us], (i / C::NU) & 1, wc, 13))) break;
+        const int2 u = units[us];
+        mbar_arrive_w(&bars[C::B_UE + us]);
+        if (u.x < 0) break;
+        const int q0 = ((int)gridDim.x - 1 - u.x) * 2 * C::BM;
+        const int n_kv0 = n_keys(q0), n_kv1 = n_keys(q0 + C::BM);
+        // the unit's first S tiles (their TMEM buffers were last read by the previous
+        // unit's P V, issued earlier by this thread)
+        ok = mbar_wait_w(&bars[C::B_Q], i & 1, wc, 2) && mbar_wait_w(&bars[C::B_KF + jg % C::NS], (jg / C::NS) & 1, wc, 3);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(0, jg % C::NS);
+        if (n_kv0 == 1) umma_commit_w(&bars[C::B_QE]);
+        if (!(ok = mbar_wait_w(&bars[C::B_Q + 1], i & 1, wc, 2))) break;
+        tc_fence_after();
+        issue_s(1, jg % C::NS);
+        if (n_kv1 == 1) umma_commit_w(&bars[C::B_QE + 1]);
+        umma_commit_w(&bars[C::B_KE + jg % C::NS]);
+        for (int j = 0; ok && j < n_kv1; ++j) {
+          const int pos = jg + j, s = pos % C::NS, s1 = (pos + 1) % C::NS;
+          if (!(ok = mbar_wait_w(&bars[C::B_VF + s], (pos / C::NS) & 1, wc, 5))) break;
+          const bool next_k = j + 1 < n_kv1;
+          if (next_k && !(ok = mbar_wait_w(&bars[C::B_KF + s1], ((pos + 1) / C::NS) & 1, wc, 3))) break;
+          if (j < n_kv0) {
+            if (!(ok = mbar_wait_w(&bars[C::B_PF], npf[0] & 1, wc, 4))) break;
+            ++npf[0];
+            tc_fence_after();
+            issue_pv(0, s, j > 0);
+            if (j + 1 < n_kv0) {
+              issue_s(0, s1);
+              if (j + 2 == n_kv0) umma_commit_w(&bars[C::B_QE]);
+            }
+          }
+          if (!(ok = mbar_wait_w(&bars[C::B_PF + 1], npf[1] & 1, wc, 4))) break;
+          ++npf[1];
+          tc_fence_after();
+          issue_pv(1, s, j > 0);
+          umma_commit_w(&bars[C::B_VE + s]);
+          if (next_k) {
+            issue_s(1, s1);
+            if (j + 2 == n_kv1) umma_commit_w(&bars[C::B_QE + 1]);
+            umma_commit_w(&bars[C::B_KE + s1]);
+          }
+        }
+        jg += n_kv1;
+      }
+      // Every MMA issued so far must complete before TMEM is freed.
+      umma_commit_w(&bars[C::B_DRAIN]);
+      volatile int no_abort = 0;
+      const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+      mbar_wait(&bars[C::B_DRAIN], 0, w2, 23);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax warpgroups
+    const int t = warp >> 2;   // which query tile of the pair
+    const int wq = warp & 3;   // TMEM lane quarter this warp may access
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t t_s = t_lane + C::TMEM_S + t * 128;
+    const uint32_t t_o = t_lane + C::TMEM_O + t * D;
+    const float sl2 = p.scale_log2;
+    int ns = 0;  // S tiles of this query tile processed over all units (phases of s_full, o_done)
+    bool ok = true;
+    for (int i = 0;; ++i) {
+      // the four warps agree to go on (a failed wait anywhere stops all of them together)
+      const int us = i % C::NU;
+      if (!named_bar_and(1 + t, 128, ok && warp_wait(&bars[C::B_UF + us], (i / C::NU) & 1, wc, 14))) break;
+      const int2 u = units[us];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
+      if (u.x < 0) break;
+      const int bh = u.y;
+      const int qt0 = ((int)gridDim.x - 1 - u.x) * 2 * C::BM + t * C::BM;
+      const int q_idx = qt0 + row;
+      const int n_kv_all = n_keys(qt0);
+      float m = -INFINITY, l = 0.f, lr = 0.f;
+      int n_kv = 0;
+      for (; n_kv < n_kv_all; ++n_kv, ++ns) {
+        if (!warp_wait(&bars[C::B_SF + t], ns & 1, wc, 6)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tmem_ld32(t_s + g * 32, s[g]);
+        tmem_wait_ld(s[0]);
+        reg_tie(s[1]);
+        reg_tie(s[2]);
+        reg_tie(s[3]);
+        const int ka = n_kv * C::BN;
+        if ((ka + C::BN > p.Nk) || (CAUSAL && (ka + C::BN - 1 > qt0))) {
+          int lim = p.Nk - 1 - ka;  // last visible column of this tile
+          if (CAUSAL) lim = min(lim, q_idx - ka);
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (g * 32 + c > lim) s[g][c] = __float_as_uint(-INFINITY);
+        }
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t* v = &s[k >> 1][(k & 1) * 16];
+          float a = fmax3(as_f(v[0]), as_f(v[1]), as_f(v[2]));
+#pragma unroll
+          for (int e = 3; e < 15; e += 2) a = fmax3(a, as_f(v[e]), as_f(v[e + 1]));
+          mx8[k] = fmaxf(a, as_f(v[15]));
+        }
+        const float mx2 =
+            fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * sl2;
+        float alpha = 1.f;
+        if (mx2 > m + kTau) {  // also taken on the first tile, where m = -inf
+          alpha = ex2(m - mx2);
+          m = mx2;
+        }
+        const uint64_t c2 = f2pack(sl2, sl2), nm2 = f2pack(-m, -m);
+        uint64_t l2[4];
+        float lra[4], lrb[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          l2[k] = 0ull;
+          lra[k] = lrb[k] = 0.f;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t pk[16];
+          softmax_weights32(s[g], c2, nm2, pk, l2, lra, lrb);
+          tmem_st16(t_s + g * 16, pk);
+        }
+        float la[8], lb[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          f2unpack(l2[k], la[2 * k], la[2 * k + 1]);
+          lb[2 * k] = lra[k];
+          lb[2 * k + 1] = lrb[k];
+        }
+        l = l * alpha + (((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7])));
+        lr = lr * alpha + (((lb[0] + lb[1]) + (lb[2] + lb[3])) + ((lb[4] + lb[5]) + (lb[6] + lb[7])));
+        // O holds P V up to the previous key tile (S of this one was issued after it)
+        if (n_kv > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int g = 0; g < D / 16; ++g) {
+            uint32_t o[16];
+            tmem_ld16(t_o + g * 16, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(as_f(o[c]) * alpha);
+            tmem_st16(t_o + g * 16, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[C::B_PF + t]);
+      }
+      // epilogue: O through the staging tile, which tile 0 takes after tile 1's store of the
+      // previous unit has read it and tile 1 after tile 0's store of this unit
+      bool go = ok && warp_wait(&bars[C::B_O + t], (ns - 1) & 1, wc, 8);
+      if (t == 1) go = warp_wait(&bars[C::B_STG], i & 1, wc, 9) && go;
+      else if (i >= 1) go = warp_wait(&bars[C::B_STG1], (i - 1) & 1, wc, 9) && go;
+      go = named_bar_and(1 + t, 128, go);
+      if (go) {
+        tc_fence_after();
+        stage_o_row<D>(smem + C::OFF_STG, row, t_o, 1.f / lr);
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1 + t, 128);
+      if (row == 0) {
+        if (go && qt0 < p.Nq) {
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_store_3d(&tm_o, smem + C::OFF_STG + c * C::CHUNK_BYTES, c * C::CHUNK, qt0, bh);
+          bulk_commit_group();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(&bars[t == 0 ? C::B_STG : C::B_STG1]);  // the other tile may take the staging tile
+      }
+      if (go && q_idx < p.Nq) p.lse[(size_t)bh * p.Nq + q_idx] = (m + log2f(l)) * 0.69314718055994530942f;
+      ok = ok && go;
     }
   }
 
@@ -638,7 +1085,8 @@ struct SeqCfg {
 template <int D, bool CAUSAL, bool FOLD>
 __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
     fwd_seq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const FwdParams p) {
   using C = Cfg<D>;
   using S = SeqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -697,34 +1145,34 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
 
   if (warp == S::W_PRODUCER) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0 && N > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+    if (N > 0) {
+      if (lane == 0) tma_prefetch_desc(&tm_q);
+      if (lane == 0) tma_prefetch_desc(&tm_k);
+      if (lane == 0) tma_prefetch_desc(&tm_v);
       for (int t = 0; t < 2; ++t) {
         if ((t == 0 ? n0 : n1) == 0) continue;
-        mbar_arrive_expect_tx(&bars[C::B_Q + t], C::TILE_BYTES);
+        mbar_arrive_expect_tx_w(&bars[C::B_Q + t], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
+          tma_load_3d_w(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
                       c * C::CHUNK, qa[t], bh);
       }
       int k_issued = 0, v_issued = 0;  // steps whose K and V copies were started
       for (int g = 0; g < N; ++g) {
         const int s = g % C::NS, kt = kt_of(g);
-        if (g >= C::NS && !mbar_wait(&bars[C::B_KE + s], ((g / C::NS) - 1) & 1, wc, 1)) break;
-        mbar_arrive_expect_tx(&bars[C::B_KF + s], C::TILE_BYTES);
+        if (g >= C::NS && !mbar_wait_w(&bars[C::B_KE + s], ((g / C::NS) - 1) & 1, wc, 1)) break;
+        mbar_arrive_expect_tx_w(&bars[C::B_KF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
+          tma_load_3d_w(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
                       c * C::CHUNK, kt * C::BN, bh);
         k_issued = g + 1;
-        if (g >= C::NS && !mbar_wait(&bars[C::B_VE + s], ((g / C::NS) - 1) & 1, wc, 1)) break;
-        mbar_arrive_expect_tx(&bars[C::B_VF + s], C::TILE_BYTES);
+        if (g >= C::NS && !mbar_wait_w(&bars[C::B_VE + s], ((g / C::NS) - 1) & 1, wc, 1)) break;
+        mbar_arrive_expect_tx_w(&bars[C::B_VF + s], C::TILE_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
+          tma_load_3d_w(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
                       c * C::CHUNK, kt * C::BN, bh);
         v_issued = g + 1;
       }
-      if (*abort_flag) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         // Let every copy already started land before the CTA can exit: the last NS of
         // each ring, one per slot, so that each wait is on its slot's newest phase.
         volatile int no_abort = 0;
@@ -739,7 +1187,7 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
     }
   } else if (warp == S::W_MMA) {
     // ---------------------------------------------------------------- UMMA issuer
-    if (lane == 0 && N > 0) {
+    if (N > 0) {
       const uint64_t dq0 = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);
       const uint64_t dk0 = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);
       const uint64_t dv0 = sdesc(sbase + C::OFF_V, C::CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);
@@ -749,10 +1197,10 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
         const uint64_t dk = desc_adv(dk0, (uint32_t)(s * C::TILE_BYTES));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + C::TMEM_S + (uint32_t)((g & 1) * 128), desc_adv(dq, kmajor_off<D>(kk)),
+          umma_ss_w(tmem + C::TMEM_S + (uint32_t)((g & 1) * 128), desc_adv(dq, kmajor_off<D>(kk)),
                   desc_adv(dk, kmajor_off<D>(kk)), C::IDESC_S, kk > 0 ? 1u : 0u);
-        umma_commit(&bars[C::B_SF + (g & 1)]);
-        umma_commit(&bars[C::B_KE + s]);
+        umma_commit_w(&bars[C::B_SF + (g & 1)]);
+        umma_commit_w(&bars[C::B_KE + s]);
       };
       auto issue_pv = [&](int g) {  // O_t (+)= P(g) V_kt, P read from buffer g & 1
         const int s = g % C::NS;
@@ -761,20 +1209,20 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
         const bool acc = kt_of(g) > 0;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts(o, tmem + C::TMEM_S + (uint32_t)((g & 1) * 128) + kk * 8,
+          umma_ts_w(o, tmem + C::TMEM_S + (uint32_t)((g & 1) * 128) + kk * 8,
                   desc_adv(dv, (uint32_t)(kk * 16 * C::ROWB)), C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
-        umma_commit(&bars[C::B_O + (g & 1)]);
-        umma_commit(&bars[C::B_VE + s]);
+        umma_commit_w(&bars[C::B_O + (g & 1)]);
+        umma_commit_w(&bars[C::B_VE + s]);
       };
       // S(g) needs its Q tile (waited once per tile) and K in ring slot g % NS
       bool q_ready[2] = {false, false};
       auto s_ready = [&](int g) -> bool {
         const int t = tile_of(g);
         if (!q_ready[t]) {
-          if (!mbar_wait(&bars[C::B_Q + t], 0, wc, 2)) return false;
+          if (!mbar_wait_w(&bars[C::B_Q + t], 0, wc, 2)) return false;
           q_ready[t] = true;
         }
-        return mbar_wait(&bars[C::B_KF + g % C::NS], (g / C::NS) & 1, wc, 3);
+        return mbar_wait_w(&bars[C::B_KF + g % C::NS], (g / C::NS) & 1, wc, 3);
       };
       bool ok = s_ready(0);
       if (ok) {
@@ -787,8 +1235,8 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
       }
       for (int g = 0; ok && g < N; ++g) {
         // P(g) V: P from the softmax, V in slot g % NS
-        if (!(ok = mbar_wait(&bars[C::B_PF + (g & 1)], (g >> 1) & 1, wc, 4))) break;
-        if (!(ok = mbar_wait(&bars[C::B_VF + g % C::NS], (g / C::NS) & 1, wc, 5))) break;
+        if (!(ok = mbar_wait_w(&bars[C::B_PF + (g & 1)], (g >> 1) & 1, wc, 4))) break;
+        if (!(ok = mbar_wait_w(&bars[C::B_VF + g % C::NS], (g / C::NS) & 1, wc, 5))) break;
         tc_fence_after();
         issue_pv(g);
         // S(g+2) over buffer g & 1, after P(g) V has read it (in-order UMMA)
@@ -798,7 +1246,7 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
           issue_s(g + 2);
         }
       }
-      umma_commit(&bars[C::B_DRAIN]);
+      umma_commit_w(&bars[C::B_DRAIN]);
       volatile int no_abort = 0;
       const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
       mbar_wait(&bars[C::B_DRAIN], 0, w2, 23);
@@ -912,36 +1360,29 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
     st_m[n1 > 0 ? 1 : 0] = m;
     st_l[n1 > 0 ? 1 : 0] = l;
     st_lr[n1 > 0 ? 1 : 0] = lr;
-    // epilogue: the last P V done means every earlier one is (in-order UMMA)
-    if (ok && N > 0 && warp_wait(&bars[C::B_O + ((N - 1) & 1)], ((N - 1) >> 1) & 1, wc, 8)) {
-      tc_fence_after();
-      for (int t = 0; t < 2; ++t) {
-        if ((t == 0 ? n0 : n1) == 0) continue;
-        const int q_idx = qa[t] + row;
-        const float inv_l = 1.f / st_lr[t];
-        const uint32_t t_o = t_lane + C::TMEM_O + (uint32_t)(t * D);
-        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.Nq + q_idx) * D;
-#pragma unroll
-        for (int gg = 0; gg < D / 16; ++gg) {
-          uint32_t o[16];
-          tmem_ld16(t_o + gg * 16, o);
-          tmem_wait_ld(o);
-          uint4 w0, w1;
-          w0.x = pack_bf16(as_f(o[0]) * inv_l, as_f(o[1]) * inv_l);
-          w0.y = pack_bf16(as_f(o[2]) * inv_l, as_f(o[3]) * inv_l);
-          w0.z = pack_bf16(as_f(o[4]) * inv_l, as_f(o[5]) * inv_l);
-          w0.w = pack_bf16(as_f(o[6]) * inv_l, as_f(o[7]) * inv_l);
-          w1.x = pack_bf16(as_f(o[8]) * inv_l, as_f(o[9]) * inv_l);
-          w1.y = pack_bf16(as_f(o[10]) * inv_l, as_f(o[11]) * inv_l);
-          w1.z = pack_bf16(as_f(o[12]) * inv_l, as_f(o[13]) * inv_l);
-          w1.w = pack_bf16(as_f(o[14]) * inv_l, as_f(o[15]) * inv_l);
-          if (q_idx < p.Nq) {
-            reinterpret_cast<uint4*>(orow + gg * 16)[0] = w0;
-            reinterpret_cast<uint4*>(orow + gg * 16)[1] = w1;
-          }
-        }
-        if (q_idx < p.Nq) p.lse[(size_t)bh * p.Nq + q_idx] = (st_m[t] + log2f(st_l[t])) * 0.69314718055994530942f;
+    // epilogue: the last P V done means every earlier one is (in-order UMMA).  Each tile's O
+    // goes through the staging tile and one bulk tensor store per column chunk; the issuing
+    // thread waits until the store has read the staging tile before the next tile's rows
+    // are written into it.  The four warps agree on the wait's outcome first.
+    const bool go = named_bar_and(
+        1, 128, ok && N > 0 && warp_wait(&bars[C::B_O + ((N - 1) & 1)], ((N - 1) >> 1) & 1, wc, 8));
+    if (go) tc_fence_after();
+    for (int t = 0; t < 2; ++t) {
+      if ((t == 0 ? n0 : n1) == 0) continue;
+      const int q_idx = qa[t] + row;
+      if (go) {
+        stage_o_row<D>(smem + C::OFF_STG, row, t_lane + C::TMEM_O + (uint32_t)(t * D), 1.f / st_lr[t]);
+        fence_proxy_async_smem();
       }
+      named_bar_sync(1, 128);
+      if (go && row == 0) {
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_store_3d(&tm_o, smem + C::OFF_STG + c * C::CHUNK_BYTES, c * C::CHUNK, qa[t], bh);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+      named_bar_sync(1, 128);
+      if (go && q_idx < p.Nq) p.lse[(size_t)bh * p.Nq + q_idx] = (st_m[t] + log2f(st_l[t])) * 0.69314718055994530942f;
     }
   }
 
@@ -954,20 +1395,32 @@ __global__ void __launch_bounds__(SeqCfg<D>::THREADS, 1)
 }
 
 template <int D, bool CAUSAL, bool FOLD>
-cudaError_t launch_seq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                         int BH, cudaStream_t st) {
+cudaError_t launch_seq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                         const FwdParams& p, int BH, cudaStream_t st) {
   using C = Cfg<D>;
   auto kern = fwd_seq_kernel<D, CAUSAL, FOLD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH);
-  kern<<<grid, SeqCfg<D>::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, p);
+  kern<<<grid, SeqCfg<D>::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                             const FwdParams& p, int BH, cudaStream_t st) {
+  using C = Cfg<D>;
+  auto kern = fwd_persist_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH);
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
 template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
-cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
-                     int BH, cudaStream_t st) {
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                     const FwdParams& p, int BH, cudaStream_t st) {
   using C = Cfg<D>;
   auto kern = fwd_kernel<D, CAUSAL, VARLEN, LOCAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
@@ -975,7 +1428,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   const int n_pairs = (p.n_q_tiles + 1) / 2;
   const int gx = (LOCAL && p.n_gp > 0) ? p.n_gp * p.n_split + (n_pairs - p.n_gp) : n_pairs;
   dim3 grid((unsigned)gx, (unsigned)BH);
-  kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, p);
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -999,18 +1452,21 @@ __global__ void wait_probe_kernel(unsigned long long limit_ns, unsigned* status)
 }  // namespace fwd
 
 cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdParams& p, int BH, cudaStream_t st) {
-#define TA11_FWD_CASE(DD)                                                                          \
-  case DD:                                                                                         \
-    if (p.local)                                                                                   \
-      return causal ? fwd::launch_t<DD, true, false, true>(tq, tk, tv, p, BH, st)                  \
-                    : fwd::launch_t<DD, false, false, true>(tq, tk, tv, p, BH, st);                \
-    if (p.va.cu_q)                                                                                 \
-      return causal ? fwd::launch_t<DD, true, true>(tq, tk, tv, p, BH, st)                         \
-                    : fwd::launch_t<DD, false, true>(tq, tk, tv, p, BH, st);                       \
-    if (causal && p.fold) return fwd::launch_seq_t<DD, true, true>(tq, tk, tv, p, BH, st);         \
-    return causal ? fwd::launch_t<DD, true, false>(tq, tk, tv, p, BH, st)                          \
-                  : fwd::launch_t<DD, false, false>(tq, tk, tv, p, BH, st);
+                       const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t st) {
+#define TA11_FWD_CASE(DD)                                                                        \
+  case DD:                                                                                       \
+    if (p.local)                                                                                 \
+      return causal ? fwd::launch_t<DD, true, false, true>(tq, tk, tv, to, p, BH, st)            \
+                    : fwd::launch_t<DD, false, false, true>(tq, tk, tv, to, p, BH, st);          \
+    if (p.va.cu_q)                                                                               \
+      return causal ? fwd::launch_t<DD, true, true>(tq, tk, tv, to, p, BH, st)                   \
+                    : fwd::launch_t<DD, false, true>(tq, tk, tv, to, p, BH, st);                 \
+    if (causal && p.fold) return fwd::launch_seq_t<DD, true, true>(tq, tk, tv, to, p, BH, st);   \
+    if (p.persist)                                                                               \
+      return causal ? fwd::launch_persist_t<DD, true>(tq, tk, tv, to, p, BH, st)                 \
+                    : fwd::launch_persist_t<DD, false>(tq, tk, tv, to, p, BH, st);               \
+    return causal ? fwd::launch_t<DD, true, false>(tq, tk, tv, to, p, BH, st)                    \
+                  : fwd::launch_t<DD, false, false>(tq, tk, tv, to, p, BH, st);
   switch (D) {
     TA11_FWD_CASE(16)
     TA11_FWD_CASE(32)
