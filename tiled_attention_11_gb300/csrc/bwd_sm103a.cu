@@ -10,7 +10,7 @@
 //            dq_accum = 0.                                          (HBM-bound)
 //   bwd      one CTA per (batch*head, 128-key tile); K_j, V_j stay in shared memory,
 //            dK_j, dV_j accumulate in TMEM; 64-query tiles Q_i, dO_i stream through
-//            a TMA ring (causal: starting at the diagonal).  Per query tile, all on
+//            a 3-stage TMA ring (causal: starting at the diagonal).  Per query tile, all on
 //            tcgen05 (keys on the M=128 axis):
 //              S^T  = K Q_i^T            -> TMEM   P^T = 2^(S^T c - lse2)  (compute WGs)
 //              dP^T = V dO_i^T           -> TMEM   dS^T = P^T o (dP^T - Dlt) -> shared memory
@@ -18,8 +18,8 @@
 //              dK  += dS^T Q_i   (A = dS^T from shared memory)
 //              dQ_i^T = K^T dS^T (A = K^T kept in TMEM, B = the same dS^T tile)
 //                                   -> TMEM, into the S^T buffer dV has just consumed
-//            Two threads issue the UMMAs: one the score GEMMs S^T, dP^T (which need only
-//            loaded tiles and free TMEM), the other the gradient GEMMs dV, dK, dQ^T
+//            Two warps issue the UMMAs: one the score GEMMs S^T, dP^T (which need only
+//            loaded tiles and free TMEM), the other the gradient GEMMs dV, dQ^T, dK
 //            (which wait for the compute warps).  The tensor core keeps almost no queue,
 //            so a single issuing thread lets it run dry at every wait (~200 cycles each,
 //            measured); with two, one feeds it while the other waits.  S^T / P^T is
@@ -47,7 +47,7 @@ struct Cfg {
   static constexpr int KV_TILE = BN * D * 2;
   static constexpr int Q_CHUNK_BYTES = BM * ROWB;
   static constexpr int Q_TILE = BM * D * 2;
-  static constexpr int NS = 2;
+  static constexpr int NS = 3;                         // Q / dO / lse2 / Dlt ring depth
   static constexpr int DS_BYTES = BN * BM * 2;         // dS^T tile, bf16, 128-byte rows
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
@@ -329,20 +329,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (!(ok = mbar_wait_w(&bars[C::B_DSF + b], (it >> 1) & 1, wc, 36))) break;
         if (it == 0 && !(ok = mbar_wait_w(&bars[C::B_KT], 0, wc, 47))) break;
         tc_fence_after();
-        const uint64_t dsa = desc_adv(dSa, (uint32_t)(b * C::DS_BYTES));
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          umma_ss_w(tmem + C::T_DK, desc_adv(dsa, (uint32_t)(kk * 32)), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_w(&bars[C::B_QE + s]);  // dK was the stage's last reader
-        // dQ^T(it) into buffer b, which dV(it) (issued above: in-order) has finished reading
+        // dQ^T(it) first, into buffer b, which dV(it) (issued above: in-order) has finished
+        // reading: the dQ warpgroup's drain of it gates S^T(it+2), so it starts as early as it can
         const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           umma_ts_w(tmem + C::T_S + (uint32_t)(b * 64), tmem + C::T_KT + kk * 8, desc_adv(ds, (uint32_t)(kk * 16 * 128)),
-                  C::IDESC_DQ, kk > 0 ? 1u : 0u);
-        umma_commit_w(&bars[C::B_DQF + b]);
+                    C::IDESC_DQ, kk > 0 ? 1u : 0u);
         umma_commit_w(&bars[C::B_DQR + b]);
+        const uint64_t dsa = desc_adv(dSa, (uint32_t)(b * C::DS_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          umma_ss_w(tmem + C::T_DK, desc_adv(dsa, (uint32_t)(kk * 32)), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_w(&bars[C::B_QE + s]);   // dK was the stage's last reader
+        umma_commit_w(&bars[C::B_DQF + b]);  // dQ^T and dK have both read dS^T buffer b
       }
       umma_commit_w(&bars[C::B_DRAIN + 1]);
       volatile int no_abort = 0;
