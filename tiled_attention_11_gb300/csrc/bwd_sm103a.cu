@@ -25,9 +25,10 @@
 //            measured); with two, one feeds it while the other waits.  S^T / P^T is
 //            double-buffered in TMEM so S(i+1) need not wait for dV(i); dQ_i^T reuses
 //            step i's buffer, and S(i+2) waits until the dQ warpgroup has moved dQ_i^T
-//            from TMEM to shared memory and added it into dq_accum (one TMA bulk
-//            reduce-add per tile).  Shared-memory bandwidth is the next limit (~290 KB
-//            per step against 128 B/cycle), which is why K^T is kept in TMEM.
+//            from TMEM to shared memory and added it into dq_accum (TMA bulk reduce-adds
+//            of two 32-query halves, so the reduce reading one half overlaps the writes of
+//            the other).  Shared-memory bandwidth is the limit (~270 KB per step against
+//            128 B/cycle), which is why K^T is kept in TMEM.
 //   convert  dq = bf16(dq_accum * scale).
 #include "fa_kernels.h"
 #include "ptx_sm103a.cuh"
@@ -521,21 +522,24 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       reg_tie(v1);
       tc_fence_before();
       mbar_arrive(&bars[C::B_DQE + b]);
-      // the previous bulk reduce must have finished reading the staging buffer
-      if (threadIdx.x == 0) bulk_wait_read_all();
-      named_bar_sync(1, 128);
-      if (d < D) {
+      // two halves of 32 queries: a half is rewritten once the reduce that last read it is
+      // done reading (bulk groups complete in order), so one half's read overlaps the other
+      // half's writes
+      float* gdst = p.dq_accum + ((size_t)wrow0 + (size_t)qs.at(it) * C::BM) * D;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) stg[c * D + d] = as_f(v0[c]);
+      for (int h = 0; h < 2; ++h) {
+        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        named_bar_sync(1, 128);
+        if (d < D) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) stg[(32 + c) * D + d] = as_f(v1[c]);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 0) {
-        float* gdst = p.dq_accum + ((size_t)wrow0 + (size_t)qs.at(it) * C::BM) * D;
-        bulk_reduce_add_f32(gdst, stg, C::STG_BYTES);
-        bulk_commit_group();
+          for (int c = 0; c < 32; ++c) stg[(h * 32 + c) * D + d] = as_f(h == 0 ? v0[c] : v1[c]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 0) {
+          bulk_reduce_add_f32(gdst + h * 32 * D, stg + h * 32 * D, C::STG_BYTES / 2);
+          bulk_commit_group();
+        }
       }
     }
     if (threadIdx.x == 0) bulk_wait_all();
