@@ -23,15 +23,29 @@ __device__ __forceinline__ float absmax8(const uint4 w, float m) {
   return m;
 }
 
+// Loads of 16 bytes, four independent ones in flight per thread (enough bytes in flight per
+// SM to cover the HBM latency); read-only path.
+__device__ __forceinline__ uint4 ld16(const uint4* p) { return __ldg(p); }
+
 __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restrict__ x, long long n,
                                                    unsigned* __restrict__ amax_bits) {
-  float m = 0.f;
+  float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
   const long long n8 = n / 8;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const uint4* x8 = reinterpret_cast<const uint4*>(x);
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) m = absmax8(x8[i], m);
-  for (long long i = n8 * 8 + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-    m = fmaxf(m, fabsf(__bfloat162float(x[i])));
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    const uint4 a = ld16(x8 + i), b = ld16(x8 + i + stride), c = ld16(x8 + i + 2 * stride),
+                d = ld16(x8 + i + 3 * stride);
+    m0 = absmax8(a, m0);
+    m1 = absmax8(b, m1);
+    m2 = absmax8(c, m2);
+    m3 = absmax8(d, m3);
+  }
+  for (; i < n8; i += stride) m0 = absmax8(ld16(x8 + i), m0);
+  for (long long j = n8 * 8 + (long long)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride)
+    m0 = fmaxf(m0, fabsf(__bfloat162float(x[j])));
+  float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   __shared__ float wm[8];
@@ -68,10 +82,19 @@ __global__ void __launch_bounds__(256) quant_kernel(const __nv_bfloat16* __restr
   const long long stride = (long long)gridDim.x * blockDim.x;
   const uint4* x8 = reinterpret_cast<const uint4*>(x);
   uint2* c8 = reinterpret_cast<uint2*>(codes);
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) c8[i] = quant8(x8[i], mult);
-  for (long long i = n8 * 8 + (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-    const uint32_t w = pack_e4m3x4(__fmul_rn(__bfloat162float(x[i]), mult), 0.f, 0.f, 0.f);
-    codes[i] = (uint8_t)(w & 0xffu);
+  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    const uint4 a = ld16(x8 + i), b = ld16(x8 + i + stride), c = ld16(x8 + i + 2 * stride),
+                d = ld16(x8 + i + 3 * stride);
+    c8[i] = quant8(a, mult);
+    c8[i + stride] = quant8(b, mult);
+    c8[i + 2 * stride] = quant8(c, mult);
+    c8[i + 3 * stride] = quant8(d, mult);
+  }
+  for (; i < n8; i += stride) c8[i] = quant8(ld16(x8 + i), mult);
+  for (long long j = n8 * 8 + (long long)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride) {
+    const uint32_t w = pack_e4m3x4(__fmul_rn(__bfloat162float(x[j]), mult), 0.f, 0.f, 0.f);
+    codes[j] = (uint8_t)(w & 0xffu);
   }
 }
 
@@ -81,17 +104,19 @@ __global__ void __launch_bounds__(256) quant_t_kernel(const __nv_bfloat16* __res
                                                       const float* __restrict__ amax, uint8_t* __restrict__ codes_t,
                                                       float* __restrict__ descale) {
   constexpr int KEYS = 64;
-  __shared__ __align__(16) uint8_t tile[D][KEYS + 16];  // [d][key]; rows padded to spread banks
+  __shared__ __align__(16) uint8_t tile[D][KEYS];  // [d][key]
   const float a = *amax;
   const float mult = multiplier(a);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *descale = a > 0.f ? a / 448.f : 1.f;
   const int bh = blockIdx.y;
   const int k0 = blockIdx.x * KEYS;
   const __nv_bfloat16* xs = x + ((size_t)bh * N + k0) * D;
+  // keys fastest: a warp stores 32 consecutive bytes of a tile row (no bank conflicts); the
+  // 16-byte loads of one key row are spread over warps and meet in L1
   for (int e = threadIdx.x; e < KEYS * (D / 8); e += blockDim.x) {
-    const int key = e / (D / 8), part = e % (D / 8);
+    const int key = e % KEYS, part = e / KEYS;
     uint2 c = make_uint2(0u, 0u);  // keys past N quantise as zero
-    if (k0 + key < N) c = quant8(reinterpret_cast<const uint4*>(xs + (size_t)key * D)[part], mult);
+    if (k0 + key < N) c = quant8(ld16(reinterpret_cast<const uint4*>(xs + (size_t)key * D) + part), mult);
     const uint32_t w[2] = {c.x, c.y};
 #pragma unroll
     for (int i = 0; i < 8; ++i) tile[part * 8 + i][key] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
