@@ -276,6 +276,10 @@ def run_ours(args):
     if rc != 0:
         raise RuntimeError(f"device status {rc} (wait site {site}) after the timed region")
 
+    if args.no_e2e:  # (profiling runs: only the device-resident steps)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     # ---------------- end to end through fa_step_host: pinned host inputs -> device, fwd + bwd,
     # every output -> pinned host.  Several steps are in flight on their own streams (own
     # device buffer and host output set each), so copies overlap kernels and each other
@@ -680,6 +684,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--e2e-lanes", type=int, default=3, help="steps in flight in the end-to-end measurement")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="stop after the device-resident steps, printing nothing (for profiler captures)")
     ap.add_argument("--table", action="store_true", help="time every workload, print a markdown table")
     ap.add_argument("--varlen-only", action="store_true", help="with --table: only the packed variable-length row")
     ap.add_argument("--window-only", action="store_true", help="with --table: only the local-window rows")

@@ -119,6 +119,16 @@ void fa_set_wait_limit_ns(unsigned long long ns);
 int fa_set_fwd_persistent(int on);
 
 /*
+ * The same choice for fa_bwd's main kernel (dense layout, no window mask, more
+ * (key tile, head) units than the SMs hold at once, every key tile with at least one
+ * query step, and D < 128 or Nq <= 8192, where it measured faster): 1 (default) persistent CTAs whose pipelines run on across units (the next
+ * unit's K / V loads and first score GEMMs overlap the current unit's dK / dV epilogue),
+ * 0 one CTA per unit.  Both compute every output bitwise the same.  Process-wide;
+ * returns the previous value.
+ */
+int fa_set_bwd_persistent(int on);
+
+/*
  * Self-test hook for the timeout path: launches a one-warp kernel that waits,
  * with the given limit, on a barrier nothing ever arrives on; it then records
  * FA_ERR_TIMEOUT in the status word and exits normally (no trap, no hang).

@@ -356,6 +356,47 @@ def test_persistent_forward_equals_one_cta_per_unit(p):
         assert_lse(f"{p.name()} b{b}h{h} L", f64(l2[b, h]), rl)
 
 
+# more (key tile, head) units than SMs: the backward's main kernel runs persistent CTAs
+# by default; (4, 16, 1000, 1500, 16, causal) has key tiles past the last query, which
+# keep one CTA per unit
+PERSIST_BWD_CASES = [I.Problem(2, 16, 2048, 2048, 128, True), I.Problem(2, 16, 2048, 2048, 64, False),
+                     I.Problem(4, 16, 1100, 1100, 32, True), I.Problem(4, 16, 1000, 1500, 16, True),
+                     I.Problem(4, 16, 1500, 1000, 128, False), I.Problem(8, 32, 300, 300, 64, True),
+                     I.Problem(1, 160, 130, 130, 128, True)]
+
+
+@pytest.mark.parametrize("p", PERSIST_BWD_CASES, ids=[p.name() for p in PERSIST_BWD_CASES])
+def test_persistent_backward_equals_one_cta_per_unit(p):
+    # dK and dV of a key tile come from one CTA in either schedule: bitwise equal.  dQ adds
+    # the key tiles' parts in arrival order in both: equal up to that order.  Both match the
+    # oracle on sampled heads.
+    assert p.B * p.H * ((p.Nk + 127) // 128) > 152
+    q, k, v, do = I.draw(p, 13)
+    dev = torch.device("cuda")
+    qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
+    _lib.fa_device_status(reset=True)
+    o, lse = _lib.forward(qg, kg, vg, p.causal, p.scale)
+    prev = _lib.fa_set_bwd_persistent(False)
+    try:
+        dq1, dk1, dv1 = _lib.backward(qg, kg, vg, o, lse, dog, p.causal, p.scale)
+        _lib.fa_set_bwd_persistent(True)
+        dq2, dk2, dv2 = _lib.backward(qg, kg, vg, o, lse, dog, p.causal, p.scale)
+        torch.cuda.synchronize()
+    finally:
+        _lib.fa_set_bwd_persistent(prev)
+    assert _lib.fa_device_status()[0] == _lib.FA_OK
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    err = (dq1.float() - dq2.float()).abs().max().item()
+    assert err <= 1e-2 * dq1.float().abs().max().item(), err
+    for (b, h) in ((0, 0), (p.B - 1, p.H - 1)):
+        qd, kd, vd, dod = (I.as_f64(t[b, h]) for t in (q, k, v, do))
+        rdq, rdk, rdv = oracle.backward_head(qd, kd, vd, dod, p.scale, p.causal)
+        tag = f"{p.name()} b{b}h{h}"
+        assert_close(tag + " dQ", f64(dq2[b, h]), rdq)
+        assert_close(tag + " dK", f64(dk2[b, h]), rdk)
+        assert_close(tag + " dV", f64(dv2[b, h]), rdv)
+
+
 def test_tensors_beyond_2_31_elements():
     # 65535 heads (the grid's maximum) x 260 rows x D = 128: 2.18e9 elements per tensor, so
     # the last heads live past element 2^31 and every offset must be 64-bit.  Inputs are drawn

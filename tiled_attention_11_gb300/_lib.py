@@ -28,7 +28,7 @@ FA_ERR_TIMEOUT = 7
 FA_ERR_SCRATCH_LIMIT = 8
 
 EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_device_status",
-            "fa_set_wait_limit_ns", "fa_set_fwd_persistent", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
+            "fa_set_wait_limit_ns", "fa_set_fwd_persistent", "fa_set_bwd_persistent", "fa_wait_probe", "fa_set_bwd_main_events", "fa_bwd_noalloc",
             "fa_graph_create", "fa_graph_launch", "fa_graph_destroy", "fa_fwd_varlen", "fa_bwd_varlen",
             "fa_bwd_varlen_workspace_size", "fa_fwd_window", "fa_bwd_window", "fa_fwd_window_workspace_size", "fa_bwd_window_workspace_size",
             "fa_quantize_e4m3",
@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
     L.fa_set_wait_limit_ns.restype = None
     L.fa_set_fwd_persistent.argtypes = [i]
     L.fa_set_fwd_persistent.restype = i
+    L.fa_set_bwd_persistent.argtypes = [i]
+    L.fa_set_bwd_persistent.restype = i
     L.fa_wait_probe.argtypes = [ctypes.c_ulonglong, vp]
     L.fa_wait_probe.restype = i
     L.fa_set_bwd_main_events.argtypes = [vp, vp]
@@ -248,6 +250,12 @@ def fa_set_fwd_persistent(on: bool) -> bool:
     """C ``fa_set_fwd_persistent``: the dense forward's schedule beyond one wave of CTAs
     (persistent CTAs by default); returns the previous setting."""
     return bool(lib().fa_set_fwd_persistent(int(bool(on))))
+
+
+def fa_set_bwd_persistent(on: bool) -> bool:
+    """C ``fa_set_bwd_persistent``: the dense backward main kernel's schedule beyond one
+    wave of CTAs (persistent CTAs by default); returns the previous setting."""
+    return bool(lib().fa_set_bwd_persistent(int(bool(on))))
 
 
 def fa_wait_probe(limit_ns: int, stream=None) -> None:

@@ -78,8 +78,20 @@ struct Cfg {
   static constexpr int B_KT = 14 + 2 * NS;   // K^T written into TMEM
   static constexpr int B_DPE = 15 + 2 * NS;  // dP^T loaded by the compute warps (its TMEM columns free)
   static constexpr int B_DRAIN = 16 + 2 * NS;  // [2] one per issuing thread
-  static constexpr int NBAR = 18 + 2 * NS;
-  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
+  // persistent kernel only: K / V smem free (a unit's last S^T, dP^T done); K^T TMEM free (its
+  // last dQ^T done); dK, dV drained from TMEM by the epilogue; work-unit ring full / empty;
+  // the answer of a launch-control request landed
+  static constexpr int B_KVE = 18 + 2 * NS;
+  static constexpr int B_KTE = 19 + 2 * NS;
+  static constexpr int B_ACCE = 20 + 2 * NS;
+  static constexpr int NU = 4;               // work-unit ring slots
+  static constexpr int B_UF = 21 + 2 * NS;
+  static constexpr int B_UE = B_UF + NU;
+  static constexpr int B_CLC = B_UE + NU;
+  static constexpr int NBAR = B_CLC + 1;
+  static constexpr int OFF_CLC = OFF_BAR + ((NBAR * 8 + 16 + 15) / 16) * 16;  // 16-byte launch-control answer
+  static constexpr int OFF_UNITS = OFF_CLC + 16;                               // NU x int2 work units
+  static constexpr int SMEM_USED = OFF_UNITS + NU * 8;
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
   // warps 0-3: dQ warpgroup, 4-11: two compute warpgroups, 12: TMA producer,
   // 13: UMMA issuer for S^T, dP^T (and TMEM allocator), 14: UMMA issuer for dV, dK, dQ^T
@@ -554,6 +566,446 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 }
 
 // ------------------------------------------------------------------------------------
+// Persistent form of bwd_kernel for the dense layout with the plain masks.  The grid still
+// has one CTA per (128-key tile, batch*head) in the same order, but a running CTA takes
+// over the next CTA that has not started (cluster launch control) instead of exiting, and
+// its pipelines run on across units: K / V of the next unit are loaded once the current
+// unit's last S^T and dP^T and its K^T build have read the old ones, K^T is rebuilt in TMEM once the last
+// dQ^T has read the old one, and the next unit's first score GEMMs run while the compute
+// warps are still in the current unit's epilogue (its dK / dV accumulate from zero once
+// that epilogue has read the old ones out of TMEM).  Step-indexed barrier phases count
+// steps over all units (g = the unit's first global step + it); unit-indexed ones count
+// units.  Roles, arithmetic and per-step order are those of bwd_kernel.
+// ------------------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
+    bwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  void* clc_resp = smem + C::OFF_CLC;
+  int2* units = reinterpret_cast<int2*>(smem + C::OFF_UNITS);
+
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+  const int n_qt = (p.Nq + C::BM - 1) / C::BM;
+  // query steps of key tile kt: causal ones start at the diagonal
+  // (the host launches this kernel only when every key tile has at least one step)
+  auto first_step = [&](int kt) { return CAUSAL ? (kt * C::BN) / C::BM : 0; };
+  auto n_steps = [&](int kt) { return n_qt - first_step(kt); };
+  const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[C::B_KV], 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bars[C::B_QF + s], 1);
+      mbar_init(&bars[C::B_QE + s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars[C::B_SF + b], 1);
+      mbar_init(&bars[C::B_PF + b], 256);
+      mbar_init(&bars[C::B_DSF + b], 256);
+      mbar_init(&bars[C::B_DQF + b], 1);
+      mbar_init(&bars[C::B_DQR + b], 1);
+      mbar_init(&bars[C::B_DQE + b], 128);
+      mbar_init(&bars[C::B_DRAIN + b], 1);
+    }
+    mbar_init(&bars[C::B_DPF], 1);
+    mbar_init(&bars[C::B_KT], 128);
+    mbar_init(&bars[C::B_DPE], 256);
+    mbar_init(&bars[C::B_KVE], 5);  // issuer A's commit and the 4 dQ warps (K^T built)
+    mbar_init(&bars[C::B_KTE], 1);
+    mbar_init(&bars[C::B_ACCE], 256);
+    for (int u = 0; u < C::NU; ++u) {
+      mbar_init(&bars[C::B_UF + u], 1);
+      mbar_init(&bars[C::B_UE + u], 14);  // both issuing warps, the 8 compute warps, the 4 dQ warps
+    }
+    mbar_init(&bars[C::B_CLC], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::W_MMA_A) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::W_PRODUCER) {
+    // ---------------------------------------------------------------- scheduler + TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+    }
+    int ux = (int)blockIdx.x, uy = (int)blockIdx.y;  // the unit to publish next (ux < 0: none)
+    int g0 = 0, issued = 0, kv_units = 0;  // the unit's first global step; steps / K,V pairs started
+    bool asked = false;
+    int n_asked = 0;
+    for (int u = 0;; ++u) {
+      const int us = u % C::NU;
+      if (u >= C::NU && !mbar_wait_w(&bars[C::B_UE + us], ((u / C::NU) - 1) & 1, wc, 50)) break;
+      units[us] = make_int2(ux, uy);
+      mbar_arrive_w(&bars[C::B_UF + us]);
+      if (ux < 0) break;
+      const int kt = ux, bh = uy, k0 = kt * C::BN, i0 = first_step(kt), n_it = n_steps(kt);
+      // K / V: free once the previous unit's last S^T and dP^T have read them
+      if (u >= 1 && !mbar_wait_w(&bars[C::B_KVE], (u - 1) & 1, wc, 51)) break;
+      mbar_arrive_expect_tx_w(&bars[C::B_KV], 2 * C::KV_TILE);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_3d_w(smem + C::OFF_K + c * C::K_CHUNK_BYTES, &tm_k, &bars[C::B_KV], c * C::CHUNK, k0, bh);
+        tma_load_3d_w(smem + C::OFF_V + c * C::K_CHUNK_BYTES, &tm_v, &bars[C::B_KV], c * C::CHUNK, k0, bh);
+      }
+      kv_units = u + 1;
+      bool ok = true;
+      for (int it = 0; it < n_it; ++it) {
+        const int g = g0 + it, s = g % C::NS, i = i0 + it;
+        if (g >= C::NS && !(ok = mbar_wait_w(&bars[C::B_QE + s], ((g / C::NS) - 1) & 1, wc, 31))) break;
+        mbar_arrive_expect_tx_w(&bars[C::B_QF + s], 2 * C::Q_TILE + 2 * C::BM * 4);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_3d_w(smem + C::OFF_Q + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_q, &bars[C::B_QF + s],
+                        c * C::CHUNK, i * C::BM, bh);
+          tma_load_3d_w(smem + C::OFF_DO + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_do, &bars[C::B_QF + s],
+                        c * C::CHUNK, i * C::BM, bh);
+        }
+        const size_t roff = (size_t)bh * p.Nq_pad + (size_t)i * C::BM;
+        bulk_load_w(smem + C::OFF_LSE + s * C::BM * 4, p.lse2 + roff, C::BM * 4, &bars[C::B_QF + s]);
+        bulk_load_w(smem + C::OFF_DLT + s * C::BM * 4, p.dlt + roff, C::BM * 4, &bars[C::B_QF + s]);
+        issued = g + 1;
+      }
+      if (!ok) break;
+      g0 += n_it;
+      // the next unit, asked for once this unit's last copies are started
+      mbar_arrive_expect_tx_w(&bars[C::B_CLC], 16);
+      clc_try_cancel_w(clc_resp, &bars[C::B_CLC]);
+      asked = true;
+      if (!mbar_wait_w(&bars[C::B_CLC], n_asked & 1, wc, 52)) break;
+      asked = false;
+      ++n_asked;
+      int cx, cy;
+      const bool taken = clc_taken(clc_resp, cx, cy);
+      ux = (taken && cx >= 0 && cx < (int)gridDim.x && cy >= 0 && cy < (int)gridDim.y) ? cx : -1;
+      uy = cy;
+    }
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+      volatile int no_abort = 0;
+      const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+      if (kv_units > 0) mbar_wait(&bars[C::B_KV], (kv_units - 1) & 1, w2, 40);
+      for (int g = issued > C::NS ? issued - C::NS : 0; g < issued; ++g)
+        mbar_wait(&bars[C::B_QF + g % C::NS], (g / C::NS) & 1, w2, 41);
+      if (asked) mbar_wait(&bars[C::B_CLC], n_asked & 1, w2, 53);
+    }
+  } else if (warp == C::W_MMA_A) {
+    // ---------------------------------------------------------------- UMMA issuer A: S^T, dP^T
+    const uint64_t dK = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);       // K, K-major
+    const uint64_t dV = sdesc(sbase + C::OFF_V, 16, 8 * C::ROWB, C::LAYOUT);       // V, K-major
+    const uint64_t dQk = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);      // Q stage 0, K-major
+    const uint64_t dOk = sdesc(sbase + C::OFF_DO, 16, 8 * C::ROWB, C::LAYOUT);     // dO stage 0, K-major
+    auto issue_s = [&](int g) {  // S^T(g) = K Q^T into TMEM buffer g & 1
+      const uint64_t q = desc_adv(dQk, (uint32_t)((g % C::NS) * C::Q_TILE));
+      const uint32_t d = tmem + C::T_S + (uint32_t)((g & 1) * 64);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma_ss_w(d, desc_adv(dK, koff<D>(C::K_CHUNK_BYTES, kk)), desc_adv(q, koff<D>(C::Q_CHUNK_BYTES, kk)),
+                  C::IDESC_S, kk > 0 ? 1u : 0u);
+      umma_commit_w(&bars[C::B_SF + (g & 1)]);
+    };
+    auto issue_dp = [&](int g) {  // dP^T(g) = V dO^T
+      const uint64_t o = desc_adv(dOk, (uint32_t)((g % C::NS) * C::Q_TILE));
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        umma_ss_w(tmem + C::T_DP, desc_adv(dV, koff<D>(C::K_CHUNK_BYTES, kk)), desc_adv(o, koff<D>(C::Q_CHUNK_BYTES, kk)),
+                  C::IDESC_S, kk > 0 ? 1u : 0u);
+      umma_commit_w(&bars[C::B_DPF]);
+    };
+    // S^T(g) needs its stage loaded and its TMEM buffer drained of dQ^T(g-2)
+    auto s_ready = [&](int g) {
+      return mbar_wait_w(&bars[C::B_QF + g % C::NS], (g / C::NS) & 1, wc, 33) &&
+             (g < 2 || mbar_wait_w(&bars[C::B_DQE + (g & 1)], ((g - 2) >> 1) & 1, wc, 49));
+    };
+    int g0 = 0;
+    bool ok = true;
+    for (int u = 0; ok; ++u) {
+      const int us = u % C::NU;
+      if (!(ok = mbar_wait_w(&bars[C::B_UF + us], (u / C::NU) & 1, wc, 54))) break;
+      const int2 un = units[us];
+      mbar_arrive_w(&bars[C::B_UE + us]);
+      if (un.x < 0) break;
+      const int n_it = n_steps(un.x);
+      if (!(ok = mbar_wait_w(&bars[C::B_KV], u & 1, wc, 32) && s_ready(g0))) break;
+      tc_fence_after();
+      issue_s(g0);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int g = g0 + it;
+        // dP^T(g) overwrites dP^T(g-1) once the compute warps have loaded it
+        if (g >= 1 && !(ok = mbar_wait_w(&bars[C::B_DPE], (g - 1) & 1, wc, 35))) break;
+        tc_fence_after();
+        issue_dp(g);
+        if (it + 1 < n_it) {
+          if (!(ok = s_ready(g + 1))) break;
+          tc_fence_after();
+          issue_s(g + 1);
+        }
+      }
+      umma_commit_w(&bars[C::B_KVE]);  // this unit's last UMMA reads of K and V are done
+      g0 += n_it;
+    }
+    umma_commit_w(&bars[C::B_DRAIN]);
+    volatile int no_abort = 0;
+    const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+    mbar_wait(&bars[C::B_DRAIN], 0, w2, 42);
+  } else if (warp == C::W_MMA_B) {
+    // ---------------------------------------------------------------- UMMA issuer B: dV, dQ^T, dK
+    const uint64_t dQm = sdesc(sbase + C::OFF_Q, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);   // MN-major
+    const uint64_t dOm = sdesc(sbase + C::OFF_DO, C::Q_CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);  // MN-major
+    const uint64_t dS0 = sdesc(sbase + C::OFF_DS, C::DS_BYTES, 1024, 2u);          // dS^T buffer 0, MN-major
+    const uint64_t dSa = sdesc(sbase + C::OFF_DS, 16, 1024, 2u);                   // the same, K-major A
+    int g0 = 0;
+    bool ok = true;
+    for (int u = 0; ok; ++u) {
+      const int us = u % C::NU;
+      if (!(ok = mbar_wait_w(&bars[C::B_UF + us], (u / C::NU) & 1, wc, 55))) break;
+      const int2 un = units[us];
+      mbar_arrive_w(&bars[C::B_UE + us]);
+      if (un.x < 0) break;
+      const int n_it = n_steps(un.x);
+      // dV and dK start from zero: the previous unit's epilogue must have read them out
+      if (u >= 1 && !(ok = mbar_wait_w(&bars[C::B_ACCE], (u - 1) & 1, wc, 56))) break;
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int g = g0 + it, s = g % C::NS, b = g & 1;
+        const uint64_t qm = desc_adv(dQm, (uint32_t)(s * C::Q_TILE));
+        const uint64_t om = desc_adv(dOm, (uint32_t)(s * C::Q_TILE));
+        if (!(ok = mbar_wait_w(&bars[C::B_PF + b], (g >> 1) & 1, wc, 34))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          umma_ts_w(tmem + C::T_DV, tmem + C::T_S + (uint32_t)(b * 64) + a_col(kk), desc_adv(om, mnoff<D>(kk)),
+                    C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+        if (!(ok = mbar_wait_w(&bars[C::B_DSF + b], (g >> 1) & 1, wc, 36))) break;
+        if (it == 0 && !(ok = mbar_wait_w(&bars[C::B_KT], u & 1, wc, 47))) break;
+        tc_fence_after();
+        const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          umma_ts_w(tmem + C::T_S + (uint32_t)(b * 64), tmem + C::T_KT + kk * 8, desc_adv(ds, (uint32_t)(kk * 16 * 128)),
+                    C::IDESC_DQ, kk > 0 ? 1u : 0u);
+        umma_commit_w(&bars[C::B_DQR + b]);
+        const uint64_t dsa = desc_adv(dSa, (uint32_t)(b * C::DS_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          umma_ss_w(tmem + C::T_DK, desc_adv(dsa, (uint32_t)(kk * 32)), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_w(&bars[C::B_QE + s]);   // dK was the stage's last reader
+        umma_commit_w(&bars[C::B_DQF + b]);  // dQ^T and dK have both read dS^T buffer b
+      }
+      umma_commit_w(&bars[C::B_KTE]);  // this unit's last read of K^T is done
+      g0 += n_it;
+    }
+    umma_commit_w(&bars[C::B_DRAIN + 1]);
+    volatile int no_abort = 0;
+    const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+    mbar_wait(&bars[C::B_DRAIN + 1], 0, w2, 42);
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- compute warpgroups
+    const int wg = (warp - 4) >> 2;  // 0: queries 0..31 of a tile (and dK), 1: queries 32..63 (and dV)
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // key row of the tile
+    const int col0 = wg * 32;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = p.scale_log2;
+    uint8_t* sds_row_base = smem + C::OFF_DS + row * 128;
+    int g0 = 0;
+    bool ok = true;
+    for (int u = 0;; ++u) {
+      const int us = u % C::NU;
+      if (!(ok = ok && warp_wait(&bars[C::B_UF + us], (u / C::NU) & 1, wc, 57))) break;
+      const int2 un = units[us];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
+      if (un.x < 0) break;
+      const int kt = un.x, bh = un.y, k0 = kt * C::BN, key = k0 + row, i0 = first_step(kt), n_it = n_steps(kt);
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int g = g0 + it, s = g % C::NS, i = i0 + it;
+        const uint32_t t_sb = (uint32_t)((g & 1) * 64);  // this step's S^T / P^T buffer
+        if (!warp_wait(&bars[C::B_QF + s], (g / C::NS) & 1, wc, 38) ||
+            !warp_wait(&bars[C::B_SF + (g & 1)], (g >> 1) & 1, wc, 39)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sreg[32];
+        tmem_ld32(t_lane + C::T_S + t_sb + col0, sreg);
+        tmem_wait_ld(sreg);
+        const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * C::BM * 4) + col0;
+        const float* dlt = reinterpret_cast<const float*>(smem + C::OFF_DLT + s * C::BM * 4) + col0;
+        const int qb = i * C::BM + col0;  // query of column 0 of this warpgroup's half
+        const bool need_mask = (k0 + C::BN > p.Nk) || (CAUSAL && (k0 + C::BN - 1 > qb));
+        const int lim = CAUSAL ? key - qb : (1 << 30);  // columns c with q = qb + c < key are masked
+        const bool key_valid = key < p.Nk;
+        float pv[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float x = ex2(fmaf(as_f(sreg[c]), sl2, -lse2[c]));
+          if (need_mask && (!key_valid || (CAUSAL && c < lim))) x = 0.f;
+          pv[c] = x;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
+        tmem_st16(t_lane + C::T_S + t_sb + wg * 32, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[C::B_PF + (g & 1)]);
+
+        if (!warp_wait(&bars[C::B_DPF], g & 1, wc, 43)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t dv[32];
+        tmem_ld32(t_lane + C::T_DP + col0, dv);
+        tmem_wait_ld(dv);
+        tc_fence_before();
+        mbar_arrive(&bars[C::B_DPE]);  // dP^T(g+1) may overwrite it now
+        uint32_t dk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float d0 = pv[2 * c] * (as_f(dv[2 * c]) - dlt[2 * c]);
+          const float d1 = pv[2 * c + 1] * (as_f(dv[2 * c + 1]) - dlt[2 * c + 1]);
+          dk[c] = pack_bf16(d0, d1);
+        }
+        // dS^T row into shared memory buffer g & 1 once the dQ^T and dK MMAs of step g-2 have
+        // read it
+        if (g >= 2 && !warp_wait(&bars[C::B_DQF + (g & 1)], ((g - 2) >> 1) & 1, wc, 44)) {
+          ok = false;
+          break;
+        }
+        uint8_t* dsrow = sds_row_base + (g & 1) * C::DS_BYTES;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int phys = (4 * wg + t) ^ (row & 7);
+          *reinterpret_cast<uint4*>(dsrow + phys * 16) = make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[C::B_DSF + (g & 1)]);
+      }
+      // epilogue: WG0 writes dK = scale * acc, WG1 writes dV, once the unit's last MMAs are
+      // done; the accumulator is handed back to issuer B as soon as it is read out
+      const int gl = g0 + n_it - 1;
+      g0 += n_it;
+      if (!(ok = ok && warp_wait(&bars[C::B_DQF + (gl & 1)], (gl >> 1) & 1, wc, 45))) break;
+      tc_fence_after();
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) + ((size_t)bh * p.Nk + key) * D;
+      const float mul = (wg == 0) ? p.scale : 1.f;
+#pragma unroll
+      for (int gg = 0; gg < D / 16; ++gg) {
+        uint32_t v[16];
+        tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + gg * 16, v);
+        tmem_wait_ld(v);
+        if (key < p.Nk) store_row_bf16<D>(dst + gg * 16, v, mul);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[C::B_ACCE]);
+    }
+  } else {
+    // ---------------------------------------------------------------- dQ warpgroup (warps 0-3)
+    const int d = warp * 32 + lane;  // TMEM lane = row d of dQ^T
+    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+    float* stg = reinterpret_cast<float*>(smem + C::OFF_STG);
+    int g0 = 0;
+    bool ok = true;
+    for (int u = 0;; ++u) {
+      // the four warps agree before any of them reaches the named barriers below
+      const int us = u % C::NU;
+      if (!named_bar_and(1, 128, ok && warp_wait(&bars[C::B_UF + us], (u / C::NU) & 1, wc, 58))) break;
+      const int2 un = units[us];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
+      if (un.x < 0) break;
+      const int kt = un.x, bh = un.y, i0 = first_step(kt), n_it = n_steps(kt);
+      // K^T into TMEM for this unit (lane d holds K[key][d] for all 128 keys as bf16 pairs,
+      // lanes d >= D zeros) once K has landed and the previous unit's dQ^T MMAs are done
+      ok = named_bar_and(1, 128, warp_wait(&bars[C::B_KV], u & 1, wc, 48) &&
+                                     (u == 0 || warp_wait(&bars[C::B_KTE], (u - 1) & 1, wc, 59)));
+      if (!ok) break;
+      {
+        const uint8_t* sK = smem + C::OFF_K;
+        const int dc = d < D ? d : 0;
+        const int chunk = dc / C::CHUNK, col = dc % C::CHUNK;
+        const uint8_t* base = sK + chunk * C::K_CHUNK_BYTES + (col % 8) * 2;
+        const int uu = col / 8;
+        uint32_t ktr[2][32];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          uint32_t pr = 0;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r = 2 * c + h;  // key row of the swizzled K-major tile
+            const int phys = uu ^ ((r * C::ROWB >> 7) & (C::ROWB / 16 - 1));
+            const uint32_t e = *reinterpret_cast<const uint16_t*>(base + r * C::ROWB + phys * 16);
+            pr |= (d < D ? e : 0u) << (16 * h);
+          }
+          ktr[c >> 5][c & 31] = pr;
+        }
+        tc_fence_after();
+        tmem_st32(t_lane + C::T_KT, ktr[0]);
+        tmem_st32(t_lane + C::T_KT + 32, ktr[1]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[C::B_KT]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::B_KVE]);  // this warp's reads of K are done
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int g = g0 + it, b = g & 1;
+        if (!(ok = named_bar_and(1, 128, warp_wait(&bars[C::B_DQR + b], (g >> 1) & 1, wc, 46)))) break;
+        tc_fence_after();
+        uint32_t v0[32], v1[32];
+        tmem_ld32(t_lane + C::T_S + (uint32_t)(b * 64), v0);
+        tmem_ld32(t_lane + C::T_S + (uint32_t)(b * 64) + 32, v1);
+        tmem_wait_ld(v0);
+        reg_tie(v1);
+        tc_fence_before();
+        mbar_arrive(&bars[C::B_DQE + b]);
+        float* gdst = p.dq_accum + ((size_t)bh * p.Nq_pad + (size_t)(i0 + it) * C::BM) * D;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+          named_bar_sync(1, 128);
+          if (d < D) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) stg[(h * 32 + c) * D + d] = as_f(h == 0 ? v0[c] : v1[c]);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (threadIdx.x == 0) {
+            bulk_reduce_add_f32(gdst + h * 32 * D, stg + h * 32 * D, C::STG_BYTES / 2);
+            bulk_commit_group();
+          }
+        }
+      }
+      g0 += n_it;
+    }
+    if (threadIdx.x == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::W_MMA_A) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------
 // prep: Dlt = rowsum(dO o O), lse2 = L * log2(e) (+inf past Nq), dq_accum = 0, for the
 // 64-row-padded workspace rows of one (sequence, head) per blockIdx.y.
 // ------------------------------------------------------------------------------------
@@ -664,6 +1116,18 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   return cudaGetLastError();
 }
 
+template <int D, bool CAUSAL>
+cudaError_t launch_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                             const BwdParams& p, int BH, cudaStream_t st) {
+  using C = Cfg<D>;
+  auto kern = bwd_persist_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)p.n_k_tiles, (unsigned)BH);
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t prep_t(const PrepParams& p, cudaStream_t st) {
   const int rows = p.va.cu_q ? (p.Nq + 63) / 64 * 64 : p.Nq_pad;  // varlen: padded maximum length
@@ -701,6 +1165,10 @@ cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensor
   if (p.va.cu_q) {
     TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true, true>(tq, tk, tv, tdo, p, BH, st)
                              : bwd::launch_t<DD, false, true>(tq, tk, tv, tdo, p, BH, st)))
+  }
+  if (p.persist) {
+    TA11_SWITCH_D(D, (causal ? bwd::launch_persist_t<DD, true>(tq, tk, tv, tdo, p, BH, st)
+                             : bwd::launch_persist_t<DD, false>(tq, tk, tv, tdo, p, BH, st)))
   }
   TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true, false>(tq, tk, tv, tdo, p, BH, st)
                            : bwd::launch_t<DD, false, false>(tq, tk, tv, tdo, p, BH, st)))

@@ -21,6 +21,8 @@ std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 // Forward kernel choice for the dense layout with plain masks beyond one wave: 1 the
 // persistent kernel, 0 one CTA per unit (the persistent kernel's parity tests compare the two).
 std::atomic<int> g_fwd_persist{1};
+// The same choice for the main backward kernel.
+std::atomic<int> g_bwd_persist{1};
 
 // Optional events recorded around the main backward kernel (timing hook).
 std::mutex g_ev_mu;
@@ -237,6 +239,8 @@ void fa_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns
 
 int fa_set_fwd_persistent(int on) { return g_fwd_persist.exchange(on ? 1 : 0); }
 
+int fa_set_bwd_persistent(int on) { return g_bwd_persist.exchange(on ? 1 : 0); }
+
 size_t fa_bwd_workspace_size(int B, int H, int Nq, int Nk, int D) {
   if (check_sizes(B, H, Nq, Nk, D, 1.f) != FA_OK) return 0;
   return ws_layout(B, H, Nq, D).total;
@@ -434,6 +438,14 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
       bp.dkv_accum = dkv_accum;
     }
   }
+  // persistent kernel: plain masks, more CTAs than one wave, every key tile with a query
+  // step (causal: the last key tile starts below Nq).  It saves a fixed time per unit;
+  // with D = 128 and more than 128 query steps per unit it measured about 1% slower than
+  // one CTA per unit, so those keep one CTA per unit.
+  const bool all_steps = !causal || (long long)(bp.n_k_tiles - 1) * 128 < Nq;
+  const bool short_units = D < 128 || Nq <= 8192;
+  bp.persist = (!lm && all_steps && short_units && (long long)bp.n_k_tiles * BH > current_sms())
+                   ? g_bwd_persist.load() : 0;
   cudaEvent_t ev_b = nullptr, ev_e = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_ev_mu);

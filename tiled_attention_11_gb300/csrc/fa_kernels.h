@@ -149,6 +149,9 @@ struct BwdParams {
   // partial dK, dV (fp32, unscaled) into dkv_accum; bwd_kv_convert writes them out.
   int n_gk, n_qsplit, split_q;
   float* dkv_accum;     // [B*H][n_gk*128][2][D] (zeroed before the launch)
+  // Dense layout, plain masks, more units than one wave and at least one query step per
+  // key tile: the persistent kernel (a CTA takes over not-yet-started CTAs of its grid).
+  int persist;
 };
 
 struct KvConvertParams {
