@@ -113,6 +113,57 @@ def test_many_short_sequences():
     check_varlen(lens, lens, 2, 128, True, seed=13)
 
 
+def test_thousands_of_sequences():
+    # more than 1024 sequences (three rounds of the kernels' 32-way slot search), empty
+    # ones among them
+    rng = np.random.default_rng(4)
+    lens = rng.integers(0, 40, size=1100).tolist()
+    check_varlen(lens, lens, 2, 64, True, seed=15)
+
+
+# more (slot, head) units than SMs: the forward runs persistent CTAs by default
+PERSIST_VARLEN = [(MIX, MIX, 16, 128, True), (MIX, MIX, 16, 64, False),
+                  ([0, 5, 0, 130, 64, 0], [0, 5, 7, 130, 0, 3], 40, 32, True),
+                  (I.doc_lengths(4096, seed=9), I.doc_lengths(4096, seed=9), 8, 128, True)]
+
+
+@pytest.mark.parametrize("case", PERSIST_VARLEN, ids=[f"H{c[2]}D{c[3]}{'c' if c[4] else 'n'}-{i}"
+                                                      for i, c in enumerate(PERSIST_VARLEN)])
+def test_persistent_forward_equals_one_cta_per_unit(case):
+    # the persistent schedule changes which SM runs a (sequence, pair, head) unit, never its
+    # arithmetic: O and L bitwise equal to one CTA per slot, and both match the oracle
+    lens_q, lens_k, H, D, causal = case
+    q, k, v, do, cu_q, cu_k = I.draw_varlen(lens_q, lens_k, H, D, 17, 1.0)
+    assert (sum(lens_q) // 256 + len(lens_q)) * H > 152
+    dev = torch.device("cuda")
+    qg, kg, vg = (t.to(dev) for t in (q, k, v))
+    cq, ck = cu_q.to(dev), cu_k.to(dev)
+    mq, mk = max(max(lens_q), 1), max(max(lens_k), 1)
+    scale = 1.0 / np.sqrt(D)
+    outs = []
+    prev = _lib.fa_set_fwd_persistent(False)
+    try:
+        for on in (False, True):
+            _lib.fa_set_fwd_persistent(on)
+            o = torch.full_like(qg, float("nan"))
+            lse = torch.full((H, q.shape[0]), float("nan"), dtype=torch.float32, device=dev)
+            _lib.fa_fwd_varlen(qg, kg, vg, o, lse, cq, ck, mq, mk, causal, scale)
+            outs.append((o, lse))
+        torch.cuda.synchronize()
+    finally:
+        _lib.fa_set_fwd_persistent(prev)
+    (o1, l1), (o2, l2) = outs
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    qd, kd, vd, dod = (I.as_f64(t) for t in (q, k, v, do))
+    ro, rl, _, _, _ = oracle.attention_varlen(qd, kd, vd, dod, cu_q.numpy(), cu_k.numpy(), scale, causal)
+    assert_close(f"H{H}D{D} O", f64(o2), ro)
+    gl = f64(l2)
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isneginf(gl), ~fin)
+    if fin.any():
+        assert np.abs(gl[fin] - rl[fin]).max() <= LSE_ABS
+
+
 def test_scaled_inputs_peaked_softmax():
     check_varlen([129, 700, 33], [129, 700, 33], 2, 128, True, seed=14, factor=8.0)
 

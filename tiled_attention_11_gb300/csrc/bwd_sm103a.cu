@@ -126,21 +126,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
-template <int D>
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[16], float mul) {
-  uint4 w0, w1;
-  w0.x = pack_bf16(as_f(v[0]) * mul, as_f(v[1]) * mul);
-  w0.y = pack_bf16(as_f(v[2]) * mul, as_f(v[3]) * mul);
-  w0.z = pack_bf16(as_f(v[4]) * mul, as_f(v[5]) * mul);
-  w0.w = pack_bf16(as_f(v[6]) * mul, as_f(v[7]) * mul);
-  w1.x = pack_bf16(as_f(v[8]) * mul, as_f(v[9]) * mul);
-  w1.y = pack_bf16(as_f(v[10]) * mul, as_f(v[11]) * mul);
-  w1.z = pack_bf16(as_f(v[12]) * mul, as_f(v[13]) * mul);
-  w1.w = pack_bf16(as_f(v[14]) * mul, as_f(v[15]) * mul);
-  reinterpret_cast<uint4*>(dst)[0] = w0;
-  reinterpret_cast<uint4*>(dst)[1] = w1;
-}
-
 template <int D, bool CAUSAL, bool VARLEN, bool LOCAL>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -169,9 +154,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       kt = kt - n_split_ctas + p.n_gk;
     }
   }
-  const int bh = blockIdx.y;
+  const int bh = blockIdx.y;  // dense: batch * head; packed: head
+  // Packed batch: column x of the grid is a compact slot (slot_seq) of sequence b, whose
+  // key tiles take its slots in order; a slot past the sequence's keys has nothing to do.
+  int by = bh;
+  if (VARLEN) {
+    const int b = slot_seq(p.va.cu_k, p.va.B, p.va.total_k, 7, (int)blockIdx.x);
+    by = b * p.va.H + bh;
+    kt = (int)blockIdx.x - slot_base(p.va.cu_k, p.va.total_k, 7, b);
+  }
   const int k0 = kt * C::BN;
-  const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, bh);
+  const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, by);
   if (VARLEN && k0 >= sv.Nk) return;  // this sequence has fewer keys: nothing to do
   // TMA coordinates (dense maps [B*H][N][D]: y = row, z = bh; packed [total][H][D]: y = head,
   // z = token) and the first workspace row of this sequence
@@ -179,7 +172,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   auto ty = [&](int r) { return VARLEN ? sv.h : r; };
   auto tzq = [&](int r) { return VARLEN ? qz_b + r : qz_b; };
   auto tzk = [&](int r) { return VARLEN ? kz_b + r : kz_b; };
-  const long long wrow0 = ws_row0(VARLEN, bh, p.Nq_pad, sv);
+  const long long wrow0 = ws_row0(VARLEN, by, p.Nq_pad, sv);
   // Query steps (64 rows) that see a key of this tile: causal ones start at the diagonal;
   // with the local mask they are the global query steps [a, g) and the window steps [L, hi)
   // (every step when the tile holds a global key).
@@ -486,7 +479,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         uint32_t v[16];
         tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + g * 16, v);
         tmem_wait_ld(v);
-        if (key < sv.Nk) store_row_bf16<D>(dst + g * 16, v, mul);
+        if (key < sv.Nk) store16_bf16(dst + g * 16, v, mul);
       }
     }
   } else {
@@ -910,7 +903,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         uint32_t v[16];
         tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + gg * 16, v);
         tmem_wait_ld(v);
-        if (key < p.Nk) store_row_bf16<D>(dst + gg * 16, v, mul);
+        if (key < p.Nk) store16_bf16(dst + gg * 16, v, mul);
       }
       tc_fence_before();
       mbar_arrive(&bars[C::B_ACCE]);
@@ -1111,7 +1104,8 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   const int gx = (LOCAL && p.n_gk > 0) ? p.n_gk * p.n_qsplit + (p.n_k_tiles - p.n_gk) : p.n_k_tiles;
-  dim3 grid((unsigned)gx, (unsigned)BH);
+  // packed batch: compact slots of 128 keys (slot_seq), one grid row per head
+  dim3 grid = VARLEN ? dim3((unsigned)((p.va.total_k >> 7) + p.va.B), (unsigned)p.va.H) : dim3((unsigned)gx, (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }

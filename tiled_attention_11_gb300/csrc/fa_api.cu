@@ -707,7 +707,9 @@ extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* 
   p.scale_log2 = scale * kLog2e;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.status = status;
-  p.va = ta11::VarlenArgs{cu_seqlens_q, cu_seqlens_k, H, total_q, total_k};
+  p.va = ta11::VarlenArgs{cu_seqlens_q, cu_seqlens_k, H, total_q, total_k, B};
+  // persistent CTAs beyond one wave (compact slots of 256 queries per head, see slot_seq)
+  p.persist = ((long long)((total_q >> 8) + B) * H > current_sms()) ? g_fwd_persist.load() : 0;
   return ta11::launch_fwd(D, causal != 0, tq, tk, tv, tq, p, B * H, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -752,7 +754,7 @@ extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const 
   float* dq_accum = reinterpret_cast<float*>(ws + w.dq_off);
   float* dlt = reinterpret_cast<float*>(ws + w.dlt_off);
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
-  const ta11::VarlenArgs va{cu_seqlens_q, cu_seqlens_k, H, total_q, total_k};
+  const ta11::VarlenArgs va{cu_seqlens_q, cu_seqlens_k, H, total_q, total_k, B};
   ta11::PrepParams pp{o, dO, lse, dq_accum, lse2, dlt, B * H, max_seqlen_q, w.Nq_pad, va};
   if (ta11::launch_bwd_prep(D, pp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   ta11::BwdParams bp{};

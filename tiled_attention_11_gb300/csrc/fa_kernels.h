@@ -16,6 +16,7 @@ struct VarlenArgs {
   const int* cu_k;
   int H;                // heads
   int total_q, total_k; // packed token counts
+  int B;                // sequences
 };
 
 // One (sequence, head) as seen by a CTA, for either layout.
@@ -46,6 +47,33 @@ __device__ __forceinline__ SeqView seq_view(const VarlenArgs& va, int Nq, int Nk
   s.Nq = min(qe - qa, Nq);
   s.Nk = min(ke - ka, Nk);
   return s;
+}
+
+// Compact tile slots of a packed batch (one grid row per head): sequence b owns slots
+// [f(b), f(b+1)) with f(b) = floor(cu[b] / 2^shift) + b.  That is at least
+// ceil(len_b / 2^shift) slots (at most one more), f(B) = floor(total / 2^shift) + B in all,
+// so a grid of f(B) columns launches at most B empty CTAs per head instead of one per
+// tile of the longest sequence in every shorter one.
+__device__ __forceinline__ int slot_base(const int* cu, int total, int shift, int b) {
+  return (max(0, min(__ldg(cu + b), total)) >> shift) + b;
+}
+
+// The sequence of slot x: the largest b < B with f(b) <= x, found by 32-way probes of
+// cu (one round of loads for B <= 32).  Every lane of a converged warp calls it and gets
+// the answer.  cu must be nondecreasing; any other input still gives some b in [0, B).
+__device__ __forceinline__ int slot_seq(const int* cu, int B, int total, int shift, int x) {
+  const int lane = (int)(threadIdx.x & 31u);
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) >> 5;
+    const int pos = lo + lane * step;
+    const bool le = pos < hi && slot_base(cu, total, shift, pos) <= x;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    const int top = m ? 31 - __clz((int)m) : 0;
+    lo += top * step;
+    hi = min(lo + step, hi);
+  }
+  return lo;
 }
 
 // Local-window + global-token mask (absolute indices, top-left like the causal mask):

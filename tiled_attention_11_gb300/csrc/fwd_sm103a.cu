@@ -81,8 +81,8 @@ struct Cfg {
   static constexpr int B_CLC = B_UE + NU;
   static constexpr int NBAR = B_CLC + 1;
   static constexpr int OFF_CLC = OFF_BAR + ((NBAR * 8 + 16 + 15) / 16) * 16;  // 16-byte launch-control answer
-  static constexpr int OFF_UNITS = OFF_CLC + 16;                               // NU x int2 work units
-  static constexpr int SMEM_USED = OFF_UNITS + NU * 8;
+  static constexpr int OFF_UNITS = OFF_CLC + 16;                               // NU x 32-byte work units
+  static constexpr int SMEM_USED = OFF_UNITS + NU * 32;
   // At least ~120 KB so only one CTA (and one 512-column TMEM allocation) fits per SM.
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
   static constexpr int THREADS = 320;
@@ -199,10 +199,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       pair = pair - n_split_ctas + p.n_gp;
     }
   }
-  const int bh = blockIdx.y;
+  const int bh = blockIdx.y;  // dense: batch * head; packed: head
+  // Packed batch: column x of the grid is a compact slot (slot_seq) of sequence b, whose
+  // pairs take its slots heaviest first; a slot past the sequence's pairs has nothing to do.
+  int by = bh;
+  if (VARLEN) {
+    const int b = slot_seq(p.va.cu_q, p.va.B, p.va.total_q, 8, (int)blockIdx.x);
+    by = b * p.va.H + bh;
+    pair = (int)blockIdx.x - slot_base(p.va.cu_q, p.va.total_q, 8, b);
+  }
+  const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, by);
+  if (VARLEN) {
+    const int n_pairs = (sv.Nq + 2 * C::BM - 1) / (2 * C::BM);
+    if (pair >= n_pairs) return;
+    pair = n_pairs - 1 - pair;
+  }
   const int q0 = pair * 2 * C::BM;
-  const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nk, bh);
-  if (VARLEN && q0 >= sv.Nq) return;  // this sequence is shorter than the pair: nothing to do
   auto o_row = [&](int q) -> size_t {  // element offset of output row q
     return (VARLEN ? ((size_t)(sv.q_tok + q) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + q)) * D;
   };
@@ -664,24 +676,36 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 }
 
 // ------------------------------------------------------------------------------------
-// Persistent form of the two-tile kernel for the dense layout with the plain masks.  The
-// grid still has one CTA per (query-tile pair, batch*head) in the same order, but a
-// running CTA takes over the next CTA that has not started yet (cluster launch control)
+// Persistent form of the two-tile kernel for the plain masks, dense or packed.  The grid
+// still has one CTA per (query-tile pair, batch*head) in the same order (packed: one per
+// compact slot and head, see slot_seq), but a running CTA takes over the next CTA that has
+// not started yet (cluster launch control)
 // instead of exiting, so the hardware keeps handing out units heaviest-first to whichever
 // SM frees up, while the CTA's pipelines run on across units: the producer loads the
 // next unit's Q tiles as soon as the current unit's last S MMAs have read the old ones,
 // and the issuer computes the next unit's first S tiles while the softmax warpgroups are
 // still in the current unit's epilogue.  Per-CTA set-up (barriers, TMEM, descriptor
 // prefetch) is paid once per SM instead of once per unit.
-//   warp 8 lane 0  publishes each unit in a 4-slot ring (unit_full / unit_empty
-//                  barriers), issues the copies, and asks for the next unit once the
-//                  current one's last copies are started;
+//   warp 8         publishes each unit (its pair, head and sequence view) in a 4-slot
+//                  ring (unit_full / unit_empty barriers), issues the copies, and asks for
+//                  the next unit once the current one's last copies are started; packed:
+//                  it resolves a slot into (sequence, pair), passes over slots with no
+//                  pair, and itself writes O = 0, L = -inf for a pair whose sequence has
+//                  no keys;
 //   warp 9 lane 0  issues the UMMAs exactly as the two-tile kernel, with ring positions
 //                  and barrier phases counted across units;
 //   warps 0-7      the two softmax warpgroups; each unit's epilogue stores O through the
-//                  staging tile, which the two tiles hand to each other (B_STG / B_STG1).
+//                  staging tile, which the two tiles hand to each other (B_STG / B_STG1)
+//                  (packed: row by row, as the two-tile kernel).
 // ------------------------------------------------------------------------------------
-template <int D, bool CAUSAL>
+// A unit as the producer publishes it: query rows [q0, q0 + 256) of one (sequence, head).
+// Dense: z = batch*head, q_tok = k_tok = 0, nq = Nq, nk = Nk; packed: z = head, q_tok /
+// k_tok the sequence's first tokens, nq / nk its lengths.  live = 0 ends the ring.
+struct FwdUnit {
+  int q0, z, q_tok, k_tok, nq, nk, live, pad;
+};
+
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -694,13 +718,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   void* clc_resp = smem + C::OFF_CLC;
-  int2* units = reinterpret_cast<int2*>(smem + C::OFF_UNITS);
+  FwdUnit* units = reinterpret_cast<FwdUnit*>(smem + C::OFF_UNITS);
 
   const int warp = (int)warp_id(), lane = (int)lane_id();
-  const int nkt = (p.Nk + C::BN - 1) / C::BN;
-  // key tiles of the query tile starting at row qa: [0, hi); a tile past the rows is
-  // computed and never stored, as in the two-tile kernel
-  auto n_keys = [&](int qa) { return CAUSAL ? min(nkt, qa / C::BM + 1) : nkt; };
+  // key tiles of the query tile starting at row qa of a sequence with nk keys: [0, hi); a
+  // tile past the rows is computed and never stored, as in the two-tile kernel
+  auto n_keys = [&](int qa, int nk) {
+    const int nkt = (nk + C::BN - 1) / C::BN;
+    return CAUSAL ? min(nkt, qa / C::BM + 1) : nkt;
+  };
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
 
   if (threadIdx.x == 0) {
@@ -744,25 +770,85 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       if (lane == 0) tma_prefetch_desc(&tm_k);
       if (lane == 0) tma_prefetch_desc(&tm_v);
       if (lane == 0) tma_prefetch_desc(&tm_o);
-      int ux = (int)blockIdx.x, uy = (int)blockIdx.y;  // the unit to publish next (ux < 0: none)
+      int ux = (int)blockIdx.x, uy = (int)blockIdx.y;  // the CTA index to work on next (ux < 0: none)
       int jg = 0, k_issued = 0, v_issued = 0, q_units = 0;  // copies started (ring positions, Q pairs)
       bool asked = false;  // a launch-control answer is pending
       int n_asked = 0;
+      // take over the next CTA of the grid that has not started (ux = -1: none is left)
+      auto claim = [&]() -> bool {
+        mbar_arrive_expect_tx_w(&bars[C::B_CLC], 16);
+        clc_try_cancel_w(clc_resp, &bars[C::B_CLC]);
+        asked = true;
+        if (!mbar_wait_w(&bars[C::B_CLC], n_asked & 1, wc, 12)) return false;
+        asked = false;
+        ++n_asked;
+        int cx, cy;
+        const bool taken = clc_taken(clc_resp, cx, cy);
+        ux = (taken && cx >= 0 && cx < (int)gridDim.x && cy >= 0 && cy < (int)gridDim.y) ? cx : -1;
+        uy = cy;
+        return true;
+      };
+      // the unit of CTA (ux, uy); false when it has nothing for the pipeline (packed: a slot
+      // past its sequence's pairs, or a pair whose sequence has no keys, whose rows get
+      // O = 0, L = -inf here)
+      auto resolve = [&](FwdUnit& un) -> bool {
+        un.live = 1;
+        un.pad = 0;
+        if (!VARLEN) {
+          un.q0 = ((int)gridDim.x - 1 - ux) * 2 * C::BM;
+          un.z = uy;
+          un.q_tok = un.k_tok = 0;
+          un.nq = p.Nq;
+          un.nk = p.Nk;
+          return true;
+        }
+        const int b = slot_seq(p.va.cu_q, p.va.B, p.va.total_q, 8, ux);
+        const int j = ux - slot_base(p.va.cu_q, p.va.total_q, 8, b);
+        const SeqView sv = seq_view<true>(p.va, p.Nq, p.Nk, b * p.va.H + uy);
+        const int n_pairs = (sv.Nq + 2 * C::BM - 1) / (2 * C::BM);
+        if (j >= n_pairs) return false;
+        un.q0 = (n_pairs - 1 - j) * 2 * C::BM;  // heaviest pair of the sequence first
+        un.z = uy;
+        un.q_tok = sv.q_tok;
+        un.k_tok = sv.k_tok;
+        un.nq = sv.Nq;
+        un.nk = sv.Nk;
+        if (sv.Nk > 0) return true;
+        const int r1 = min(un.q0 + 2 * C::BM, sv.Nq);
+        for (int e = lane; e < (r1 - un.q0) * (D / 8); e += 32) {
+          const int q = un.q0 + e / (D / 8);
+          reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                   ((size_t)(sv.q_tok + q) * p.va.H + uy) * D)[e % (D / 8)] = make_uint4(0, 0, 0, 0);
+        }
+        for (int q = un.q0 + lane; q < r1; q += 32) p.lse[(size_t)uy * p.va.total_q + sv.q_tok + q] = -INFINITY;
+        return false;
+      };
       for (int i = 0;; ++i) {
+        FwdUnit un;
+        un.live = 0;
+        bool ok = true;
+        while (ux >= 0 && !resolve(un))
+          if (!(ok = claim())) break;
+        if (!ok) break;
+        if (ux < 0) un.live = 0;
         const int us = i % C::NU;
         if (i >= C::NU && !mbar_wait_w(&bars[C::B_UE + us], ((i / C::NU) - 1) & 1, wc, 10)) break;
-        units[us] = make_int2(ux, uy);
+        units[us] = un;  // (every lane holds the same record)
         mbar_arrive_w(&bars[C::B_UF + us]);
-        if (ux < 0) break;
-        const int q0 = ((int)gridDim.x - 1 - ux) * 2 * C::BM, bh = uy;
-        const int n_kv = n_keys(q0 + C::BM);  // tile 1's walk contains tile 0's
-        bool ok = true;
+        if (!un.live) break;
+        const int q0 = un.q0;
+        // TMA coordinates of row r: dense maps [B*H][N][D] (y = row, z = batch*head), packed
+        // maps [total][H][D] (y = head, z = token)
+        auto ty = [&](int r) { return VARLEN ? un.z : r; };
+        auto tzq = [&](int r) { return VARLEN ? un.q_tok + r : un.z; };
+        auto tzk = [&](int r) { return VARLEN ? un.k_tok + r : un.z; };
+        const int n_kv = n_keys(q0 + C::BM, un.nk);  // tile 1's walk contains tile 0's
         for (int t = 0; t < 2 && ok; ++t) {  // Q_t is free once the last S MMA reading it is done
           if (i >= 1 && !(ok = mbar_wait_w(&bars[C::B_QE + t], (i - 1) & 1, wc, 11))) break;
           mbar_arrive_expect_tx_w(&bars[C::B_Q + t], C::TILE_BYTES);
           for (int c = 0; c < C::NCHUNK; ++c)
             tma_load_3d_w(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
-                        c * C::CHUNK, q0 + t * C::BM, bh);
+                        c * C::CHUNK, ty(q0 + t * C::BM), tzq(q0 + t * C::BM));
         }
         if (!ok) break;
         q_units = i + 1;
@@ -772,29 +858,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           mbar_arrive_expect_tx_w(&bars[C::B_KF + s], C::TILE_BYTES);
           for (int c = 0; c < C::NCHUNK; ++c)
             tma_load_3d_w(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
-                        c * C::CHUNK, j * C::BN, bh);
+                        c * C::CHUNK, ty(j * C::BN), tzk(j * C::BN));
           k_issued = jg + 1;
           if (jg >= C::NS && !(ok = mbar_wait_w(&bars[C::B_VE + s], ((jg / C::NS) - 1) & 1, wc, 1))) break;
           mbar_arrive_expect_tx_w(&bars[C::B_VF + s], C::TILE_BYTES);
           for (int c = 0; c < C::NCHUNK; ++c)
             tma_load_3d_w(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
-                        c * C::CHUNK, j * C::BN, bh);
+                        c * C::CHUNK, ty(j * C::BN), tzk(j * C::BN));
           v_issued = jg + 1;
         }
         if (!ok) break;
         // Ask for the next unit only now, with this unit's last copies started (NS key tiles
         // before its end): a unit claimed earlier would sit behind the whole current one
         // while other SMs go idle, which unbalances launches of very uneven units.
-        mbar_arrive_expect_tx_w(&bars[C::B_CLC], 16);
-        clc_try_cancel_w(clc_resp, &bars[C::B_CLC]);
-        asked = true;
-        if (!mbar_wait_w(&bars[C::B_CLC], n_asked & 1, wc, 12)) break;
-        asked = false;
-        ++n_asked;
-        int cx, cy;
-        const bool taken = clc_taken(clc_resp, cx, cy);
-        ux = (taken && cx >= 0 && cx < (int)gridDim.x && cy >= 0 && cy < (int)gridDim.y) ? cx : -1;
-        uy = cy;
+        if (!claim()) break;
       }
       if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         // Let every copy already started land before the CTA can exit: the newest phase of
@@ -839,11 +916,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       for (int i = 0; ok; ++i) {
         const int us = i % C::NU;
         if (!(ok = mbar_wait_w(&bars[C::B_UF + us], (i / C::NU) & 1, wc, 13))) break;
-        const int2 u = units[us];
+        const FwdUnit u = units[us];
         mbar_arrive_w(&bars[C::B_UE + us]);
-        if (u.x < 0) break;
-        const int q0 = ((int)gridDim.x - 1 - u.x) * 2 * C::BM;
-        const int n_kv0 = n_keys(q0), n_kv1 = n_keys(q0 + C::BM);
+        if (!u.live) break;
+        const int nk = VARLEN ? u.nk : p.Nk;
+        const int n_kv0 = n_keys(u.q0, nk), n_kv1 = n_keys(u.q0 + C::BM, nk);
         // the unit's first S tiles (their TMEM buffers were last read by the previous
         // unit's P V, issued earlier by this thread)
         ok = mbar_wait_w(&bars[C::B_Q], i & 1, wc, 2) && mbar_wait_w(&bars[C::B_KF + jg % C::NS], (jg / C::NS) & 1, wc, 3);
@@ -905,14 +982,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       // the four warps agree to go on (a failed wait anywhere stops all of them together)
       const int us = i % C::NU;
       if (!named_bar_and(1 + t, 128, ok && warp_wait(&bars[C::B_UF + us], (i / C::NU) & 1, wc, 14))) break;
-      const int2 u = units[us];
+      const FwdUnit u = units[us];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
-      if (u.x < 0) break;
-      const int bh = u.y;
-      const int qt0 = ((int)gridDim.x - 1 - u.x) * 2 * C::BM + t * C::BM;
+      if (!u.live) break;
+      const int qt0 = u.q0 + t * C::BM;
       const int q_idx = qt0 + row;
-      const int n_kv_all = n_keys(qt0);
+      const int nk = VARLEN ? u.nk : p.Nk, nq = VARLEN ? u.nq : p.Nq;  // (dense: kernel parameters)
+      const int n_kv_all = n_keys(qt0, nk);
       float m = -INFINITY, l = 0.f, lr = 0.f;
       int n_kv = 0;
       for (; n_kv < n_kv_all; ++n_kv, ++ns) {
@@ -929,8 +1006,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         reg_tie(s[2]);
         reg_tie(s[3]);
         const int ka = n_kv * C::BN;
-        if ((ka + C::BN > p.Nk) || (CAUSAL && (ka + C::BN - 1 > qt0))) {
-          int lim = p.Nk - 1 - ka;  // last visible column of this tile
+        if ((ka + C::BN > nk) || (CAUSAL && (ka + C::BN - 1 > qt0))) {
+          int lim = nk - 1 - ka;  // last visible column of this tile
           if (CAUSAL) lim = min(lim, q_idx - ka);
 #pragma unroll
           for (int g = 0; g < 4; ++g)
@@ -993,6 +1070,27 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&bars[C::B_PF + t]);
       }
+      if (VARLEN) {
+        // packed layout: O row by row (a bulk store of a tile would run into the next
+        // sequence); the next unit's P V overwrites O only after this tile's P is ready
+        bool go = named_bar_and(1 + t, 128, ok && warp_wait(&bars[C::B_O + t], (ns - 1) & 1, wc, 8));
+        if (go) {
+          tc_fence_after();
+          const float inv_l = 1.f / lr;
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + ((size_t)(u.q_tok + q_idx) * p.va.H + u.z) * D;
+#pragma unroll
+          for (int g = 0; g < D / 16; ++g) {
+            uint32_t o[16];
+            tmem_ld16(t_o + g * 16, o);
+            tmem_wait_ld(o);
+            if (q_idx < nq) store16_bf16(orow + g * 16, o, inv_l);
+          }
+          if (q_idx < nq)
+            p.lse[(size_t)u.z * p.va.total_q + u.q_tok + q_idx] = (m + log2f(l)) * 0.69314718055994530942f;
+        }
+        ok = ok && go;
+        continue;
+      }
       // epilogue: O through the staging tile, which tile 0 takes after tile 1's store of the
       // previous unit has read it and tile 1 after tile 0's store of this unit
       bool go = ok && warp_wait(&bars[C::B_O + t], (ns - 1) & 1, wc, 8);
@@ -1006,15 +1104,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
       named_bar_sync(1 + t, 128);
       if (row == 0) {
-        if (go && qt0 < p.Nq) {
+        if (go && qt0 < nq) {
           for (int c = 0; c < C::NCHUNK; ++c)
-            tma_store_3d(&tm_o, smem + C::OFF_STG + c * C::CHUNK_BYTES, c * C::CHUNK, qt0, bh);
+            tma_store_3d(&tm_o, smem + C::OFF_STG + c * C::CHUNK_BYTES, c * C::CHUNK, qt0, u.z);
           bulk_commit_group();
           bulk_wait_read_all();
         }
         mbar_arrive(&bars[t == 0 ? C::B_STG : C::B_STG1]);  // the other tile may take the staging tile
       }
-      if (go && q_idx < p.Nq) p.lse[(size_t)bh * p.Nq + q_idx] = (m + log2f(l)) * 0.69314718055994530942f;
+      if (go && q_idx < nq) p.lse[(size_t)u.z * nq + q_idx] = (m + log2f(l)) * 0.69314718055994530942f;
       ok = ok && go;
     }
   }
@@ -1406,14 +1504,15 @@ cudaError_t launch_seq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN = false>
 cudaError_t launch_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                              const FwdParams& p, int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = fwd_persist_kernel<D, CAUSAL>;
+  auto kern = fwd_persist_kernel<D, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH);
+  dim3 grid = VARLEN ? dim3((unsigned)((p.va.total_q >> 8) + p.va.B), (unsigned)p.va.H)
+                     : dim3((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
@@ -1427,7 +1526,8 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   if (e != cudaSuccess) return e;
   const int n_pairs = (p.n_q_tiles + 1) / 2;
   const int gx = (LOCAL && p.n_gp > 0) ? p.n_gp * p.n_split + (n_pairs - p.n_gp) : n_pairs;
-  dim3 grid((unsigned)gx, (unsigned)BH);
+  // packed batch: compact slots of 256 queries (slot_seq), one grid row per head
+  dim3 grid = VARLEN ? dim3((unsigned)((p.va.total_q >> 8) + p.va.B), (unsigned)p.va.H) : dim3((unsigned)gx, (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
@@ -1458,6 +1558,9 @@ cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensor
     if (p.local)                                                                                 \
       return causal ? fwd::launch_t<DD, true, false, true>(tq, tk, tv, to, p, BH, st)            \
                     : fwd::launch_t<DD, false, false, true>(tq, tk, tv, to, p, BH, st);          \
+    if (p.va.cu_q && p.persist)                                                                  \
+      return causal ? fwd::launch_persist_t<DD, true, true>(tq, tk, tv, to, p, BH, st)           \
+                    : fwd::launch_persist_t<DD, false, true>(tq, tk, tv, to, p, BH, st);         \
     if (p.va.cu_q)                                                                               \
       return causal ? fwd::launch_t<DD, true, true>(tq, tk, tv, to, p, BH, st)                   \
                     : fwd::launch_t<DD, false, true>(tq, tk, tv, to, p, BH, st);                 \

@@ -527,6 +527,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 16 fp32 values (as bits) times mul, rounded to bf16 and stored as two 16-byte words.
+__device__ __forceinline__ void store16_bf16(__nv_bfloat16* dst, const uint32_t (&v)[16], float mul) {
+  uint4 w0, w1;
+  w0.x = pack_bf16(__uint_as_float(v[0]) * mul, __uint_as_float(v[1]) * mul);
+  w0.y = pack_bf16(__uint_as_float(v[2]) * mul, __uint_as_float(v[3]) * mul);
+  w0.z = pack_bf16(__uint_as_float(v[4]) * mul, __uint_as_float(v[5]) * mul);
+  w0.w = pack_bf16(__uint_as_float(v[6]) * mul, __uint_as_float(v[7]) * mul);
+  w1.x = pack_bf16(__uint_as_float(v[8]) * mul, __uint_as_float(v[9]) * mul);
+  w1.y = pack_bf16(__uint_as_float(v[10]) * mul, __uint_as_float(v[11]) * mul);
+  w1.z = pack_bf16(__uint_as_float(v[12]) * mul, __uint_as_float(v[13]) * mul);
+  w1.w = pack_bf16(__uint_as_float(v[14]) * mul, __uint_as_float(v[15]) * mul);
+  reinterpret_cast<uint4*>(dst)[0] = w0;
+  reinterpret_cast<uint4*>(dst)[1] = w1;
+}
+
 // Four floats -> four e4m3 bytes (round to nearest even, saturating), a in the low byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
   uint32_t r;
