@@ -357,8 +357,8 @@ def test_persistent_forward_equals_one_cta_per_unit(p):
 
 
 # more (key tile, head) units than SMs: the backward's main kernel runs persistent CTAs
-# by default; (4, 16, 1000, 1500, 16, causal) has key tiles past the last query, which
-# keep one CTA per unit
+# by default; (4, 16, 1000, 1500, 16, causal) has key tiles past the last query, whose
+# dK, dV rows the persistent kernel's producer sets to zero
 PERSIST_BWD_CASES = [I.Problem(2, 16, 2048, 2048, 128, True), I.Problem(2, 16, 2048, 2048, 64, False),
                      I.Problem(4, 16, 1100, 1100, 32, True), I.Problem(4, 16, 1000, 1500, 16, True),
                      I.Problem(4, 16, 1500, 1000, 128, False), I.Problem(8, 32, 300, 300, 64, True),

@@ -121,47 +121,60 @@ def test_thousands_of_sequences():
     check_varlen(lens, lens, 2, 64, True, seed=15)
 
 
-# more (slot, head) units than SMs: the forward runs persistent CTAs by default
+# more (slot, head) units than SMs: forward and backward run persistent CTAs by default
 PERSIST_VARLEN = [(MIX, MIX, 16, 128, True), (MIX, MIX, 16, 64, False),
                   ([0, 5, 0, 130, 64, 0], [0, 5, 7, 130, 0, 3], 40, 32, True),
+                  ([200, 77, 1, 513], [77, 200, 300, 129], 40, 16, True),
                   (I.doc_lengths(4096, seed=9), I.doc_lengths(4096, seed=9), 8, 128, True)]
 
 
 @pytest.mark.parametrize("case", PERSIST_VARLEN, ids=[f"H{c[2]}D{c[3]}{'c' if c[4] else 'n'}-{i}"
                                                       for i, c in enumerate(PERSIST_VARLEN)])
-def test_persistent_forward_equals_one_cta_per_unit(case):
-    # the persistent schedule changes which SM runs a (sequence, pair, head) unit, never its
-    # arithmetic: O and L bitwise equal to one CTA per slot, and both match the oracle
+def test_persistent_equals_one_cta_per_unit(case):
+    # the persistent schedule changes which SM runs a unit, never its arithmetic: O, L, dK
+    # and dV bitwise equal to one CTA per slot, dQ equal up to the order in which key tiles
+    # add into it, and all of them match the oracle
     lens_q, lens_k, H, D, causal = case
     q, k, v, do, cu_q, cu_k = I.draw_varlen(lens_q, lens_k, H, D, 17, 1.0)
-    assert (sum(lens_q) // 256 + len(lens_q)) * H > 152
+    assert (sum(lens_q) // 256 + len(lens_q)) * H > 152 and (sum(lens_k) // 128 + len(lens_k)) * H > 152
     dev = torch.device("cuda")
-    qg, kg, vg = (t.to(dev) for t in (q, k, v))
+    qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
     cq, ck = cu_q.to(dev), cu_k.to(dev)
     mq, mk = max(max(lens_q), 1), max(max(lens_k), 1)
     scale = 1.0 / np.sqrt(D)
     outs = []
-    prev = _lib.fa_set_fwd_persistent(False)
+    prev = (_lib.fa_set_fwd_persistent(False), _lib.fa_set_bwd_persistent(False))
     try:
         for on in (False, True):
             _lib.fa_set_fwd_persistent(on)
+            _lib.fa_set_bwd_persistent(on)
             o = torch.full_like(qg, float("nan"))
             lse = torch.full((H, q.shape[0]), float("nan"), dtype=torch.float32, device=dev)
             _lib.fa_fwd_varlen(qg, kg, vg, o, lse, cq, ck, mq, mk, causal, scale)
-            outs.append((o, lse))
+            dq, dk, dv = (torch.full_like(t, float("nan")) for t in (qg, kg, vg))
+            _lib.fa_bwd_varlen(qg, kg, vg, o, lse, dog, dq, dk, dv, cq, ck, mq, mk, causal, scale)
+            outs.append((o, lse, dq, dk, dv))
         torch.cuda.synchronize()
     finally:
-        _lib.fa_set_fwd_persistent(prev)
-    (o1, l1), (o2, l2) = outs
+        _lib.fa_set_fwd_persistent(prev[0])
+        _lib.fa_set_bwd_persistent(prev[1])
+    (o1, l1, dq1, dk1, dv1), (o2, l2, dq2, dk2, dv2) = outs
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    err = (dq1.float() - dq2.float()).abs().max().item()
+    assert err <= 1e-2 * max(dq1.float().abs().max().item(), 1e-30), err
     qd, kd, vd, dod = (I.as_f64(t) for t in (q, k, v, do))
-    ro, rl, _, _, _ = oracle.attention_varlen(qd, kd, vd, dod, cu_q.numpy(), cu_k.numpy(), scale, causal)
-    assert_close(f"H{H}D{D} O", f64(o2), ro)
+    ro, rl, rdq, rdk, rdv = oracle.attention_varlen(qd, kd, vd, dod, cu_q.numpy(), cu_k.numpy(), scale, causal)
+    tag = f"H{H}D{D}"
+    assert_close(tag + " O", f64(o2), ro)
     gl = f64(l2)
     fin = np.isfinite(rl)
     assert np.array_equal(np.isneginf(gl), ~fin)
     if fin.any():
         assert np.abs(gl[fin] - rl[fin]).max() <= LSE_ABS
+    assert_close(tag + " dQ", f64(dq2), rdq)
+    assert_close(tag + " dK", f64(dk2), rdk)
+    assert_close(tag + " dV", f64(dv2), rdv)
 
 
 def test_scaled_inputs_peaked_softmax():

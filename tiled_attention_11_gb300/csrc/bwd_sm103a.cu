@@ -90,9 +90,10 @@ struct Cfg {
   static constexpr int B_CLC = B_UE + NU;
   static constexpr int NBAR = B_CLC + 1;
   static constexpr int OFF_CLC = OFF_BAR + ((NBAR * 8 + 16 + 15) / 16) * 16;  // 16-byte launch-control answer
-  static constexpr int OFF_UNITS = OFF_CLC + 16;                               // NU x int2 work units
-  static constexpr int SMEM_USED = OFF_UNITS + NU * 8;
+  static constexpr int OFF_UNITS = OFF_CLC + 16;                               // NU x 32-byte work units
+  static constexpr int SMEM_USED = OFF_UNITS + NU * 32;
   static constexpr int SMEM_ALLOC = (SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024) + 1024;
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
   // warps 0-3: dQ warpgroup, 4-11: two compute warpgroups, 12: TMA producer,
   // 13: UMMA issuer for S^T, dP^T (and TMEM allocator), 14: UMMA issuer for dV, dK, dQ^T
   static constexpr int THREADS = 480;
@@ -559,8 +560,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 }
 
 // ------------------------------------------------------------------------------------
-// Persistent form of bwd_kernel for the dense layout with the plain masks.  The grid still
-// has one CTA per (128-key tile, batch*head) in the same order, but a running CTA takes
+// Persistent form of bwd_kernel for the plain masks, dense or packed.  The grid still has
+// one CTA per (128-key tile, batch*head) in the same order (packed: one per compact slot
+// and head, see slot_seq), but a running CTA takes
 // over the next CTA that has not started (cluster launch control) instead of exiting, and
 // its pipelines run on across units: K / V of the next unit are loaded once the current
 // unit's last S^T and dP^T and its K^T build have read the old ones, K^T is rebuilt in TMEM once the last
@@ -568,9 +570,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 // warps are still in the current unit's epilogue (its dK / dV accumulate from zero once
 // that epilogue has read the old ones out of TMEM).  Step-indexed barrier phases count
 // steps over all units (g = the unit's first global step + it); unit-indexed ones count
-// units.  Roles, arithmetic and per-step order are those of bwd_kernel.
+// units.  Roles, arithmetic and per-step order are those of bwd_kernel.  The producer
+// resolves each CTA index into a unit (packed: passing over slots past a sequence's keys)
+// and itself writes dK = dV = 0 for a key tile that no query step sees.
 // ------------------------------------------------------------------------------------
-template <int D, bool CAUSAL>
+// A unit as the producer publishes it: keys [k0, k0 + 128) of one (sequence, head).  Dense:
+// z = batch*head, q_tok = k_tok = b = 0, nq = Nq, nk = Nk; packed: z = head, q_tok / k_tok
+// the sequence's first tokens, nq / nk its lengths, b its index.  live = 0 ends the ring.
+struct BwdUnit {
+  int k0, z, q_tok, k_tok, nq, nk, b, live;
+};
+
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     bwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -583,14 +594,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   void* clc_resp = smem + C::OFF_CLC;
-  int2* units = reinterpret_cast<int2*>(smem + C::OFF_UNITS);
+  BwdUnit* units = reinterpret_cast<BwdUnit*>(smem + C::OFF_UNITS);
 
   const int warp = (int)warp_id(), lane = (int)lane_id();
-  const int n_qt = (p.Nq + C::BM - 1) / C::BM;
-  // query steps of key tile kt: causal ones start at the diagonal
-  // (the host launches this kernel only when every key tile has at least one step)
-  auto first_step = [&](int kt) { return CAUSAL ? (kt * C::BN) / C::BM : 0; };
-  auto n_steps = [&](int kt) { return n_qt - first_step(kt); };
+  // query steps of a unit: causal ones start at the diagonal; a published unit has one at least
+  auto first_step = [&](const BwdUnit& u) { return CAUSAL ? u.k0 / C::BM : 0; };
+  auto n_steps = [&](const BwdUnit& u) { return (u.nq + C::BM - 1) / C::BM - first_step(u); };
+  // first workspace row of the unit's (sequence, head)
+  auto wrow0 = [&](const BwdUnit& u) -> long long {
+    return VARLEN ? (long long)u.z * p.Nq_pad + 64LL * ((u.q_tok + 63) / 64 + u.b) : (long long)u.z * p.Nq_pad;
+  };
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
 
   if (threadIdx.x == 0) {
@@ -639,37 +652,97 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
     }
-    int ux = (int)blockIdx.x, uy = (int)blockIdx.y;  // the unit to publish next (ux < 0: none)
+    int ux = (int)blockIdx.x, uy = (int)blockIdx.y;  // the CTA index to work on next (ux < 0: none)
     int g0 = 0, issued = 0, kv_units = 0;  // the unit's first global step; steps / K,V pairs started
     bool asked = false;
     int n_asked = 0;
+    // take over the next CTA of the grid that has not started (ux = -1: none is left)
+    auto claim = [&]() -> bool {
+      mbar_arrive_expect_tx_w(&bars[C::B_CLC], 16);
+      clc_try_cancel_w(clc_resp, &bars[C::B_CLC]);
+      asked = true;
+      if (!mbar_wait_w(&bars[C::B_CLC], n_asked & 1, wc, 52)) return false;
+      asked = false;
+      ++n_asked;
+      int cx, cy;
+      const bool taken = clc_taken(clc_resp, cx, cy);
+      ux = (taken && cx >= 0 && cx < (int)gridDim.x && cy >= 0 && cy < (int)gridDim.y) ? cx : -1;
+      uy = cy;
+      return true;
+    };
+    // the unit of CTA (ux, uy); false when it has nothing for the pipeline (packed: a slot past
+    // its sequence's keys; either layout: a key tile no query sees, whose dK, dV rows get
+    // zeros here)
+    auto resolve = [&](BwdUnit& un) -> bool {
+      un.live = 1;
+      if (!VARLEN) {
+        un.k0 = ux * C::BN;
+        un.z = uy;
+        un.q_tok = un.k_tok = un.b = 0;
+        un.nq = p.Nq;
+        un.nk = p.Nk;
+      } else {
+        const int b = slot_seq(p.va.cu_k, p.va.B, p.va.total_k, 7, ux);
+        const int kt = ux - slot_base(p.va.cu_k, p.va.total_k, 7, b);
+        const SeqView sv = seq_view<true>(p.va, p.Nq, p.Nk, b * p.va.H + uy);
+        if (kt * C::BN >= sv.Nk) return false;
+        un.k0 = kt * C::BN;
+        un.z = uy;
+        un.q_tok = sv.q_tok;
+        un.k_tok = sv.k_tok;
+        un.nq = sv.Nq;
+        un.nk = sv.Nk;
+        un.b = b;
+      }
+      if (n_steps(un) > 0) return true;
+      const int r1 = min(un.k0 + C::BN, un.nk);
+      for (int e = lane; e < (r1 - un.k0) * (D / 8); e += 32) {
+        const int key = un.k0 + e / (D / 8);
+        const size_t off = VARLEN ? ((size_t)(un.k_tok + key) * p.va.H + un.z) * D : ((size_t)un.z * p.Nk + key) * D;
+        reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dk) + off)[e % (D / 8)] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dv) + off)[e % (D / 8)] = make_uint4(0, 0, 0, 0);
+      }
+      return false;
+    };
     for (int u = 0;; ++u) {
+      BwdUnit un;
+      un.live = 0;
+      bool ok = true;
+      while (ux >= 0 && !resolve(un))
+        if (!(ok = claim())) break;
+      if (!ok) break;
+      if (ux < 0) un.live = 0;
       const int us = u % C::NU;
       if (u >= C::NU && !mbar_wait_w(&bars[C::B_UE + us], ((u / C::NU) - 1) & 1, wc, 50)) break;
-      units[us] = make_int2(ux, uy);
+      units[us] = un;  // (every lane holds the same record)
       mbar_arrive_w(&bars[C::B_UF + us]);
-      if (ux < 0) break;
-      const int kt = ux, bh = uy, k0 = kt * C::BN, i0 = first_step(kt), n_it = n_steps(kt);
-      // K / V: free once the previous unit's last S^T and dP^T have read them
+      if (!un.live) break;
+      const int k0 = un.k0, i0 = first_step(un), n_it = n_steps(un);
+      const long long w0 = wrow0(un);
+      // TMA coordinates of row r: dense maps [B*H][N][D] (y = row, z = batch*head), packed
+      // maps [total][H][D] (y = head, z = token)
+      auto ty = [&](int r) { return VARLEN ? un.z : r; };
+      auto tzq = [&](int r) { return VARLEN ? un.q_tok + r : un.z; };
+      auto tzk = [&](int r) { return VARLEN ? un.k_tok + r : un.z; };
+      // K / V: free once the previous unit's last S^T and dP^T and its K^T build have read them
       if (u >= 1 && !mbar_wait_w(&bars[C::B_KVE], (u - 1) & 1, wc, 51)) break;
       mbar_arrive_expect_tx_w(&bars[C::B_KV], 2 * C::KV_TILE);
       for (int c = 0; c < C::NCHUNK; ++c) {
-        tma_load_3d_w(smem + C::OFF_K + c * C::K_CHUNK_BYTES, &tm_k, &bars[C::B_KV], c * C::CHUNK, k0, bh);
-        tma_load_3d_w(smem + C::OFF_V + c * C::K_CHUNK_BYTES, &tm_v, &bars[C::B_KV], c * C::CHUNK, k0, bh);
+        tma_load_3d_w(smem + C::OFF_K + c * C::K_CHUNK_BYTES, &tm_k, &bars[C::B_KV], c * C::CHUNK, ty(k0), tzk(k0));
+        tma_load_3d_w(smem + C::OFF_V + c * C::K_CHUNK_BYTES, &tm_v, &bars[C::B_KV], c * C::CHUNK, ty(k0), tzk(k0));
       }
       kv_units = u + 1;
-      bool ok = true;
       for (int it = 0; it < n_it; ++it) {
         const int g = g0 + it, s = g % C::NS, i = i0 + it;
         if (g >= C::NS && !(ok = mbar_wait_w(&bars[C::B_QE + s], ((g / C::NS) - 1) & 1, wc, 31))) break;
         mbar_arrive_expect_tx_w(&bars[C::B_QF + s], 2 * C::Q_TILE + 2 * C::BM * 4);
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_load_3d_w(smem + C::OFF_Q + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_q, &bars[C::B_QF + s],
-                        c * C::CHUNK, i * C::BM, bh);
+                        c * C::CHUNK, ty(i * C::BM), tzq(i * C::BM));
           tma_load_3d_w(smem + C::OFF_DO + s * C::Q_TILE + c * C::Q_CHUNK_BYTES, &tm_do, &bars[C::B_QF + s],
-                        c * C::CHUNK, i * C::BM, bh);
+                        c * C::CHUNK, ty(i * C::BM), tzq(i * C::BM));
         }
-        const size_t roff = (size_t)bh * p.Nq_pad + (size_t)i * C::BM;
+        const size_t roff = (size_t)w0 + (size_t)i * C::BM;
         bulk_load_w(smem + C::OFF_LSE + s * C::BM * 4, p.lse2 + roff, C::BM * 4, &bars[C::B_QF + s]);
         bulk_load_w(smem + C::OFF_DLT + s * C::BM * 4, p.dlt + roff, C::BM * 4, &bars[C::B_QF + s]);
         issued = g + 1;
@@ -677,16 +750,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       if (!ok) break;
       g0 += n_it;
       // the next unit, asked for once this unit's last copies are started
-      mbar_arrive_expect_tx_w(&bars[C::B_CLC], 16);
-      clc_try_cancel_w(clc_resp, &bars[C::B_CLC]);
-      asked = true;
-      if (!mbar_wait_w(&bars[C::B_CLC], n_asked & 1, wc, 52)) break;
-      asked = false;
-      ++n_asked;
-      int cx, cy;
-      const bool taken = clc_taken(clc_resp, cx, cy);
-      ux = (taken && cx >= 0 && cx < (int)gridDim.x && cy >= 0 && cy < (int)gridDim.y) ? cx : -1;
-      uy = cy;
+      if (!claim()) break;
     }
     if (__any_sync(0xffffffffu, *abort_flag != 0)) {
       volatile int no_abort = 0;
@@ -729,10 +793,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     for (int u = 0; ok; ++u) {
       const int us = u % C::NU;
       if (!(ok = mbar_wait_w(&bars[C::B_UF + us], (u / C::NU) & 1, wc, 54))) break;
-      const int2 un = units[us];
+      const BwdUnit un = units[us];
       mbar_arrive_w(&bars[C::B_UE + us]);
-      if (un.x < 0) break;
-      const int n_it = n_steps(un.x);
+      if (!un.live) break;
+      const int n_it = n_steps(un);
       if (!(ok = mbar_wait_w(&bars[C::B_KV], u & 1, wc, 32) && s_ready(g0))) break;
       tc_fence_after();
       issue_s(g0);
@@ -766,10 +830,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     for (int u = 0; ok; ++u) {
       const int us = u % C::NU;
       if (!(ok = mbar_wait_w(&bars[C::B_UF + us], (u / C::NU) & 1, wc, 55))) break;
-      const int2 un = units[us];
+      const BwdUnit un = units[us];
       mbar_arrive_w(&bars[C::B_UE + us]);
-      if (un.x < 0) break;
-      const int n_it = n_steps(un.x);
+      if (!un.live) break;
+      const int n_it = n_steps(un);
       // dV and dK start from zero: the previous unit's epilogue must have read them out
       if (u >= 1 && !(ok = mbar_wait_w(&bars[C::B_ACCE], (u - 1) & 1, wc, 56))) break;
       for (int it = 0; ok && it < n_it; ++it) {
@@ -820,11 +884,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     for (int u = 0;; ++u) {
       const int us = u % C::NU;
       if (!(ok = ok && warp_wait(&bars[C::B_UF + us], (u / C::NU) & 1, wc, 57))) break;
-      const int2 un = units[us];
+      const BwdUnit un = units[us];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
-      if (un.x < 0) break;
-      const int kt = un.x, bh = un.y, k0 = kt * C::BN, key = k0 + row, i0 = first_step(kt), n_it = n_steps(kt);
+      if (!un.live) break;
+      const int k0 = un.k0, key = k0 + row, i0 = first_step(un), n_it = n_steps(un);
+      const int nk = VARLEN ? un.nk : p.Nk;  // (dense: the kernel parameter)
       for (int it = 0; it < n_it && ok; ++it) {
         const int g = g0 + it, s = g % C::NS, i = i0 + it;
         const uint32_t t_sb = (uint32_t)((g & 1) * 64);  // this step's S^T / P^T buffer
@@ -840,9 +905,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * C::BM * 4) + col0;
         const float* dlt = reinterpret_cast<const float*>(smem + C::OFF_DLT + s * C::BM * 4) + col0;
         const int qb = i * C::BM + col0;  // query of column 0 of this warpgroup's half
-        const bool need_mask = (k0 + C::BN > p.Nk) || (CAUSAL && (k0 + C::BN - 1 > qb));
+        const bool need_mask = (k0 + C::BN > nk) || (CAUSAL && (k0 + C::BN - 1 > qb));
         const int lim = CAUSAL ? key - qb : (1 << 30);  // columns c with q = qb + c < key are masked
-        const bool key_valid = key < p.Nk;
+        const bool key_valid = key < nk;
         float pv[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -896,14 +961,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       g0 += n_it;
       if (!(ok = ok && warp_wait(&bars[C::B_DQF + (gl & 1)], (gl >> 1) & 1, wc, 45))) break;
       tc_fence_after();
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) + ((size_t)bh * p.Nk + key) * D;
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) +
+                           (VARLEN ? ((size_t)(un.k_tok + key) * p.va.H + un.z) * D : ((size_t)un.z * p.Nk + key) * D);
       const float mul = (wg == 0) ? p.scale : 1.f;
 #pragma unroll
       for (int gg = 0; gg < D / 16; ++gg) {
         uint32_t v[16];
         tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + gg * 16, v);
         tmem_wait_ld(v);
-        if (key < p.Nk) store16_bf16(dst + gg * 16, v, mul);
+        if (key < nk) store16_bf16(dst + gg * 16, v, mul);
       }
       tc_fence_before();
       mbar_arrive(&bars[C::B_ACCE]);
@@ -919,11 +985,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       // the four warps agree before any of them reaches the named barriers below
       const int us = u % C::NU;
       if (!named_bar_and(1, 128, ok && warp_wait(&bars[C::B_UF + us], (u / C::NU) & 1, wc, 58))) break;
-      const int2 un = units[us];
+      const BwdUnit un = units[us];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
-      if (un.x < 0) break;
-      const int kt = un.x, bh = un.y, i0 = first_step(kt), n_it = n_steps(kt);
+      if (!un.live) break;
+      const int i0 = first_step(un), n_it = n_steps(un);
+      const long long w0 = wrow0(un);
       // K^T into TMEM for this unit (lane d holds K[key][d] for all 128 keys as bf16 pairs,
       // lanes d >= D zeros) once K has landed and the previous unit's dQ^T MMAs are done
       ok = named_bar_and(1, 128, warp_wait(&bars[C::B_KV], u & 1, wc, 48) &&
@@ -968,7 +1035,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         reg_tie(v1);
         tc_fence_before();
         mbar_arrive(&bars[C::B_DQE + b]);
-        float* gdst = p.dq_accum + ((size_t)bh * p.Nq_pad + (size_t)(i0 + it) * C::BM) * D;
+        float* gdst = p.dq_accum + ((size_t)w0 + (size_t)(i0 + it) * C::BM) * D;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -1110,14 +1177,15 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN = false>
 cudaError_t launch_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                              const BwdParams& p, int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = bwd_persist_kernel<D, CAUSAL>;
+  auto kern = bwd_persist_kernel<D, CAUSAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.n_k_tiles, (unsigned)BH);
+  dim3 grid = VARLEN ? dim3((unsigned)((p.va.total_k >> 7) + p.va.B), (unsigned)p.va.H)
+                     : dim3((unsigned)p.n_k_tiles, (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
@@ -1155,6 +1223,10 @@ cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensor
   if (p.local) {
     TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true, false, true>(tq, tk, tv, tdo, p, BH, st)
                              : bwd::launch_t<DD, false, false, true>(tq, tk, tv, tdo, p, BH, st)))
+  }
+  if (p.va.cu_q && p.persist) {
+    TA11_SWITCH_D(D, (causal ? bwd::launch_persist_t<DD, true, true>(tq, tk, tv, tdo, p, BH, st)
+                             : bwd::launch_persist_t<DD, false, true>(tq, tk, tv, tdo, p, BH, st)))
   }
   if (p.va.cu_q) {
     TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true, true>(tq, tk, tv, tdo, p, BH, st)

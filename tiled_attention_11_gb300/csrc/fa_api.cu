@@ -438,14 +438,11 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
       bp.dkv_accum = dkv_accum;
     }
   }
-  // persistent kernel: plain masks, more CTAs than one wave, every key tile with a query
-  // step (causal: the last key tile starts below Nq).  It saves a fixed time per unit;
-  // with D = 128 and more than 128 query steps per unit it measured about 1% slower than
-  // one CTA per unit, so those keep one CTA per unit.
-  const bool all_steps = !causal || (long long)(bp.n_k_tiles - 1) * 128 < Nq;
+  // persistent kernel: plain masks, more CTAs than one wave.  It saves a fixed time per
+  // unit; with D = 128 and more than 128 query steps per unit it measured about 1% slower
+  // than one CTA per unit, so those keep one CTA per unit.
   const bool short_units = D < 128 || Nq <= 8192;
-  bp.persist = (!lm && all_steps && short_units && (long long)bp.n_k_tiles * BH > current_sms())
-                   ? g_bwd_persist.load() : 0;
+  bp.persist = (!lm && short_units && (long long)bp.n_k_tiles * BH > current_sms()) ? g_bwd_persist.load() : 0;
   cudaEvent_t ev_b = nullptr, ev_e = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_ev_mu);
@@ -772,6 +769,9 @@ extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const 
   bp.wait_limit_ns = g_wait_limit_ns.load();
   bp.status = status;
   bp.va = va;
+  // persistent kernel beyond one wave of compact 128-key slots (slot_seq), as for the dense layout
+  bp.persist = ((D < 128 || max_seqlen_q <= 8192) && (long long)((total_k >> 7) + B) * H > current_sms())
+                   ? g_bwd_persist.load() : 0;
   if (ta11::launch_bwd(D, causal != 0, tq, tk, tv, tdo, bp, B * H, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   ta11::ConvParams cp{dq_accum, dq, B * H, max_seqlen_q, w.Nq_pad, scale, va};
   if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
