@@ -434,7 +434,7 @@ def quantize_e4m3_transposed(v, stream=None):
     ldt, amax, descale) with ldt = N rounded up to 16."""
     B, H, N, D = v.shape
     ldt = (N + 15) // 16 * 16
-    codes = torch.zeros((B, H, D, ldt), dtype=torch.uint8, device=v.device)
+    codes = torch.empty((B, H, D, ldt), dtype=torch.uint8, device=v.device)  # (every byte is written)
     sc = torch.empty(2, dtype=torch.float32, device=v.device)
     amax, descale = sc[0:1], sc[1:2]
     rc = lib().fa_quantize_e4m3_transposed(_ptr(v, "v", torch.bfloat16), B, H, N, D, ldt,

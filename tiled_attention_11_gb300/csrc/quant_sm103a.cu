@@ -29,6 +29,8 @@ __device__ __forceinline__ uint4 ld16(const uint4* p) { return __ldg(p); }
 
 __global__ void __launch_bounds__(256) amax_kernel(const __nv_bfloat16* __restrict__ x, long long n,
                                                    unsigned* __restrict__ amax_bits) {
+  // the quantise kernel that follows may be launched now; it waits for this grid's result
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f;
   const long long n8 = n / 8;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -75,6 +77,7 @@ __device__ __forceinline__ uint2 quant8(const uint4 w, float mult) {
 __global__ void __launch_bounds__(256) quant_kernel(const __nv_bfloat16* __restrict__ x, long long n,
                                                     const float* __restrict__ amax, uint8_t* __restrict__ codes,
                                                     float* __restrict__ descale) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the amax grid has completed
   const float a = *amax;
   const float mult = multiplier(a);
   if (blockIdx.x == 0 && threadIdx.x == 0) *descale = a > 0.f ? a / 448.f : 1.f;
@@ -98,35 +101,53 @@ __global__ void __launch_bounds__(256) quant_kernel(const __nv_bfloat16* __restr
   }
 }
 
-// x [BH][N][D] bf16 -> codes_t [BH][D][ldt]: one block per (64-key slab, head).
+// x [BH][N][D] bf16 -> codes_t [BH][D][ldt]: one block per (64-key slab, head).  A thread
+// quantises the same 8 columns of 4 consecutive keys and writes, per column, the 4 codes
+// as one 32-bit word of the transposed tile; tile rows are 72 bytes apart so the two
+// column groups a warp writes fall on different banks.  Every byte of [0, ldt) of a row is
+// written (keys past N as zero codes).
 template <int D>
 __global__ void __launch_bounds__(256) quant_t_kernel(const __nv_bfloat16* __restrict__ x, int N, int ldt,
                                                       const float* __restrict__ amax, uint8_t* __restrict__ codes_t,
                                                       float* __restrict__ descale) {
-  constexpr int KEYS = 64;
-  __shared__ __align__(16) uint8_t tile[D][KEYS];  // [d][key]
+  constexpr int KEYS = 64, ROW = KEYS + 8;  // tile row stride (bytes)
+  __shared__ __align__(16) uint8_t tile[D * ROW];  // [d][key]
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the amax grid has completed
   const float a = *amax;
   const float mult = multiplier(a);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *descale = a > 0.f ? a / 448.f : 1.f;
   const int bh = blockIdx.y;
   const int k0 = blockIdx.x * KEYS;
   const __nv_bfloat16* xs = x + ((size_t)bh * N + k0) * D;
-  // keys fastest: a warp stores 32 consecutive bytes of a tile row (no bank conflicts); the
-  // 16-byte loads of one key row are spread over warps and meet in L1
-  for (int e = threadIdx.x; e < KEYS * (D / 8); e += blockDim.x) {
-    const int key = e % KEYS, part = e / KEYS;
-    uint2 c = make_uint2(0u, 0u);  // keys past N quantise as zero
-    if (k0 + key < N) c = quant8(ld16(reinterpret_cast<const uint4*>(xs + (size_t)key * D) + part), mult);
-    const uint32_t w[2] = {c.x, c.y};
+  for (int e = threadIdx.x; e < (KEYS / 4) * (D / 8); e += blockDim.x) {
+    const int j = e % (KEYS / 4), part = e / (KEYS / 4);  // keys 4j .. 4j+3, columns 8*part ..
+    uint4 w[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) tile[part * 8 + i][key] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
+    for (int r = 0; r < 4; ++r) {
+      const int key = 4 * j + r;
+      w[r] = k0 + key < N ? ld16(reinterpret_cast<const uint4*>(xs + (size_t)key * D) + part) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint2 c[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) c[r] = quant8(w[r], mult);  // (zero input -> zero codes)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int sh = 8 * (i & 3);
+      uint32_t v = 0u;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) v |= (((i < 4 ? c[r].x : c[r].y) >> sh) & 0xffu) << (8 * r);
+      *reinterpret_cast<uint32_t*>(&tile[(part * 8 + i) * ROW + 4 * j]) = v;
+    }
   }
   __syncthreads();
   uint8_t* out = codes_t + (size_t)bh * D * ldt + k0;
   for (int e = threadIdx.x; e < D * (KEYS / 16); e += blockDim.x) {
     const int d = e / (KEYS / 16), chunk = e % (KEYS / 16);
-    if (k0 + chunk * 16 < N)  // ldt >= N rounded up to 16, so whole 16-byte chunks fit
-      *reinterpret_cast<uint4*>(out + (size_t)d * ldt + chunk * 16) = *reinterpret_cast<const uint4*>(&tile[d][chunk * 16]);
+    if (k0 + chunk * 16 < N) {  // ldt >= N rounded up to 16, so whole 16-byte chunks fit
+      const uint2* src = reinterpret_cast<const uint2*>(&tile[d * ROW + chunk * 16]);
+      const uint2 lo = src[0], hi = src[1];
+      *reinterpret_cast<uint4*>(out + (size_t)d * ldt + chunk * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
   }
 }
 
@@ -144,11 +165,29 @@ cudaError_t launch_amax_bf16(const void* x, long long n, float* amax, cudaStream
   return cudaGetLastError();
 }
 
+namespace quant {
+// Launch on `st` as a programmatic dependent of the amax kernel before it: the grid may
+// start while that one drains, and waits (griddepcontrol.wait) before it reads amax.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+}  // namespace quant
+
 cudaError_t launch_quant_e4m3(const void* x, long long n, const float* amax, void* codes, float* descale,
                               cudaStream_t st) {
-  quant::quant_kernel<<<quant::grid_for(n / 8 + 1), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), n, amax,
-                                                                   static_cast<uint8_t*>(codes), descale);
-  return cudaGetLastError();
+  return quant::launch_dependent(quant::quant_kernel, dim3((unsigned)quant::grid_for(n / 8 + 1)), st,
+                                 static_cast<const __nv_bfloat16*>(x), n, amax, static_cast<uint8_t*>(codes), descale);
 }
 
 cudaError_t launch_quant_e4m3_t(const void* x, int BH, int N, int D, int ldt, const float* amax, void* codes_t,
@@ -157,11 +196,10 @@ cudaError_t launch_quant_e4m3_t(const void* x, int BH, int N, int D, int ldt, co
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   uint8_t* c = static_cast<uint8_t*>(codes_t);
   switch (D) {
-    case 64: quant::quant_t_kernel<64><<<grid, 256, 0, st>>>(xb, N, ldt, amax, c, descale); break;
-    case 128: quant::quant_t_kernel<128><<<grid, 256, 0, st>>>(xb, N, ldt, amax, c, descale); break;
+    case 64: return quant::launch_dependent(quant::quant_t_kernel<64>, grid, st, xb, N, ldt, amax, c, descale);
+    case 128: return quant::launch_dependent(quant::quant_t_kernel<128>, grid, st, xb, N, ldt, amax, c, descale);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace ta11
