@@ -34,8 +34,10 @@ if ROOT not in sys.path:
 METRIC = "attention fwd/bwd TFLOP/s (bf16 causal H=32 N=4096 D=128), % of TC peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-BWD_SOURCES = ["tiled_attention_11_gb300/csrc/bwd_sm103a.cu", "tiled_attention_11_gb300/csrc/ptx_sm103a.cuh"]
-FWD_SOURCES = ["tiled_attention_11_gb300/csrc/fwd_sm103a.cu", "tiled_attention_11_gb300/csrc/ptx_sm103a.cuh"]
+BWD_SOURCES = ["tiled_attention_11_gb300/csrc/bwd_sm103a.cu", "tiled_attention_11_gb300/csrc/ptx_sm103a.cuh",
+               "tiled_attention_11_gb300/csrc/fa_kernels.h"]
+FWD_SOURCES = ["tiled_attention_11_gb300/csrc/fwd_sm103a.cu", "tiled_attention_11_gb300/csrc/ptx_sm103a.cuh",
+               "tiled_attention_11_gb300/csrc/fa_kernels.h"]
 
 
 # ------------------------------------------------------------------ host helpers (CPU-testable)
@@ -334,10 +336,10 @@ def run_ours(args):
     bwd_tf = flops_bwd / (bwd_ms * 1e-3) / 1e12
     main_tf = flops_bwd / (main_ms * 1e-3) / 1e12
     if main_ms >= fwd_ms:
-        dom, dom_ms, dom_flops, dom_src = "fa_bwd main kernel (bwd_kernel<128,causal>)", main_ms, flops_bwd, BWD_SOURCES
+        dom, dom_ms, dom_flops, dom_src = "fa_bwd main kernel (bwd_persist_kernel<128,causal>)", main_ms, flops_bwd, BWD_SOURCES
         traffic = traffic_for("bwd_main_layer", BWD_SOURCES)
     else:
-        dom, dom_ms, dom_flops, dom_src = "fa_fwd kernel (fwd_kernel<128,causal>)", fwd_ms, flops_fwd, FWD_SOURCES
+        dom, dom_ms, dom_flops, dom_src = "fa_fwd kernel (fwd_persist_kernel<128,causal>)", fwd_ms, flops_fwd, FWD_SOURCES
         traffic = traffic_for("fwd_layer", FWD_SOURCES)
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
 
