@@ -322,6 +322,12 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     e2e_ms = max_over_ranks(e2e_s.elapsed_time(e2e_e) / K2, dev)
+    # the host link's own rates (pinned buffers of the step's size, copy engines, best of 5):
+    # no step can move its inputs in and its outputs out faster than both directions at once
+    del lanes
+    torch.cuda.empty_cache()
+    link = link_rates(dev, h2d)
+    e2e_floor_ms = max(h2d, d2h) / (link["both_gbs"] * 1e9) * 1e3
 
     if rank != 0:
         if world > 1:
@@ -371,7 +377,9 @@ def run_ours(args):
                      "traffic": traffic, "algorithmic_flops_per_launch": dom_flops},
         "e2e": {"value": round(job_throughput(flops_step, world, e2e_ms), 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "steps": K2, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": f"fa_step_host (pinned host buffers), {len(lanes)} steps in flight on {len(lanes)} streams"},
+                "api": f"fa_step_host (pinned host buffers), {args.e2e_lanes} steps in flight on {args.e2e_lanes} streams",
+                "link_gbs": link, "floor_ms": round(e2e_floor_ms, 4),
+                "frac_of_floor": round(e2e_floor_ms / e2e_ms, 4)},
         "gpu_launches": 4 * K,
         "clocks": clk,
     }
@@ -384,6 +392,52 @@ def run_ours(args):
     print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def link_rates(dev, nbytes: int) -> dict:
+    """Host <-> device copy rates (GB/s) for pinned buffers of nbytes: host to device,
+    device to host, and each direction while both run at once (two streams)."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def best(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s1)
+            fn()
+            e1.record(s1)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return min(ts)
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s1):
+            h_out.copy_(d_out, non_blocking=True)
+
+    def both():
+        s2.wait_stream(s1)
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+        s1.wait_stream(s2)
+
+    r = {k: round(nbytes / (best(f) * 1e-3) / 1e9, 1) for k, f in (("h2d_gbs", h2d), ("d2h_gbs", d2h),
+                                                                 ("both_gbs", both))}
+    del h_in, h_out, d_in, d_out
+    torch.cuda.empty_cache()
+    return r
 
 
 # ------------------------------------------------------------------ per-workload table

@@ -154,3 +154,43 @@ def test_fp8_long_sampled_rows():
         r, a = err(o[0, h][rows], ro)
         assert r <= REL_L2 and a <= MAX_FRAC, f"h{h}: rel {r:.3e} frac {a:.3e}"
         assert np.abs(lse[0, h][rows] - rl).max() <= LSE_ABS
+
+
+# more (query-tile pair, head) units than SMs: the FP8 forward runs persistent CTAs by default
+PERSIST_CASES = [I.Problem(2, 16, 2048, 2048, 128, True), I.Problem(4, 16, 1100, 1100, 64, False),
+                 I.Problem(8, 32, 300, 300, 128, True), I.Problem(4, 16, 700, 1500, 64, True)]
+
+
+@pytest.mark.parametrize("p", PERSIST_CASES, ids=[p.name() for p in PERSIST_CASES])
+def test_fp8_persistent_equals_one_cta_per_unit(p):
+    # the persistent schedule changes which SM runs a unit, never its arithmetic: O and L
+    # bitwise equal to one CTA per unit, and the oracle agrees on the first and last head
+    assert p.B * p.H * ((p.Nq + 255) // 256) > 152
+    q, k, v, _ = I.draw(p, 19)
+    (q8, qd), (k8, kd), (v8, vd) = oracle_codes(q), oracle_codes(k), oracle_codes(v)
+    dev = torch.device("cuda")
+    ldv = (p.Nk + 15) // 16 * 16
+    vt = np.zeros((p.B, p.H, p.D, ldv), np.uint8)
+    vt[..., :p.Nk] = v8.transpose(0, 1, 3, 2)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    sc = lambda d: torch.tensor([d], dtype=torch.float32, device=dev)  # noqa: E731
+    args = (t(q8), t(k8), t(vt), ldv, sc(qd), sc(kd), sc(vd))
+    outs = []
+    prev = _lib.fa_set_fwd_persistent(False)
+    try:
+        for on in (False, True):
+            _lib.fa_set_fwd_persistent(on)
+            o = torch.full((p.B, p.H, p.Nq, p.D), float("nan"), dtype=torch.bfloat16, device=dev)
+            lse = torch.full((p.B, p.H, p.Nq), float("nan"), dtype=torch.float32, device=dev)
+            _lib.fa_fwd_fp8(*args, o, lse, p.causal, p.scale)
+            outs.append((o, lse))
+        torch.cuda.synchronize()
+    finally:
+        _lib.fa_set_fwd_persistent(prev)
+    (o1, l1), (o2, l2) = outs
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for (b, h) in ((0, 0), (p.B - 1, p.H - 1)):
+        ro, rl = fp8_ref.forward_head(q8[b, h], k8[b, h], v8[b, h], qd, kd, vd, p.scale, p.causal)
+        r, a = err(f64(o2[b, h]), ro)
+        assert r <= REL_L2 and a <= MAX_FRAC, f"{p.name()} b{b}h{h}: rel {r:.3e} frac {a:.3e}"
+        assert np.abs(f64(l2[b, h]) - rl).max() <= LSE_ABS

@@ -220,6 +220,8 @@ struct Fp8FwdParams {
   const float* v_descale;
   unsigned long long wait_limit_ns;
   unsigned* status;
+  // more (query-tile pair, head) units than one wave: the persistent kernel
+  int persist;
 };
 
 // Host launchers (return cudaError_t of the launch).
