@@ -1072,28 +1072,41 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 template <int D>
 struct RowCfg {
   static constexpr int TPR = D / 8;          // threads per row, 8 bf16 each
-  static constexpr int ROWS = 256 / TPR;     // rows per 256-thread block
+  static constexpr int ROWS = 256 / TPR;     // rows per pass of a 256-thread block
+  static constexpr int NSUB = ROWS < 64 ? 64 / ROWS : 1;  // passes per block
+  static constexpr int ROWS_CTA = ROWS * NSUB;             // rows per block, a multiple of 64
 };
 
 template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
-  constexpr int TPR = RowCfg<D>::TPR;
+  using R = RowCfg<D>;
+  constexpr int TPR = R::TPR;
   const int bh = blockIdx.y;
   const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nq, bh);
   const int rows = VARLEN ? (sv.Nq + 63) / 64 * 64 : p.Nq_pad;  // padded rows of this sequence
+  const int rb = blockIdx.x * R::ROWS_CTA;                       // first row of this block
+  if (rb >= rows) return;  // (packed: a sequence shorter than the longest)
   const long long row0 = ws_row0(VARLEN, bh, p.Nq_pad, sv);
-  const int r = blockIdx.x * RowCfg<D>::ROWS + threadIdx.x / TPR;
   const int part = threadIdx.x % TPR;
-  const bool active = r < rows;
-  const bool valid = active && r < sv.Nq;
-  const size_t tok = VARLEN ? ((size_t)(sv.q_tok + r) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + r);
-  float acc = 0.f;
-  if (valid) {
-    const size_t off = tok * D + part * 8;
-    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.o) + off);
-    const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dout) + off);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  // every pass's loads first, so NSUB 16-byte loads per tensor are in flight per thread
+  uint4 a[R::NSUB], b[R::NSUB];
+#pragma unroll
+  for (int k = 0; k < R::NSUB; ++k) {
+    const int r = rb + k * R::ROWS + threadIdx.x / TPR;
+    a[k] = b[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < sv.Nq) {
+      const size_t tok = VARLEN ? ((size_t)(sv.q_tok + r) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + r);
+      const size_t off = tok * D + part * 8;
+      a[k] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.o) + off);
+      b[k] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.dout) + off);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < R::NSUB; ++k) {
+    const int r = rb + k * R::ROWS + threadIdx.x / TPR;
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[k]);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[k]);
+    float acc = 0.f;  // (zero words for rows past the sequence)
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const float2 fa = __bfloat1622float2(a2[t]);
@@ -1101,19 +1114,19 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
       acc = fmaf(fa.x, fb.x, acc);
       acc = fmaf(fa.y, fb.y, acc);
     }
-  }
 #pragma unroll
-  for (int w = TPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-  if (active) {
-    const size_t wr = (size_t)(row0 + r);
-    float4* z = reinterpret_cast<float4*>(p.dq_accum + wr * D + part * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (part == 0) {
-      p.dlt[wr] = acc;
-      const size_t li = VARLEN ? (size_t)sv.h * p.va.total_q + sv.q_tok + r : (size_t)bh * sv.Nq + r;
-      const float L = valid ? p.lse[li] : -INFINITY;  // -inf: the row sees no key
-      p.lse2[wr] = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
+    for (int w = TPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (r < rows) {
+      const size_t wr = (size_t)(row0 + r);
+      float4* z = reinterpret_cast<float4*>(p.dq_accum + wr * D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (part == 0) {
+        p.dlt[wr] = acc;
+        const size_t li = VARLEN ? (size_t)sv.h * p.va.total_q + sv.q_tok + r : (size_t)bh * sv.Nq + r;
+        const float L = r < sv.Nq ? p.lse[li] : -INFINITY;  // -inf: the row sees no key
+        p.lse2[wr] = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
+      }
     }
   }
 }
@@ -1123,22 +1136,37 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
 // ------------------------------------------------------------------------------------
 template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) convert_kernel(const ConvParams p) {
-  constexpr int TPR = RowCfg<D>::TPR;
+  using R = RowCfg<D>;
+  constexpr int TPR = R::TPR;
   const int bh = blockIdx.y;
   const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nq, bh);
-  const int r = blockIdx.x * RowCfg<D>::ROWS + threadIdx.x / TPR;
-  if (r >= sv.Nq) return;
+  const int rb = blockIdx.x * R::ROWS_CTA;
+  if (rb >= sv.Nq) return;
   const int d = (threadIdx.x % TPR) * 8;
   const long long row0 = ws_row0(VARLEN, bh, p.Nq_pad, sv);
-  const float4* src = reinterpret_cast<const float4*>(p.dq_accum + (size_t)(row0 + r) * D + d);
-  const float4 a = src[0], b = src[1];
-  uint4 w;
-  w.x = pack_bf16(a.x * p.scale, a.y * p.scale);
-  w.y = pack_bf16(a.z * p.scale, a.w * p.scale);
-  w.z = pack_bf16(b.x * p.scale, b.y * p.scale);
-  w.w = pack_bf16(b.z * p.scale, b.w * p.scale);
-  const size_t tok = VARLEN ? ((size_t)(sv.q_tok + r) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + r);
-  *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + tok * D + d) = w;
+  float4 a[R::NSUB], b[R::NSUB];
+#pragma unroll
+  for (int k = 0; k < R::NSUB; ++k) {
+    const int r = rb + k * R::ROWS + threadIdx.x / TPR;
+    if (r < sv.Nq) {
+      const float4* src = reinterpret_cast<const float4*>(p.dq_accum + (size_t)(row0 + r) * D + d);
+      a[k] = src[0];
+      b[k] = src[1];
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < R::NSUB; ++k) {
+    const int r = rb + k * R::ROWS + threadIdx.x / TPR;
+    if (r < sv.Nq) {
+      uint4 w;
+      w.x = pack_bf16(a[k].x * p.scale, a[k].y * p.scale);
+      w.y = pack_bf16(a[k].z * p.scale, a[k].w * p.scale);
+      w.z = pack_bf16(b[k].x * p.scale, b[k].y * p.scale);
+      w.w = pack_bf16(b[k].z * p.scale, b[k].w * p.scale);
+      const size_t tok = VARLEN ? ((size_t)(sv.q_tok + r) * p.va.H + sv.h) : ((size_t)bh * sv.Nq + r);
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq) + tok * D + d) = w;
+    }
+  }
 }
 
 // dK = scale * dk_accum, dV = dv_accum (bf16) for the rows of split global key tiles.
@@ -1193,7 +1221,7 @@ cudaError_t launch_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const
 template <int D>
 cudaError_t prep_t(const PrepParams& p, cudaStream_t st) {
   const int rows = p.va.cu_q ? (p.Nq + 63) / 64 * 64 : p.Nq_pad;  // varlen: padded maximum length
-  dim3 grid((unsigned)((rows + RowCfg<D>::ROWS - 1) / RowCfg<D>::ROWS), (unsigned)p.BH);
+  dim3 grid((unsigned)((rows + RowCfg<D>::ROWS_CTA - 1) / RowCfg<D>::ROWS_CTA), (unsigned)p.BH);
   if (p.va.cu_q) prep_kernel<D, true><<<grid, 256, 0, st>>>(p);
   else prep_kernel<D, false><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
@@ -1201,7 +1229,7 @@ cudaError_t prep_t(const PrepParams& p, cudaStream_t st) {
 
 template <int D>
 cudaError_t conv_t(const ConvParams& p, cudaStream_t st) {
-  dim3 grid((unsigned)((p.Nq + RowCfg<D>::ROWS - 1) / RowCfg<D>::ROWS), (unsigned)p.BH);
+  dim3 grid((unsigned)((p.Nq + RowCfg<D>::ROWS_CTA - 1) / RowCfg<D>::ROWS_CTA), (unsigned)p.BH);
   if (p.va.cu_q) convert_kernel<D, true><<<grid, 256, 0, st>>>(p);
   else convert_kernel<D, false><<<grid, 256, 0, st>>>(p);
   return cudaGetLastError();
