@@ -48,14 +48,19 @@ struct Cfg {
   static constexpr int KV_TILE = BN * D * 2;
   static constexpr int Q_CHUNK_BYTES = BM * ROWB;
   static constexpr int Q_TILE = BM * D * 2;
-  static constexpr int NS = 3;                         // Q / dO / lse2 / Dlt ring depth
+  static constexpr int NS = D <= 64 ? 4 : 3;           // Q / dO / lse2 / Dlt ring depth
+  // S^T / P^T / dQ^T TMEM buffers and dS^T shared-memory buffers: two at D = 128 (TMEM is
+  // full), three at D <= 64, where the smaller accumulators leave room for a third and the
+  // per-step chain (S^T -> P -> dS^T -> dQ^T -> drain -> S^T of the step NB later) spans
+  // one more step.  The one-CTA-per-unit kernel uses the first two.
+  static constexpr int NB = D <= 64 ? 3 : 2;
   static constexpr int DS_BYTES = BN * BM * 2;         // dS^T tile, bf16, 128-byte rows
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
   static constexpr int OFF_Q = 2 * KV_TILE;
   static constexpr int OFF_DO = OFF_Q + NS * Q_TILE;
   static constexpr int OFF_DS = OFF_DO + NS * Q_TILE;
-  static constexpr int OFF_LSE = OFF_DS + 2 * DS_BYTES;
+  static constexpr int OFF_LSE = OFF_DS + NB * DS_BYTES;
   static constexpr int OFF_DLT = OFF_LSE + NS * BM * 4;
   static constexpr int OFF_STG = OFF_DLT + NS * BM * 4;  // dQ_i staging, fp32 [BM][D]
   static constexpr int STG_BYTES = BM * D * 4;
@@ -65,27 +70,27 @@ struct Cfg {
   static constexpr int B_KV = 0;
   static constexpr int B_QF = 1;             // [NS] Q, dO, lse2, Dlt stage loaded
   static constexpr int B_QE = 1 + NS;        // [NS] stage free (dK, its last reader, done)
-  static constexpr int B_SF = 1 + 2 * NS;    // [2] S^T in TMEM buffer b
-  static constexpr int B_DPF = 3 + 2 * NS;   // dP^T in TMEM
-  static constexpr int B_PF = 4 + 2 * NS;    // [2] P^T in TMEM buffer b (compute warps)
+  static constexpr int B_SF = 1 + 2 * NS;    // [NB] S^T in TMEM buffer b
+  static constexpr int B_DPF = B_SF + NB;    // dP^T in TMEM
+  static constexpr int B_PF = B_DPF + 1;     // [NB] P^T in TMEM buffer b (compute warps)
   // [2] dS^T in shared memory buffer b (compute warps).  One per buffer: dP^T(i+1) waits only
   // for the compute warps to have loaded dP^T(i), so they can publish dS^T(i) and dS^T(i+1)
   // before issuer B waits for dS^T(i); dS^T(i+2) needs dQ^T(i), which B issues after that wait.
-  static constexpr int B_DSF = 6 + 2 * NS;
-  static constexpr int B_DQF = 8 + 2 * NS;   // [2] dQ^T MMA of a step done: its dS^T smem buffer is free
-  static constexpr int B_DQR = 10 + 2 * NS;  // [2] dQ^T in TMEM buffer b, ready for the dQ warpgroup
-  static constexpr int B_DQE = 12 + 2 * NS;  // [2] dQ^T drained from TMEM buffer b (buffer free)
-  static constexpr int B_KT = 14 + 2 * NS;   // K^T written into TMEM
-  static constexpr int B_DPE = 15 + 2 * NS;  // dP^T loaded by the compute warps (its TMEM columns free)
-  static constexpr int B_DRAIN = 16 + 2 * NS;  // [2] one per issuing thread
+  static constexpr int B_DSF = B_PF + NB;
+  static constexpr int B_DQF = B_DSF + NB;   // [NB] dQ^T and dK MMAs of a step done: its dS^T smem buffer is free
+  static constexpr int B_DQR = B_DQF + NB;   // [NB] dQ^T in TMEM buffer b, ready for the dQ warpgroup
+  static constexpr int B_DQE = B_DQR + NB;   // [NB] dQ^T drained from TMEM buffer b (buffer free)
+  static constexpr int B_KT = B_DQE + NB;    // K^T written into TMEM
+  static constexpr int B_DPE = B_KT + 1;     // dP^T loaded by the compute warps (its TMEM columns free)
+  static constexpr int B_DRAIN = B_DPE + 1;  // [2] one per issuing thread
   // persistent kernel only: K / V smem free (a unit's last S^T, dP^T done); K^T TMEM free (its
   // last dQ^T done); dK, dV drained from TMEM by the epilogue; work-unit ring full / empty;
   // the answer of a launch-control request landed
-  static constexpr int B_KVE = 18 + 2 * NS;
-  static constexpr int B_KTE = 19 + 2 * NS;
-  static constexpr int B_ACCE = 20 + 2 * NS;
+  static constexpr int B_KVE = B_DRAIN + 2;
+  static constexpr int B_KTE = B_KVE + 1;
+  static constexpr int B_ACCE = B_KTE + 1;
   static constexpr int NU = 4;               // work-unit ring slots
-  static constexpr int B_UF = 21 + 2 * NS;
+  static constexpr int B_UF = B_ACCE + 1;
   static constexpr int B_UE = B_UF + NU;
   static constexpr int B_CLC = B_UE + NU;
   static constexpr int NBAR = B_CLC + 1;
@@ -98,13 +103,14 @@ struct Cfg {
   // 13: UMMA issuer for S^T, dP^T (and TMEM allocator), 14: UMMA issuer for dV, dK, dQ^T
   static constexpr int THREADS = 480;
   static constexpr int W_PRODUCER = 12, W_MMA_A = 13, W_MMA_B = 14;
-  // TMEM columns: S^T/P^T/dQ^T buffer 0 | buffer 1 | dP^T | K^T (bf16 pairs) | dV | dK
-  static constexpr int T_S = 0, T_DP = 128, T_KT = 192, T_DV = 256, T_DK = 256 + D;
+  // TMEM columns: S^T/P^T/dQ^T buffers 0 .. NB-1 | dP^T | K^T (bf16 pairs) | dV | dK
+  static constexpr int T_S = 0, T_DP = NB * 64, T_KT = T_DP + 64, T_DV = T_KT + 64, T_DK = T_DV + D;
   static constexpr int TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, BM, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
   static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, false, true);   // dQ^T (A = K^T in TMEM, B MN-major)
   static_assert(Q_TILE % 1024 == 0 && KV_TILE % 1024 == 0 && OFF_STG % 128 == 0, "alignment");
+  static_assert(T_DK + D <= TMEM_COLS, "TMEM budget");
 };
 
 // Byte offset of the kk-th 16-wide K slice of a K-major tile whose CHUNK-wide column
@@ -199,15 +205,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(&bars[C::B_QF + s], 1);
       mbar_init(&bars[C::B_QE + s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NB; ++b) {
       mbar_init(&bars[C::B_SF + b], 1);
       mbar_init(&bars[C::B_PF + b], 256);
       mbar_init(&bars[C::B_DSF + b], 256);
       mbar_init(&bars[C::B_DQF + b], 1);
       mbar_init(&bars[C::B_DQR + b], 1);
       mbar_init(&bars[C::B_DQE + b], 128);
-      mbar_init(&bars[C::B_DRAIN + b], 1);
     }
+    mbar_init(&bars[C::B_DRAIN], 1);
+    mbar_init(&bars[C::B_DRAIN + 1], 1);
     mbar_init(&bars[C::B_DPF], 1);
     mbar_init(&bars[C::B_KT], 128);
     mbar_init(&bars[C::B_DPE], 256);
@@ -612,15 +619,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(&bars[C::B_QF + s], 1);
       mbar_init(&bars[C::B_QE + s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NB; ++b) {
       mbar_init(&bars[C::B_SF + b], 1);
       mbar_init(&bars[C::B_PF + b], 256);
       mbar_init(&bars[C::B_DSF + b], 256);
       mbar_init(&bars[C::B_DQF + b], 1);
       mbar_init(&bars[C::B_DQR + b], 1);
       mbar_init(&bars[C::B_DQE + b], 128);
-      mbar_init(&bars[C::B_DRAIN + b], 1);
     }
+    mbar_init(&bars[C::B_DRAIN], 1);
+    mbar_init(&bars[C::B_DRAIN + 1], 1);
     mbar_init(&bars[C::B_DPF], 1);
     mbar_init(&bars[C::B_KT], 128);
     mbar_init(&bars[C::B_DPE], 256);
@@ -766,14 +774,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const uint64_t dV = sdesc(sbase + C::OFF_V, 16, 8 * C::ROWB, C::LAYOUT);       // V, K-major
     const uint64_t dQk = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);      // Q stage 0, K-major
     const uint64_t dOk = sdesc(sbase + C::OFF_DO, 16, 8 * C::ROWB, C::LAYOUT);     // dO stage 0, K-major
-    auto issue_s = [&](int g) {  // S^T(g) = K Q^T into TMEM buffer g & 1
+    auto issue_s = [&](int g) {  // S^T(g) = K Q^T into TMEM buffer g % NB
       const uint64_t q = desc_adv(dQk, (uint32_t)((g % C::NS) * C::Q_TILE));
-      const uint32_t d = tmem + C::T_S + (uint32_t)((g & 1) * 64);
+      const uint32_t d = tmem + C::T_S + (uint32_t)((g % C::NB) * 64);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         umma_ss_w(d, desc_adv(dK, koff<D>(C::K_CHUNK_BYTES, kk)), desc_adv(q, koff<D>(C::Q_CHUNK_BYTES, kk)),
                   C::IDESC_S, kk > 0 ? 1u : 0u);
-      umma_commit_w(&bars[C::B_SF + (g & 1)]);
+      umma_commit_w(&bars[C::B_SF + g % C::NB]);
     };
     auto issue_dp = [&](int g) {  // dP^T(g) = V dO^T
       const uint64_t o = desc_adv(dOk, (uint32_t)((g % C::NS) * C::Q_TILE));
@@ -783,10 +791,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
                   C::IDESC_S, kk > 0 ? 1u : 0u);
       umma_commit_w(&bars[C::B_DPF]);
     };
-    // S^T(g) needs its stage loaded and its TMEM buffer drained of dQ^T(g-2)
+    // S^T(g) needs its stage loaded and its TMEM buffer drained of dQ^T(g-NB)
     auto s_ready = [&](int g) {
       return mbar_wait_w(&bars[C::B_QF + g % C::NS], (g / C::NS) & 1, wc, 33) &&
-             (g < 2 || mbar_wait_w(&bars[C::B_DQE + (g & 1)], ((g - 2) >> 1) & 1, wc, 49));
+             (g < C::NB || mbar_wait_w(&bars[C::B_DQE + g % C::NB], ((g - C::NB) / C::NB) & 1, wc, 49));
     };
     int g0 = 0;
     bool ok = true;
@@ -837,16 +845,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       // dV and dK start from zero: the previous unit's epilogue must have read them out
       if (u >= 1 && !(ok = mbar_wait_w(&bars[C::B_ACCE], (u - 1) & 1, wc, 56))) break;
       for (int it = 0; ok && it < n_it; ++it) {
-        const int g = g0 + it, s = g % C::NS, b = g & 1;
+        const int g = g0 + it, s = g % C::NS, b = g % C::NB, ph = (g / C::NB) & 1;
         const uint64_t qm = desc_adv(dQm, (uint32_t)(s * C::Q_TILE));
         const uint64_t om = desc_adv(dOm, (uint32_t)(s * C::Q_TILE));
-        if (!(ok = mbar_wait_w(&bars[C::B_PF + b], (g >> 1) & 1, wc, 34))) break;
+        if (!(ok = mbar_wait_w(&bars[C::B_PF + b], ph, wc, 34))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
           umma_ts_w(tmem + C::T_DV, tmem + C::T_S + (uint32_t)(b * 64) + a_col(kk), desc_adv(om, mnoff<D>(kk)),
                     C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-        if (!(ok = mbar_wait_w(&bars[C::B_DSF + b], (g >> 1) & 1, wc, 36))) break;
+        if (!(ok = mbar_wait_w(&bars[C::B_DSF + b], ph, wc, 36))) break;
         if (it == 0 && !(ok = mbar_wait_w(&bars[C::B_KT], u & 1, wc, 47))) break;
         tc_fence_after();
         const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
@@ -892,9 +900,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const int nk = VARLEN ? un.nk : p.Nk;  // (dense: the kernel parameter)
       for (int it = 0; it < n_it && ok; ++it) {
         const int g = g0 + it, s = g % C::NS, i = i0 + it;
-        const uint32_t t_sb = (uint32_t)((g & 1) * 64);  // this step's S^T / P^T buffer
+        const int b = g % C::NB, ph = (g / C::NB) & 1;
+        const uint32_t t_sb = (uint32_t)(b * 64);  // this step's S^T / P^T buffer
         if (!warp_wait(&bars[C::B_QF + s], (g / C::NS) & 1, wc, 38) ||
-            !warp_wait(&bars[C::B_SF + (g & 1)], (g >> 1) & 1, wc, 39)) {
+            !warp_wait(&bars[C::B_SF + b], ph, wc, 39)) {
           ok = false;
           break;
         }
@@ -921,7 +930,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         tmem_st16(t_lane + C::T_S + t_sb + wg * 32, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars[C::B_PF + (g & 1)]);
+        mbar_arrive(&bars[C::B_PF + b]);
 
         if (!warp_wait(&bars[C::B_DPF], g & 1, wc, 43)) {
           ok = false;
@@ -940,26 +949,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           const float d1 = pv[2 * c + 1] * (as_f(dv[2 * c + 1]) - dlt[2 * c + 1]);
           dk[c] = pack_bf16(d0, d1);
         }
-        // dS^T row into shared memory buffer g & 1 once the dQ^T and dK MMAs of step g-2 have
-        // read it
-        if (g >= 2 && !warp_wait(&bars[C::B_DQF + (g & 1)], ((g - 2) >> 1) & 1, wc, 44)) {
+        // dS^T row into shared memory buffer g % NB once the dQ^T and dK MMAs of step g-NB
+        // have read it
+        if (g >= C::NB && !warp_wait(&bars[C::B_DQF + b], ((g - C::NB) / C::NB) & 1, wc, 44)) {
           ok = false;
           break;
         }
-        uint8_t* dsrow = sds_row_base + (g & 1) * C::DS_BYTES;
+        uint8_t* dsrow = sds_row_base + b * C::DS_BYTES;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const int phys = (4 * wg + t) ^ (row & 7);
           *reinterpret_cast<uint4*>(dsrow + phys * 16) = make_uint4(dk[4 * t], dk[4 * t + 1], dk[4 * t + 2], dk[4 * t + 3]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bars[C::B_DSF + (g & 1)]);
+        mbar_arrive(&bars[C::B_DSF + b]);
       }
       // epilogue: WG0 writes dK = scale * acc, WG1 writes dV, once the unit's last MMAs are
       // done; the accumulator is handed back to issuer B as soon as it is read out
       const int gl = g0 + n_it - 1;
       g0 += n_it;
-      if (!(ok = ok && warp_wait(&bars[C::B_DQF + (gl & 1)], (gl >> 1) & 1, wc, 45))) break;
+      if (!(ok = ok && warp_wait(&bars[C::B_DQF + gl % C::NB], (gl / C::NB) & 1, wc, 45))) break;
       tc_fence_after();
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) +
                            (VARLEN ? ((size_t)(un.k_tok + key) * p.va.H + un.z) * D : ((size_t)un.z * p.Nk + key) * D);
@@ -1025,8 +1034,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (lane == 0) mbar_arrive(&bars[C::B_KVE]);  // this warp's reads of K are done
       }
       for (int it = 0; ok && it < n_it; ++it) {
-        const int g = g0 + it, b = g & 1;
-        if (!(ok = named_bar_and(1, 128, warp_wait(&bars[C::B_DQR + b], (g >> 1) & 1, wc, 46)))) break;
+        const int g = g0 + it, b = g % C::NB;
+        if (!(ok = named_bar_and(1, 128, warp_wait(&bars[C::B_DQR + b], (g / C::NB) & 1, wc, 46)))) break;
         tc_fence_after();
         uint32_t v0[32], v1[32];
         tmem_ld32(t_lane + C::T_S + (uint32_t)(b * 64), v0);
