@@ -585,7 +585,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     if (LOCAL && chunk >= 0) {
       // partial record of this key chunk: unnormalised O accumulator, m, l, lr
       if (ok && n_kv > 0 && !warp_wait(&bars[C::B_O + t], (n_kv - 1) & 1, wc, 8)) ok = false;
-      if (ok && q_idx < sv.Nq) {
+      if (ok) {  // (the TMEM loads are warp-wide; rows past the sequence store nothing)
+        const bool rv = q_idx < sv.Nq;
         const size_t rec = ((size_t)bh * (p.n_gp * 2 * C::BM) + q_idx) * p.n_split + chunk;
         float* po = p.part_o + rec * D;
         if (n_kv > 0) {
@@ -597,13 +598,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             tmem_wait_ld(o);
 #pragma unroll
             for (int c = 0; c < 16; c += 4)
-              *reinterpret_cast<float4*>(po + g * 16 + c) = make_float4(as_f(o[c]), as_f(o[c + 1]), as_f(o[c + 2]), as_f(o[c + 3]));
+              if (rv)
+                *reinterpret_cast<float4*>(po + g * 16 + c) =
+                    make_float4(as_f(o[c]), as_f(o[c + 1]), as_f(o[c + 2]), as_f(o[c + 3]));
           }
-        } else {
+        } else if (rv) {
           for (int d = 0; d < D; d += 4) *reinterpret_cast<float4*>(po + d) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        *reinterpret_cast<float4*>(p.part_ml + rec * 4) =
-            n_kv > 0 ? make_float4(m, l, lr, 0.f) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        if (rv)
+          *reinterpret_cast<float4*>(p.part_ml + rec * 4) =
+              n_kv > 0 ? make_float4(m, l, lr, 0.f) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
       }
     } else if (n_kv_all == 0) {  // this tile's rows see no key: O = 0, L = -inf
       if (q_idx < sv.Nq) {
