@@ -162,7 +162,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       kt = kt - n_split_ctas + p.n_gk;
     }
   }
-  const int bh = blockIdx.y;  // dense: batch * head; packed: head
+  int bh = blockIdx.y;  // dense: batch * head; packed: head
+  if (!VARLEN && !LOCAL && p.lpt) {
+    // longest-first over all heads: key tile 0 of every head, then key tile 1, ...
+    const int lin = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+    kt = lin / (int)gridDim.y;
+    bh = lin % (int)gridDim.y;
+  }
   // Packed batch: column x of the grid is a compact slot (slot_seq) of sequence b, whose
   // key tiles take its slots in order; a slot past the sequence's keys has nothing to do.
   int by = bh;
@@ -685,8 +691,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     auto resolve = [&](BwdUnit& un) -> bool {
       un.live = 1;
       if (!VARLEN) {
-        un.k0 = ux * C::BN;
-        un.z = uy;
+        // lpt: units in longest-first order over all heads (key tile 0 of every head, then
+        // key tile 1, ...), for causal launches of a few waves whose tail would otherwise be
+        // one head's heaviest key tiles starting last
+        int kt = ux, zz = uy;
+        if (p.lpt) {
+          const int lin = uy * (int)gridDim.x + ux;
+          kt = lin / (int)gridDim.y;
+          zz = lin % (int)gridDim.y;
+        }
+        un.k0 = kt * C::BN;
+        un.z = zz;
         un.q_tok = un.k_tok = un.b = 0;
         un.nq = p.Nq;
         un.nk = p.Nk;

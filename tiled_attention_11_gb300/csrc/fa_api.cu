@@ -23,6 +23,8 @@ std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_fwd_persist{1};
 // The same choice for the main backward kernel.
 std::atomic<int> g_bwd_persist{1};
+// Longest-first claim order for causal persistent launches of a few waves.
+std::atomic<int> g_lpt{1};
 
 // Optional events recorded around the main backward kernel (timing hook).
 std::mutex g_ev_mu;
@@ -332,6 +334,9 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
   const long long n_ctas = (long long)BH * ((p.n_q_tiles + 1) / 2);
   p.fold = (!lm && causal && n_ctas <= current_sms()) ? 1 : 0;
   p.persist = (!lm && !p.fold && n_ctas > current_sms()) ? g_fwd_persist.load() : 0;
+  // causal launches of up to eight waves: longest-first over all heads, so no head's
+  // heaviest pairs start last (the layer's 13 waves keep head-by-head order for L2 locality)
+  p.lpt = (p.persist && causal && n_ctas <= 8LL * current_sms()) ? g_lpt.load() : 0;
   if (lm) {
     p.lm = *lm;
     p.local = 1;
@@ -443,6 +448,8 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   // than one CTA per unit, so those keep one CTA per unit.
   const bool short_units = D < 128 || Nq <= 8192;
   bp.persist = (!lm && short_units && (long long)bp.n_k_tiles * BH > current_sms()) ? g_bwd_persist.load() : 0;
+  // causal launches of a few waves (persistent or not): longest-first over all heads
+  bp.lpt = (!lm && causal && (long long)bp.n_k_tiles * BH <= 8LL * current_sms()) ? g_lpt.load() : 0;
   cudaEvent_t ev_b = nullptr, ev_e = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_ev_mu);

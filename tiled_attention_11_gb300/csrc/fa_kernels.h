@@ -138,6 +138,8 @@ struct FwdParams {
   // Dense layout, plain masks, more units than one wave: the persistent kernel (a CTA
   // takes over not-yet-started CTAs of its grid instead of exiting).
   int persist;
+  // persistent, dense: claim units longest-first over all heads instead of head by head
+  int lpt;
 };
 
 struct FwdCombineParams {
@@ -180,6 +182,8 @@ struct BwdParams {
   // Dense layout, plain masks, more units than one wave and at least one query step per
   // key tile: the persistent kernel (a CTA takes over not-yet-started CTAs of its grid).
   int persist;
+  // persistent, dense: claim units longest-first over all heads instead of head by head
+  int lpt;
 };
 
 struct KvConvertParams {

@@ -799,8 +799,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         un.live = 1;
         un.pad = 0;
         if (!VARLEN) {
-          un.q0 = ((int)gridDim.x - 1 - ux) * 2 * C::BM;
-          un.z = uy;
+          // lpt: units in longest-first order over all heads (rank-major: every head's
+          // heaviest pair, then every head's next one), for launches of a few waves whose
+          // tail would otherwise be one head's heaviest pairs starting last
+          int pr = ux, zz = uy;
+          if (p.lpt) {
+            const int lin = uy * (int)gridDim.x + ux;
+            pr = lin / (int)gridDim.y;
+            zz = lin % (int)gridDim.y;
+          }
+          un.q0 = ((int)gridDim.x - 1 - pr) * 2 * C::BM;
+          un.z = zz;
           un.q_tok = un.k_tok = 0;
           un.nq = p.Nq;
           un.nk = p.Nk;
