@@ -863,6 +863,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int l
   // persistent CTAs beyond one wave; past 16384 queries per head the units are long enough
   // that one CTA per unit measured 1% faster
   p.persist = (Nq <= 16384 && (long long)((Nq + 255) / 256) * BH > current_sms()) ? g_fwd_persist.load() : 0;
+  p.lpt = (p.persist && causal && (long long)((Nq + 255) / 256) * BH <= 8LL * current_sms()) ? g_lpt.load() : 0;
   return ta11::launch_fwd_fp8(D, causal != 0, tq, tk, tv, p, (int)BH, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -226,6 +226,8 @@ struct Fp8FwdParams {
   unsigned* status;
   // more (query-tile pair, head) units than one wave: the persistent kernel
   int persist;
+  // persistent: claim units longest-first over all heads instead of head by head
+  int lpt;
 };
 
 // Host launchers (return cudaError_t of the launch).

@@ -397,6 +397,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   // key tiles of query tile t of pair `pair` (heaviest pairs of a head first: pair =
   // gridDim.x - 1 - x)
   auto n_keys = [&](int pair, int t) { return CAUSAL ? min(nk_tiles, 2 * pair + 1 + t) : nk_tiles; };
+  // a published unit is a CTA index (x, y); lpt maps it to (pair rank, head) rank-major
+  auto unit_rank = [&](int2 u) { return p.lpt ? (u.y * (int)gridDim.x + u.x) / (int)gridDim.y : u.x; };
+  auto unit_head = [&](int2 u) { return p.lpt ? (u.y * (int)gridDim.x + u.x) % (int)gridDim.y : u.y; };
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
 
   if (threadIdx.x == 0) {
@@ -448,7 +451,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       units[us] = make_int2(ux, uy);
       mbar_arrive_w(&bars[C::B_UF + us]);
       if (ux < 0) break;
-      const int pair = (int)gridDim.x - 1 - ux, bh = uy, q0 = pair * 2 * C::BM;
+      // lpt: longest-first over all heads (rank-major), for causal launches of a few waves
+      int pr = ux, bh = uy;
+      if (p.lpt) {
+        const int lin = uy * (int)gridDim.x + ux;
+        pr = lin / (int)gridDim.y;
+        bh = lin % (int)gridDim.y;
+      }
+      const int pair = (int)gridDim.x - 1 - pr, q0 = pair * 2 * C::BM;
       const int n_kv = n_keys(pair, 1);  // tile 1's walk contains tile 0's
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t) {  // Q_t is free once the last S MMA reading it is done
@@ -526,7 +536,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const int2 u = units[us];
       mbar_arrive_w(&bars[C::B_UE + us]);
       if (u.x < 0) break;
-      const int pair = (int)gridDim.x - 1 - u.x;
+      const int pair = (int)gridDim.x - 1 - unit_rank(u);
       const int n_kv0 = n_keys(pair, 0), n_kv1 = n_keys(pair, 1);
       // the unit's first S tiles (their TMEM columns were last read by the previous unit's
       // P V, issued earlier by this warp)
@@ -593,7 +603,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
       if (u.x < 0) break;
-      const int pair = (int)gridDim.x - 1 - u.x, bh = u.y;
+      const int pair = (int)gridDim.x - 1 - unit_rank(u), bh = unit_head(u);
       const int qt0 = pair * 2 * C::BM + t * C::BM;
       const int q_idx = qt0 + row;
       const int n_kv = n_keys(pair, t);
