@@ -110,6 +110,7 @@ struct Cfg {
   static constexpr uint32_t IDESC_S = idesc_bf16(128, BM, false, false);   // S^T, dP^T
   static constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);    // dV, dK (B MN-major)
   static constexpr uint32_t IDESC_DQ = idesc_bf16(128, BM, false, true);   // dQ^T (A = K^T in TMEM, B MN-major)
+  static constexpr uint32_t IDESC_DQ2 = idesc_bf16(128, 2 * BM, false, true);  // dQ^T of two steps at once
   static_assert(Q_TILE % 1024 == 0 && KV_TILE % 1024 == 0 && OFF_STG % 128 == 0, "alignment");
   static_assert(T_DK + D <= TMEM_COLS, "TMEM budget");
 };
@@ -873,19 +874,34 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         if (!(ok = mbar_wait_w(&bars[C::B_DSF + b], ph, wc, 36))) break;
         if (it == 0 && !(ok = mbar_wait_w(&bars[C::B_KT], u & 1, wc, 47))) break;
         tc_fence_after();
-        const uint64_t ds = desc_adv(dS0, (uint32_t)(b * C::DS_BYTES));
+        // D = 64 (NB = 4): the dQ^T of an even step and the next step of the same unit run as
+        // one N = 128 UMMA group over their two adjacent dS^T / TMEM buffers (an N = 64
+        // group costs three quarters of an N = 128 one; 2-3% faster at D = 64, slower at
+        // D <= 32); other steps run alone
+        constexpr bool PAIRS = C::NB >= 4 && D == 64;
+        const bool first_of_pair = PAIRS && (g & 1) == 0 && it + 1 < n_it;
+        const bool second_of_pair = PAIRS && (g & 1) == 1 && it >= 1;
+        if (!first_of_pair) {
+          const int b0 = second_of_pair ? b - 1 : b;
+          const uint64_t ds = desc_adv(dS0, (uint32_t)(b0 * C::DS_BYTES));
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          umma_ts_w(tmem + C::T_S + (uint32_t)(b * 64), tmem + C::T_KT + kk * 8, desc_adv(ds, (uint32_t)(kk * 16 * 128)),
-                    C::IDESC_DQ, kk > 0 ? 1u : 0u);
-        umma_commit_w(&bars[C::B_DQR + b]);
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            umma_ts_w(tmem + C::T_S + (uint32_t)(b0 * 64), tmem + C::T_KT + kk * 8,
+                      desc_adv(ds, (uint32_t)(kk * 16 * 128)), second_of_pair ? C::IDESC_DQ2 : C::IDESC_DQ,
+                      kk > 0 ? 1u : 0u);
+          if (second_of_pair) umma_commit_w(&bars[C::B_DQR + b0]);
+          umma_commit_w(&bars[C::B_DQR + b]);
+        }
         const uint64_t dsa = desc_adv(dSa, (uint32_t)(b * C::DS_BYTES));
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
           umma_ss_w(tmem + C::T_DK, desc_adv(dsa, (uint32_t)(kk * 32)), desc_adv(qm, mnoff<D>(kk)), C::IDESC_KV,
                     (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_w(&bars[C::B_QE + s]);   // dK was the stage's last reader
-        umma_commit_w(&bars[C::B_DQF + b]);  // dQ^T and dK have both read dS^T buffer b
+        umma_commit_w(&bars[C::B_QE + s]);  // dK was the stage's last reader
+        // dQ^T and dK have both read dS^T buffer b (a pair's first buffer is released with
+        // the second, after their joint dQ^T)
+        if (second_of_pair) umma_commit_w(&bars[C::B_DQF + b - 1]);
+        if (!first_of_pair) umma_commit_w(&bars[C::B_DQF + b]);
       }
       umma_commit_w(&bars[C::B_KTE]);  // this unit's last read of K^T is done
       g0 += n_it;
