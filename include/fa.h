@@ -212,6 +212,14 @@ int fa_step_host(const void* q_h, const void* k_h, const void* v_h, const void* 
  * fa_quantize_e4m3_transposed: bf16 [B,H,N,D] -> codes_t [B,H,D,ldt] (keys innermost, the
  *   layout fa_fwd_fp8 takes for V), same rule with one scale for the whole tensor;
  *   ldt >= N and a multiple of 16; bytes of a row past N may be left unwritten; D in {64, 128}.
+ * fa_quantize_qkv_e4m3: the three quantisations fa_fwd_fp8 takes, in one call: q bf16
+ *   [B,H,Nq,D] -> q8 and k bf16 [B,H,Nk,D] -> k8 as fa_quantize_e4m3, v bf16 [B,H,Nk,D] ->
+ *   vt8 [B,H,D,ldv] as fa_quantize_e4m3_transposed (ldv >= Nk, a multiple of 16), with
+ *   amax[3] and descale[3] (device floats, in the order q, k, v; amax zeroed first on
+ *   `stream`).  Codes and descales are those of the three separate calls bit for bit; one
+ *   amax pass reads the three tensors and one pass writes the three code tensors, so the
+ *   call makes one memset and two kernel launches instead of three and six.  D in {64, 128};
+ *   all tensors 16-byte aligned; no output may overlap an input or another output.
  * fa_fwd_fp8: O = softmax(scale * (qd*Q8)(kd*K8)^T) (vd*V8) and L as for fa_fwd, with
  *   q8, k8 e4m3 [B,H,N,D], vt8 e4m3 [B,H,D,ldv] (ldv >= Nk, multiple of 16), descales as
  *   device floats; O bf16 [B,H,Nq,D], L fp32 [B,H,Nq].  Both GEMMs run on e4m3 operands
@@ -223,6 +231,8 @@ int fa_step_host(const void* q_h, const void* k_h, const void* v_h, const void* 
 int fa_quantize_e4m3(const void* x, long long n, void* codes, float* amax, float* descale, cudaStream_t stream);
 int fa_quantize_e4m3_transposed(const void* x, int B, int H, int N, int D, int ldt, void* codes_t, float* amax,
                                 float* descale, cudaStream_t stream);
+int fa_quantize_qkv_e4m3(const void* q, const void* k, const void* v, int B, int H, int Nq, int Nk, int D, void* q8,
+                         void* k8, void* vt8, int ldv, float* amax, float* descale, cudaStream_t stream);
 int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int ldv, const float* q_descale,
                const float* k_descale, const float* v_descale, void* o, float* lse, int B, int H, int Nq, int Nk,
                int D, float scale, int causal, cudaStream_t stream);

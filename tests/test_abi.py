@@ -209,6 +209,20 @@ def test_fp8_validation_codes(L):
     assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 64, 100, c, a, d, None) == _lib.FA_ERR_INVALID_ARG
     assert L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 48, 112, c, a, d, None) == _lib.FA_ERR_UNSUPPORTED_D
     reaches_device(lambda: L.fa_quantize_e4m3_transposed(x, 1, 2, 100, 64, 112, c, a, d, None))
+    q, k, v, q8, k8, vt8, am, de = (vp(x) for x in ptrs(8))
+    qkv = lambda **kw: L.fa_quantize_qkv_e4m3(kw.get("q", q), k, v, 2, 3, 100, kw.get("Nk", 90),  # noqa: E731
+                                             kw.get("D", 128), kw.get("q8", q8), k8, vt8, kw.get("ldv", 96),
+                                             kw.get("am", am), kw.get("de", de), None)
+    assert qkv(D=32) == _lib.FA_ERR_UNSUPPORTED_D
+    assert qkv(ldv=80) == _lib.FA_ERR_INVALID_ARG       # < Nk
+    assert qkv(ldv=100) == _lib.FA_ERR_INVALID_ARG      # not a multiple of 16
+    assert qkv(Nk=0) == _lib.FA_ERR_INVALID_ARG
+    assert qkv(q8=vp(0)) == _lib.FA_ERR_INVALID_ARG
+    assert qkv(q8=q) == _lib.FA_ERR_INVALID_ARG         # codes overlap their input
+    assert qkv(de=vp(ptrs(8)[6] + 8)) == _lib.FA_ERR_INVALID_ARG  # descale[3] overlaps amax[3]
+    assert qkv(q=vp(ptrs(1)[0] + 8)) == _lib.FA_ERR_MISALIGNED
+    assert qkv(am=vp(ptrs(8)[6] + 2)) == _lib.FA_ERR_MISALIGNED
+    reaches_device(lambda: qkv())
 
 
 def test_step_host_validation_codes(L):
@@ -301,3 +315,5 @@ def test_length_limit(L):
     assert fp8(M + 1, 16, 16) == bad
     assert fp8(16, M + 16, M + 16) == bad
     assert L.fa_quantize_e4m3_transposed(far[0], 1, 1, M + 1, 64, M + 16, *far[1:4], None) == bad
+    assert L.fa_quantize_qkv_e4m3(*far[:3], 1, 1, M + 1, 16, 64, *far[3:6], 16, *far[6:8], None) == bad
+    assert L.fa_quantize_qkv_e4m3(*far[:3], 1, 1, 16, M + 1, 64, *far[3:6], M + 16, *far[6:8], None) == bad

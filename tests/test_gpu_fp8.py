@@ -87,6 +87,46 @@ def test_quantize_transposed_bit_exact(shape):
     assert descale.item() == wd
 
 
+# the three tensors of one call in one launch pair: Nq != Nk, ragged key slabs (not a
+# multiple of 128 or of 16), a single key, an all-zero tensor, wide value ranges
+QKV_CASES = [((2, 3, 257, 1000, 128), (1.0, 1.0, 1.0)), ((1, 2, 100, 129, 64), (3.0, 1e-3, 700.0)),
+             ((1, 1, 1, 1, 128), (1.0, 2.0, 0.5)), ((3, 2, 4099, 300, 64), (0.0, 1.0, 5.0)),
+             ((1, 4, 64, 4096, 128), (1.0, 0.0, 0.0))]
+
+
+@pytest.mark.parametrize("shape,mults", QKV_CASES)
+def test_quantize_qkv_bit_exact(shape, mults):
+    B, H, Nq, Nk, D = shape
+    g = torch.Generator().manual_seed(3 + sum(shape))
+    q, k, v = ((torch.randn((B, H, n, D), generator=g) * m).to(torch.bfloat16)
+               for n, m in ((Nq, mults[0]), (Nk, mults[1]), (Nk, mults[2])))
+    q8, k8, vt8, ldv, amax, descale = _lib.quantize_qkv_e4m3(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    assert ldv % 16 == 0 and Nk <= ldv < Nk + 16
+    vt = vt8.cpu().numpy()
+    for t, (x, got) in enumerate(((q, q8.cpu().numpy()), (k, k8.cpu().numpy()), (v, vt[..., :Nk]))):
+        want, wd = oracle_codes(x)
+        if t == 2:
+            want = want.transpose(0, 1, 3, 2)
+            assert int(vt[..., Nk:].max(initial=0)) == 0  # keys past Nk up to ldv: zero codes
+        assert np.array_equal(got, want), f"tensor {t}"
+        assert descale.cpu().numpy()[t].view(np.uint32) == np.float32(wd).view(np.uint32)
+        assert amax.cpu().numpy()[t] == np.abs(x.to(torch.float32).numpy()).max()
+
+
+def test_quantize_qkv_equals_separate_calls():
+    p = I.Problem(2, 8, 1500, 1500, 128, True)
+    q, k, v = (t.cuda() for t in I.draw(p, 5)[:3])
+    q8, k8, vt8, ldv, _, descale = _lib.quantize_qkv_e4m3(q, k, v)
+    sq, _, dq = _lib.quantize_e4m3(q)
+    sk, _, dk = _lib.quantize_e4m3(k)
+    svt, sldv, _, dv = _lib.quantize_e4m3_transposed(v)
+    torch.cuda.synchronize()
+    assert ldv == sldv
+    assert torch.equal(q8, sq) and torch.equal(k8, sk) and torch.equal(vt8, svt)
+    assert torch.equal(descale, torch.cat([dq, dk, dv]))
+
+
 def run_fp8(p, seed):
     q, k, v, _ = I.draw(p, seed)
     (q8, qd), (k8, kd), (v8, vd) = oracle_codes(q), oracle_codes(k), oracle_codes(v)

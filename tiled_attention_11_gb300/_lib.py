@@ -32,7 +32,7 @@ EXPORTED = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_strerror", "fa_devi
             "fa_graph_create", "fa_graph_launch", "fa_graph_destroy", "fa_fwd_varlen", "fa_bwd_varlen",
             "fa_bwd_varlen_workspace_size", "fa_fwd_window", "fa_bwd_window", "fa_fwd_window_workspace_size", "fa_bwd_window_workspace_size",
             "fa_quantize_e4m3",
-            "fa_quantize_e4m3_transposed", "fa_fwd_fp8", "fa_step_host",
+            "fa_quantize_e4m3_transposed", "fa_quantize_qkv_e4m3", "fa_fwd_fp8", "fa_step_host",
             "fa_step_host_device_bytes")
 
 _lib = None
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
     L.fa_quantize_e4m3.restype = i
     L.fa_quantize_e4m3_transposed.argtypes = [vp, i, i, i, i, i, vp, vp, vp, vp]
     L.fa_quantize_e4m3_transposed.restype = i
+    L.fa_quantize_qkv_e4m3.argtypes = [vp, vp, vp, i, i, i, i, i, vp, vp, vp, i, vp, vp, vp]
+    L.fa_quantize_qkv_e4m3.restype = i
     L.fa_fwd_fp8.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     L.fa_fwd_fp8.restype = i
     L.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, i, vp, sz, vp]
@@ -462,13 +464,30 @@ def fa_fwd_fp8(q8, k8, vt8, ldv: int, q_descale, k_descale, v_descale, o, lse, c
     _check(rc, "fa_fwd_fp8")
 
 
+def quantize_qkv_e4m3(q, k, v, stream=None):
+    """C ``fa_quantize_qkv_e4m3`` on bf16 q [B,H,Nq,D], k, v [B,H,Nk,D]: returns (q8, k8 uint8
+    like q, k; vt8 uint8 [B,H,D,ldv]; ldv = Nk rounded up to 16; amax, descale: float32 CUDA
+    tensors of 3, in the order q, k, v)."""
+    B, H, Nq, Nk, D = _dense_sizes(q, k, v)
+    ldv = (Nk + 15) // 16 * 16
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device=q.device)
+    k8 = torch.empty(k.shape, dtype=torch.uint8, device=q.device)
+    vt8 = torch.empty((B, H, D, ldv), dtype=torch.uint8, device=q.device)  # (every byte is written)
+    sc = torch.empty(6, dtype=torch.float32, device=q.device)
+    amax, descale = sc[0:3], sc[3:6]
+    rc = lib().fa_quantize_qkv_e4m3(_ptr(q, "q", torch.bfloat16), _ptr(k, "k", torch.bfloat16),
+                                    _ptr(v, "v", torch.bfloat16), B, H, Nq, Nk, D, _ptr(q8, "q8", torch.uint8),
+                                    _ptr(k8, "k8", torch.uint8), _ptr(vt8, "vt8", torch.uint8), ldv,
+                                    amax.data_ptr(), descale.data_ptr(), _stream(stream))
+    _check(rc, "fa_quantize_qkv_e4m3")
+    return q8, k8, vt8, ldv, amax, descale
+
+
 def forward_fp8(q, k, v, causal: bool, scale: float | None = None, stream=None):
-    """Quantise bf16 q, k, v per tensor (three kernels each side) and run the FP8 forward;
-    returns (o bf16, lse float32)."""
-    _dense_sizes(q, k, v)
-    q8, _, qd = quantize_e4m3(q, stream)
-    k8, _, kd = quantize_e4m3(k, stream)
-    vt8, ldv, _, vd = quantize_e4m3_transposed(v, stream)
+    """Quantise bf16 q, k, v per tensor (fa_quantize_qkv_e4m3: two kernels) and run the FP8
+    forward; returns (o bf16, lse float32)."""
+    q8, k8, vt8, ldv, _, sc = quantize_qkv_e4m3(q, k, v, stream)
+    qd, kd, vd = sc[0:1], sc[1:2], sc[2:3]
     B, H, Nq, D = q.shape
     o = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)

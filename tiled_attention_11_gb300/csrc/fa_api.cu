@@ -824,6 +824,36 @@ extern "C" int fa_quantize_e4m3_transposed(const void* x, int B, int H, int N, i
              : FA_ERR_LAUNCH;
 }
 
+extern "C" int fa_quantize_qkv_e4m3(const void* q, const void* k, const void* v, int B, int H, int Nq, int Nk,
+                                    int D, void* q8, void* k8, void* vt8, int ldv, float* amax, float* descale,
+                                    cudaStream_t stream) {
+  if (!q || !k || !v || !q8 || !k8 || !vt8 || !amax || !descale) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || !valid_len(Nq) || !valid_len(Nk) || (long long)B * H > 65535 || ldv < Nk || ldv % 16 != 0)
+    return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED_D;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(q8, 16) || !aligned(k8, 16) ||
+      !aligned(vt8, 16) || !aligned(amax, 4) || !aligned(descale, 4))
+    return FA_ERR_MISALIGNED;
+  const size_t BH = (size_t)B * H;
+  const Range ins[] = {rng(q, BH * Nq * D * 2), rng(k, BH * Nk * D * 2), rng(v, BH * Nk * D * 2)};
+  const Range outs[] = {rng(q8, BH * Nq * D), rng(k8, BH * Nk * D), rng(vt8, BH * D * ldv), rng(amax, 12),
+                        rng(descale, 12)};
+  for (int a = 0; a < 5; ++a) {
+    for (const Range& in : ins)
+      if (overlap(outs[a], in)) return FA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 5; ++b)
+      if (overlap(outs[a], outs[b])) return FA_ERR_INVALID_ARG;
+  }
+  unsigned* status = nullptr;
+  int rc_dev = current_device(&status);
+  if (rc_dev != FA_OK) return rc_dev;
+  if (cudaMemsetAsync(amax, 0, 12, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  return ta11::launch_quantize_qkv(q, k, v, (int)BH, Nq, Nk, D, q8, k8, vt8, ldv, amax, descale, stream) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_LAUNCH;
+}
+
 extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int ldv, const float* q_descale,
                           const float* k_descale, const float* v_descale, void* o, float* lse, int B, int H, int Nq,
                           int Nk, int D, float scale, int causal, cudaStream_t stream) {

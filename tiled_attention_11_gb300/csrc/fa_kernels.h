@@ -251,6 +251,11 @@ cudaError_t launch_quant_e4m3(const void* x, long long n, const float* amax, voi
                               cudaStream_t st);
 cudaError_t launch_quant_e4m3_t(const void* x, int BH, int N, int D, int ldt, const float* amax, void* codes_t,
                                 float* descale, cudaStream_t st);
+// Q, K (codes in place order) and V (codes transposed, [BH][D][ldv]) of one call: one amax
+// launch over the three (amax[3], zeroed by the caller's stream order), one code launch.
+cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, int BH, int Nq, int Nk, int D,
+                                void* q8, void* k8, void* vt8, int ldv, float* amax, float* descale,
+                                cudaStream_t st);
 cudaError_t launch_wait_probe(unsigned long long limit_ns, unsigned* status, cudaStream_t st);
 
 }  // namespace ta11
