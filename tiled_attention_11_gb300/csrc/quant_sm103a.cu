@@ -322,12 +322,14 @@ cudaError_t launch_quantize_qkv(const void* q, const void* k, const void* v, int
   a.BH = BH;
   a.Nk = Nk;
   a.ldv = ldv;
-  a.n_slabs = (Nk + 127) / 128;
-  a.n_vt = a.n_slabs * BH;
-  a.n_qb = (int)((a.nq8 + quant::kChunk - 1) / quant::kChunk);
+  const long long n_vt = (long long)((Nk + 127) / 128) * BH;
+  const long long n_qb = (a.nq8 + quant::kChunk - 1) / quant::kChunk;
   const long long n_kb = (a.nk8 + quant::kChunk - 1) / quant::kChunk;
-  const long long blocks = (long long)a.n_vt + a.n_qb + n_kb;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const long long blocks = n_vt + n_qb + n_kb;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;  // (checked before any narrowing)
+  a.n_slabs = (Nk + 127) / 128;
+  a.n_vt = (int)n_vt;
+  a.n_qb = (int)n_qb;
   const dim3 grid((unsigned)blocks);
   switch (D) {
     case 64: return quant::launch_dependent(quant::quant_qkv_kernel<64>, grid, st, a);
