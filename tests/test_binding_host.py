@@ -90,6 +90,17 @@ def test_forward_fp8_checks_k_and_v_against_q():
         _lib.forward_fp8(z(B, H, NQ, D), z(B, H, NK, D), z(B, H, NK + 16, D), True)
 
 
+def test_quantize_qkv_checks_k_and_v_against_q():
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        _lib.quantize_qkv_e4m3(z(B, H, NQ, D), z(B, H, NK, D), z(B, H, NK, D))
+    for k, v, msg in ((z(B, H, NK, 128), z(B, H, NK, D), "k has shape"),
+                      (z(B, H, NK, D), z(B, H, NK + 16, D), "v has shape"),
+                      (z(B, H + 1, NK, D), z(B, H, NK, D), "k has shape"),
+                      (z(H, NK, D), z(B, H, NK, D), r"must be \[B, H, N, D\]")):
+        with pytest.raises(ValueError, match=msg):
+            _lib.quantize_qkv_e4m3(z(B, H, NQ, D), k, v)
+
+
 def fp8_args():
     ldv = (NK + 15) // 16 * 16
     return dict(q8=z(B, H, NQ, D, dtype=U8), k8=z(B, H, NK, D, dtype=U8), vt8=z(B, H, D, ldv, dtype=U8), ldv=ldv,
