@@ -245,3 +245,43 @@ def test_window_split_global_keys(p, wl, wr, g):
     assert (_lib.fa_bwd_window_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D, wl, wr, g) >
             _lib.fa_bwd_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D))
     check_window(p, wl, wr, g)
+
+
+# Beyond one wave of query-tile pairs the forward of an unsplit mask (causal, or no global
+# rows to split) runs persistent CTAs by default: same per-row arithmetic and key order as
+# one CTA per pair, so O and L agree bit for bit.  Ragged tails (a pair whose second tile is
+# past the rows), Nq > Nk (tiles whose rows see no key), globals across two tiles, D 16-128.
+PERSIST_CASES = [
+    (I.Problem(1, 32, 1100, 1100, 128, True), 300, -1, 64, True),
+    (I.Problem(2, 40, 700, 700, 64, False), 100, 50, 0, False),
+    (I.Problem(1, 64, 600, 333, 32, False), 50, 40, 0, True),
+    (I.Problem(1, 48, 1000, 1000, 16, False), 64, 64, 100, False),
+    (I.Problem(1, 32, 1300, 900, 128, True), 200, -1, 130, False),
+]
+
+
+@pytest.mark.parametrize("p,wl,wr,g,with_oracle", PERSIST_CASES,
+                         ids=[f"{c[0].name()}-wl{c[1]}-wr{c[2]}-g{c[3]}" for c in PERSIST_CASES])
+def test_window_forward_persistent_equals_one_cta_per_pair(p, wl, wr, g, with_oracle):
+    q, k, v, _ = I.draw(p, 4)
+    dev = torch.device("cuda")
+    qg, kg, vg = (t.to(dev) for t in (q, k, v))
+    outs = {}
+    prev = _lib.fa_set_fwd_persistent(True)
+    try:
+        for on in (True, False):
+            _lib.fa_set_fwd_persistent(on)
+            o = torch.full_like(qg, float("nan"))
+            lse = torch.full((p.B, p.H, p.Nq), float("nan"), dtype=torch.float32, device=dev)
+            _lib.fa_fwd_window(qg, kg, vg, o, lse, p.causal, wl, wr, g, p.scale)
+            torch.cuda.synchronize()
+            outs[on] = (o, lse)
+    finally:
+        _lib.fa_set_fwd_persistent(prev)
+    assert torch.equal(outs[True][0], outs[False][0]), "O"
+    assert torch.equal(outs[True][1], outs[False][1]), "L"
+    if with_oracle:
+        qd, kd, vd = (I.as_f64(t) for t in (q, k, v))
+        ro, rl = masked_ref.attention_forward(qd, kd, vd, p.scale, p.causal, wl, wr, g)
+        assert_close("persistent O", f64(outs[True][0]), ro)
+        assert_lse("persistent L", f64(outs[True][1]), rl)

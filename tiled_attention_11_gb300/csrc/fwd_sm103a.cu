@@ -1138,6 +1138,427 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------------------------
+// Persistent form of the two-tile kernel for the local-window + global-token mask (dense
+// layout, no split global rows: causal, or no global tokens, or few key tiles).  The
+// schedule is fwd_persist_kernel's (units claimed through cluster launch control, the K/V
+// ring, barrier phases and the staging tile carried across units); the walk over each unit's
+// key tiles is fwd_kernel's LOCAL one: the union of the two query tiles' sets (global tiles
+// [a, g) and window tiles [L, hi)), each tile taking part where its set has the key tile.
+// Units are the one-CTA kernel's pairs in its order (pairs holding global rows first).
+// Both Q tiles are loaded for every unit and every Q / Q-free barrier completes once per
+// unit, also for a tile that sees no key (its rows get O = 0, L = -inf), so the phases stay
+// in step.  Per-row arithmetic and key order are fwd_kernel's.
+// ------------------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
+    fwd_persist_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                             const FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  void* clc_resp = smem + C::OFF_CLC;
+  FwdUnit* units = reinterpret_cast<FwdUnit*>(smem + C::OFF_UNITS);
+
+  const int warp = (int)warp_id(), lane = (int)lane_id();
+  // key tiles the query tile starting at row qa visits (fwd_kernel's set, no key chunk)
+  auto key_set = [&](int qa) -> TileSet {
+    if (qa >= p.Nq) return TileSet::make(0, 0, 0, 0);
+    const int qb = min(qa + C::BM, p.Nq) - 1;
+    int kmax = p.Nk - 1;
+    if (qa >= p.lm.n_glob) kmax = min(kmax, max(qb + p.lm.win_r, p.lm.n_glob - 1));
+    if (CAUSAL) kmax = min(kmax, qb);
+    const int hi = kmax >= 0 ? kmax / C::BN + 1 : 0;
+    if (qa < p.lm.n_glob) return TileSet::make(0, 0, 0, hi);
+    return TileSet::make(0, (p.lm.n_glob + C::BN - 1) / C::BN, max(qa - p.lm.win_l, 0) / C::BN, hi);
+  };
+  const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars[C::B_Q + t], 1);
+      mbar_init(&bars[C::B_SF + t], 1);
+      mbar_init(&bars[C::B_PF + t], 128);
+      mbar_init(&bars[C::B_O + t], 1);
+      mbar_init(&bars[C::B_QE + t], 1);
+    }
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&bars[C::B_KF + s], 1);
+      mbar_init(&bars[C::B_VF + s], 1);
+      mbar_init(&bars[C::B_KE + s], 1);
+      mbar_init(&bars[C::B_VE + s], 1);
+    }
+    for (int u = 0; u < C::NU; ++u) {
+      mbar_init(&bars[C::B_UF + u], 1);
+      mbar_init(&bars[C::B_UE + u], 9);  // the issuing thread and one lane of each softmax warp
+    }
+    mbar_init(&bars[C::B_DRAIN], 1);
+    mbar_init(&bars[C::B_STG], 1);
+    mbar_init(&bars[C::B_STG1], 1);
+    mbar_init(&bars[C::B_CLC], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::W_MMA) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::W_PRODUCER) {
+    // ---------------------------------------------------------------- scheduler + TMA producer
+    {
+      if (lane == 0) tma_prefetch_desc(&tm_q);
+      if (lane == 0) tma_prefetch_desc(&tm_k);
+      if (lane == 0) tma_prefetch_desc(&tm_v);
+      if (lane == 0) tma_prefetch_desc(&tm_o);
+      int ux = (int)blockIdx.x, uy = (int)blockIdx.y;  // the CTA index to work on next (ux < 0: none)
+      int jg = 0, k_issued = 0, v_issued = 0, q_units = 0;  // copies started (ring positions, Q pairs)
+      bool asked = false;  // a launch-control answer is pending
+      int n_asked = 0;
+      auto claim = [&]() -> bool {  // take over the next CTA of the grid that has not started
+        mbar_arrive_expect_tx_w(&bars[C::B_CLC], 16);
+        clc_try_cancel_w(clc_resp, &bars[C::B_CLC]);
+        asked = true;
+        if (!mbar_wait_w(&bars[C::B_CLC], n_asked & 1, wc, 12)) return false;
+        asked = false;
+        ++n_asked;
+        int cx, cy;
+        const bool taken = clc_taken(clc_resp, cx, cy);
+        ux = (taken && cx >= 0 && cx < (int)gridDim.x && cy >= 0 && cy < (int)gridDim.y) ? cx : -1;
+        uy = cy;
+        return true;
+      };
+      for (int i = 0;; ++i) {
+        FwdUnit un;
+        un.live = ux >= 0 ? 1 : 0;
+        un.q0 = ux * 2 * C::BM;  // pairs in launch order: those holding global rows first
+        un.z = uy;
+        un.q_tok = un.k_tok = 0;
+        un.nq = p.Nq;
+        un.nk = p.Nk;
+        un.pad = 0;
+        bool ok = true;
+        const int us = i % C::NU;
+        if (i >= C::NU && !mbar_wait_w(&bars[C::B_UE + us], ((i / C::NU) - 1) & 1, wc, 10)) break;
+        units[us] = un;  // (every lane holds the same record)
+        mbar_arrive_w(&bars[C::B_UF + us]);
+        if (!un.live) break;
+        const int q0 = un.q0;
+        const TileSet ks0 = key_set(q0), ks1 = key_set(q0 + C::BM);
+        for (int t = 0; t < 2 && ok; ++t) {  // Q_t is free once the last S MMA reading it is done
+          if (i >= 1 && !(ok = mbar_wait_w(&bars[C::B_QE + t], (i - 1) & 1, wc, 11))) break;
+          mbar_arrive_expect_tx_w(&bars[C::B_Q + t], C::TILE_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d_w(smem + C::OFF_Q + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, &bars[C::B_Q + t],
+                          c * C::CHUNK, q0 + t * C::BM, un.z);
+        }
+        if (!ok) break;
+        q_units = i + 1;
+        for (int kt = min(ks0.next(-1), ks1.next(-1)); ok && kt != TileSet::kNone;
+             kt = min(ks0.next(kt), ks1.next(kt)), ++jg) {
+          const int s = jg % C::NS;
+          if (jg >= C::NS && !(ok = mbar_wait_w(&bars[C::B_KE + s], ((jg / C::NS) - 1) & 1, wc, 1))) break;
+          mbar_arrive_expect_tx_w(&bars[C::B_KF + s], C::TILE_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d_w(smem + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, &bars[C::B_KF + s],
+                          c * C::CHUNK, kt * C::BN, un.z);
+          k_issued = jg + 1;
+          if (jg >= C::NS && !(ok = mbar_wait_w(&bars[C::B_VE + s], ((jg / C::NS) - 1) & 1, wc, 1))) break;
+          mbar_arrive_expect_tx_w(&bars[C::B_VF + s], C::TILE_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d_w(smem + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, &bars[C::B_VF + s],
+                          c * C::CHUNK, kt * C::BN, un.z);
+          v_issued = jg + 1;
+        }
+        if (!ok) break;
+        if (!claim()) break;  // the next unit, once this one's last copies are started
+      }
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+        // Let every copy already started land before the CTA can exit.
+        volatile int no_abort = 0;
+        const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+        for (int j = k_issued > C::NS ? k_issued - C::NS : 0; j < k_issued; ++j)
+          mbar_wait(&bars[C::B_KF + j % C::NS], (j / C::NS) & 1, w2, 20);
+        for (int j = v_issued > C::NS ? v_issued - C::NS : 0; j < v_issued; ++j)
+          mbar_wait(&bars[C::B_VF + j % C::NS], (j / C::NS) & 1, w2, 21);
+        if (q_units > 0)
+          for (int t = 0; t < 2; ++t) mbar_wait(&bars[C::B_Q + t], (q_units - 1) & 1, w2, 22);
+        if (asked) mbar_wait(&bars[C::B_CLC], n_asked & 1, w2, 24);
+      }
+    }
+  } else if (warp == C::W_MMA) {
+    // ---------------------------------------------------------------- UMMA issuer
+    {
+      const uint64_t dq0 = sdesc(sbase + C::OFF_Q, 16, 8 * C::ROWB, C::LAYOUT);
+      const uint64_t dk0 = sdesc(sbase + C::OFF_K, 16, 8 * C::ROWB, C::LAYOUT);
+      const uint64_t dv0 = sdesc(sbase + C::OFF_V, C::CHUNK_BYTES, 8 * C::ROWB, C::LAYOUT);
+      auto issue_s = [&](int t, int slot) {  // S_t = Q_t K^T (K in ring slot `slot`)
+        const uint64_t dq = desc_adv(dq0, (uint32_t)(t * C::TILE_BYTES));
+        const uint64_t dk = desc_adv(dk0, (uint32_t)(slot * C::TILE_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss_w(tmem + C::TMEM_S + t * 128, desc_adv(dq, kmajor_off<D>(kk)), desc_adv(dk, kmajor_off<D>(kk)),
+                    C::IDESC_S, kk > 0 ? 1u : 0u);
+        umma_commit_w(&bars[C::B_SF + t]);
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {  // O_t (+)= P_t V   (A = P from TMEM)
+        const uint64_t dv = desc_adv(dv0, (uint32_t)(slot * C::TILE_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          umma_ts_w(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * 128 + kk * 8,
+                    desc_adv(dv, (uint32_t)(kk * 16 * C::ROWB)), C::IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        umma_commit_w(&bars[C::B_O + t]);
+      };
+      int jg = 0;            // ring position of the unit's first key tile
+      int npf[2] = {0, 0};   // P tiles consumed per query tile over all units (phases of p_full)
+      bool ok = true;
+      for (int i = 0; ok; ++i) {
+        const int us = i % C::NU;
+        if (!(ok = mbar_wait_w(&bars[C::B_UF + us], (i / C::NU) & 1, wc, 13))) break;
+        const FwdUnit u = units[us];
+        mbar_arrive_w(&bars[C::B_UE + us]);
+        if (!u.live) break;
+        const TileSet ks[2] = {key_set(u.q0), key_set(u.q0 + C::BM)};
+        bool qr[2] = {false, false};  // Q_t of this unit waited for
+        auto wait_q = [&](int t) {    // (one wait per unit and tile, before its first S)
+          if (!qr[t]) {
+            if (!mbar_wait_w(&bars[C::B_Q + t], i & 1, wc, 2)) return false;
+            qr[t] = true;
+          }
+          tc_fence_after();
+          return true;
+        };
+        int n_s[2] = {0, 0}, n_pv[2] = {0, 0};  // S and P V tiles issued in this unit
+        // S_t over ring slot `slot`; Q_t is free for the next unit after its last S
+        auto s_of = [&](int t, int slot) {
+          issue_s(t, slot);
+          if (++n_s[t] == ks[t].count()) umma_commit_w(&bars[C::B_QE + t]);
+        };
+        const int first_kt = min(ks[0].next(-1), ks[1].next(-1));
+        if (first_kt != TileSet::kNone) {
+          // the unit's first S tiles (their TMEM buffers were last read by the previous
+          // unit's P V, issued earlier by this thread)
+          ok = mbar_wait_w(&bars[C::B_KF + jg % C::NS], (jg / C::NS) & 1, wc, 3);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (ok && ks[t].has(first_kt) && (ok = wait_q(t))) s_of(t, jg % C::NS);
+          if (!ok) break;
+          umma_commit_w(&bars[C::B_KE + jg % C::NS]);
+        }
+        int j = 0;
+        for (int kt = first_kt; ok && kt != TileSet::kNone; ++j) {
+          const int pos = jg + j, s = pos % C::NS, s1 = (pos + 1) % C::NS;
+          const int kn = min(ks[0].next(kt), ks[1].next(kt));
+          const bool next_k = kn != TileSet::kNone;
+          if (!(ok = mbar_wait_w(&bars[C::B_VF + s], (pos / C::NS) & 1, wc, 5))) break;
+          if (next_k && !(ok = mbar_wait_w(&bars[C::B_KF + s1], ((pos + 1) / C::NS) & 1, wc, 3))) break;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok) break;
+            const bool a = ks[t].has(kt), n = next_k && ks[t].has(kn);  // t takes part now / next
+            if (a) {  // P_t -> O_t
+              if (!(ok = mbar_wait_w(&bars[C::B_PF + t], npf[t] & 1, wc, 4))) break;
+              ++npf[t];
+              tc_fence_after();
+              issue_pv(t, s, n_pv[t] > 0);
+              ++n_pv[t];
+            }
+            if (t == 1) umma_commit_w(&bars[C::B_VE + s]);
+            if (n) {  // S_t of its next key tile, over the consumed P_t
+              if ((!a || !qr[t]) && !(ok = wait_q(t))) break;
+              s_of(t, s1);
+            }
+          }
+          if (ok && next_k) umma_commit_w(&bars[C::B_KE + s1]);
+          kt = kn;
+        }
+        if (!ok) break;
+        jg += j;
+        // a tile that sees no key in this unit: its Q is free at once
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (ok && ks[t].count() == 0 && (ok = wait_q(t))) umma_commit_w(&bars[C::B_QE + t]);
+      }
+      // Every MMA issued so far must complete before TMEM is freed.
+      umma_commit_w(&bars[C::B_DRAIN]);
+      volatile int no_abort = 0;
+      const WaitCtx w2{p.wait_limit_ns, p.status, &no_abort};
+      mbar_wait(&bars[C::B_DRAIN], 0, w2, 23);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax warpgroups
+    const int t = warp >> 2;   // which query tile of the pair
+    const int wq = warp & 3;   // TMEM lane quarter this warp may access
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t t_s = t_lane + C::TMEM_S + t * 128;
+    const uint32_t t_o = t_lane + C::TMEM_O + t * D;
+    const float sl2 = p.scale_log2;
+    int ns = 0;  // S tiles of this query tile processed over all units (phases of s_full, o_done)
+    bool ok = true;
+    for (int i = 0;; ++i) {
+      // the four warps agree to go on (a failed wait anywhere stops all of them together)
+      const int us = i % C::NU;
+      if (!named_bar_and(1 + t, 128, ok && warp_wait(&bars[C::B_UF + us], (i / C::NU) & 1, wc, 14))) break;
+      const FwdUnit u = units[us];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
+      if (!u.live) break;
+      const int qt0 = u.q0 + t * C::BM;
+      const int q_idx = qt0 + row;
+      int n_kv_all, kg, kl;  // the set is [0, kg) then [kl, ...): step n visits tile n or kl + n - kg
+      {
+        const TileSet ks = key_set(qt0);
+        n_kv_all = ks.count();
+        kg = ks.g;
+        kl = ks.L;
+      }
+      float m = -INFINITY, l = 0.f, lr = 0.f;
+      int n_kv = 0;
+      for (; n_kv < n_kv_all; ++n_kv, ++ns) {
+        if (!warp_wait(&bars[C::B_SF + t], ns & 1, wc, 6)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tmem_ld32(t_s + g * 32, s[g]);
+        tmem_wait_ld(s[0]);
+        reg_tie(s[1]);
+        reg_tie(s[2]);
+        reg_tie(s[3]);
+        // Mask keys past Nk, (causal) keys after this row's query index and keys outside
+        // the window that are not global, unless the row is global.
+        const int ka = (n_kv < kg ? n_kv : kl + (n_kv - kg)) * C::BN;
+        const bool need_mask = (ka + C::BN > p.Nk) || (CAUSAL && (ka + C::BN - 1 > qt0)) ||
+                               !(ka + C::BN <= p.lm.n_glob || qt0 + C::BM - 1 < p.lm.n_glob ||
+                                 (ka >= qt0 + C::BM - 1 - p.lm.win_l && ka + C::BN - 1 <= qt0 + p.lm.win_r));
+        if (need_mask) {
+          int lim = p.Nk - 1 - ka;  // last visible column of this tile
+          if (CAUSAL) lim = min(lim, q_idx - ka);
+          // visible: c <= lim and (c < gc or wlo <= c <= whi)
+          const bool grow = q_idx < p.lm.n_glob;
+          const int gc = grow ? C::BN : p.lm.n_glob - ka;
+          const int wlo = q_idx - p.lm.win_l - ka, whi = q_idx + p.lm.win_r - ka;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int cc = g * 32 + c;
+              if (cc > lim || (cc >= gc && (cc < wlo || cc > whi))) s[g][c] = __float_as_uint(-INFINITY);
+            }
+        }
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t* v = &s[k >> 1][(k & 1) * 16];
+          float a = fmax3(as_f(v[0]), as_f(v[1]), as_f(v[2]));
+#pragma unroll
+          for (int e = 3; e < 15; e += 2) a = fmax3(a, as_f(v[e]), as_f(v[e + 1]));
+          mx8[k] = fmaxf(a, as_f(v[15]));
+        }
+        const float mx2 =
+            fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])) * sl2;
+        float alpha = 1.f;
+        if (mx2 > m + kTau) {  // also taken on the first tile with a visible key, where m = -inf
+          alpha = ex2(m - mx2);
+          m = mx2;
+        }
+        // a row whose keys so far were all masked keeps m = -inf: subtract 0
+        const float msub = m == -INFINITY ? 0.f : m;
+        const uint64_t c2 = f2pack(sl2, sl2), nm2 = f2pack(-msub, -msub);
+        uint64_t l2[4];
+        float lra[4], lrb[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          l2[k] = 0ull;
+          lra[k] = lrb[k] = 0.f;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t pk[16];
+          softmax_weights32(s[g], c2, nm2, pk, l2, lra, lrb);
+          tmem_st16(t_s + g * 16, pk);
+        }
+        float la[8], lb[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          f2unpack(l2[k], la[2 * k], la[2 * k + 1]);
+          lb[2 * k] = lra[k];
+          lb[2 * k + 1] = lrb[k];
+        }
+        l = l * alpha + (((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7])));
+        lr = lr * alpha + (((lb[0] + lb[1]) + (lb[2] + lb[3])) + ((lb[4] + lb[5]) + (lb[6] + lb[7])));
+        // O holds P V up to the previous key tile (S of this one was issued after it)
+        if (n_kv > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int g = 0; g < D / 16; ++g) {
+            uint32_t o[16];
+            tmem_ld16(t_o + g * 16, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(as_f(o[c]) * alpha);
+            tmem_st16(t_o + g * 16, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[C::B_PF + t]);
+      }
+      // epilogue: O through the staging tile, which tile 0 takes after tile 1's store of the
+      // previous unit has read it and tile 1 after tile 0's store of this unit (a tile that
+      // sees no key stores its rows directly and still hands the staging tile on)
+      const bool has_keys = n_kv_all > 0;
+      bool go = ok && (!has_keys || warp_wait(&bars[C::B_O + t], (ns - 1) & 1, wc, 8));
+      if (t == 1) go = warp_wait(&bars[C::B_STG], i & 1, wc, 9) && go;
+      else if (i >= 1) go = warp_wait(&bars[C::B_STG1], (i - 1) & 1, wc, 9) && go;
+      go = named_bar_and(1 + t, 128, go);
+      if (go && has_keys) {
+        tc_fence_after();
+        // (a row with no visible key has lr = l = 0 and gets O = 0, L = -inf)
+        stage_o_row<D>(smem + C::OFF_STG, row, t_o, lr == 0.f ? 0.f : 1.f / lr);
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1 + t, 128);
+      if (row == 0) {
+        if (go && has_keys && qt0 < p.Nq) {
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_store_3d(&tm_o, smem + C::OFF_STG + c * C::CHUNK_BYTES, c * C::CHUNK, qt0, u.z);
+          bulk_commit_group();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(&bars[t == 0 ? C::B_STG : C::B_STG1]);  // the other tile may take the staging tile
+      }
+      if (go && q_idx < p.Nq) {
+        const size_t r = (size_t)u.z * p.Nq + q_idx;
+        if (!has_keys) {
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + r * D;
+          for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+        }
+        p.lse[r] = l == 0.f ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+      }
+      ok = ok && go;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::W_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // Merge the per-chunk partial records of the split global query rows: with M = max_c m_c,
 // O = sum_c O_c 2^(m_c - M) / sum_c lr_c 2^(m_c - M) and L = (M + log2 sum_c l_c 2^(m_c - M)) ln 2,
 // the same result as one pass over every key tile (up to rounding order).  D/8 threads per row.
@@ -1530,6 +1951,17 @@ cudaError_t launch_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const
   return cudaGetLastError();
 }
 
+template <int D, bool CAUSAL>
+cudaError_t launch_persist_local_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t st) {
+  using C = Cfg<D>;
+  auto kern = fwd_persist_local_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH), C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
 template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                      const FwdParams& p, int BH, cudaStream_t st) {
@@ -1568,6 +2000,9 @@ cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensor
                        const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t st) {
 #define TA11_FWD_CASE(DD)                                                                        \
   case DD:                                                                                       \
+    if (p.local && p.persist && p.n_gp == 0)                                                     \
+      return causal ? fwd::launch_persist_local_t<DD, true>(tq, tk, tv, to, p, BH, st)           \
+                    : fwd::launch_persist_local_t<DD, false>(tq, tk, tv, to, p, BH, st);         \
     if (p.local)                                                                                 \
       return causal ? fwd::launch_t<DD, true, false, true>(tq, tk, tv, to, p, BH, st)            \
                     : fwd::launch_t<DD, false, false, true>(tq, tk, tv, to, p, BH, st);          \
