@@ -120,12 +120,14 @@ void fa_set_wait_limit_ns(unsigned long long ns);
 int fa_set_fwd_persistent(int on);
 
 /*
- * The same choice for fa_bwd's main kernel (dense layout, no window mask, more
- * (key tile, head) units than the SMs hold at once, every key tile with at least one
- * query step, and D < 128 or Nq <= 8192, where it measured faster): 1 (default) persistent CTAs whose pipelines run on across units (the next
- * unit's K / V loads and first score GEMMs overlap the current unit's dK / dV epilogue),
- * 0 one CTA per unit.  Both compute every output bitwise the same.  Process-wide;
- * returns the previous value.
+ * The same choice for the backward's main kernel when its (key tile, head) units are more
+ * than the SMs hold at once: fa_bwd and fa_bwd_varlen with D < 128 or at most 8192 queries
+ * per head (where it measured faster), fa_bwd_window unless it splits global key tiles over
+ * query chunks (see fa_bwd_window_workspace_size).  1 (default) persistent CTAs whose
+ * pipelines run on across units (the next unit's K / V loads and first score GEMMs overlap
+ * the current unit's dK / dV epilogue), 0 one CTA per unit.  dK and dV are bitwise the same
+ * either way; dQ adds fp32 contributions in no fixed order, as fa_bwd documents.
+ * Process-wide; returns the previous value.
  */
 int fa_set_bwd_persistent(int on);
 

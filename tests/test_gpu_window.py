@@ -285,3 +285,44 @@ def test_window_forward_persistent_equals_one_cta_per_pair(p, wl, wr, g, with_or
         ro, rl = masked_ref.attention_forward(qd, kd, vd, p.scale, p.causal, wl, wr, g)
         assert_close("persistent O", f64(outs[True][0]), ro)
         assert_lse("persistent L", f64(outs[True][1]), rl)
+
+
+# The backward of an unsplit mask (no global key tiles split over query chunks) also runs
+# persistent CTAs beyond one wave: dK and dV bitwise those of one CTA per key tile, dQ (fp32
+# reductions in another order) within the parity tolerance.  Adds key tiles no query sees
+# (Nq < Nk causal: zero dK, dV) and D = 64 (dQ^T of two steps per UMMA group).
+BWD_PERSIST_CASES = PERSIST_CASES[:4] + [
+    (I.Problem(1, 32, 900, 1300, 128, True), 200, -1, 130, True),
+    (I.Problem(1, 16, 2000, 2000, 64, True), 256, -1, 0, False),
+]
+
+
+@pytest.mark.parametrize("p,wl,wr,g,with_oracle", BWD_PERSIST_CASES,
+                         ids=[f"{c[0].name()}-wl{c[1]}-wr{c[2]}-g{c[3]}" for c in BWD_PERSIST_CASES])
+def test_window_backward_persistent_equals_one_cta_per_tile(p, wl, wr, g, with_oracle):
+    q, k, v, do = I.draw(p, 8)
+    dev = torch.device("cuda")
+    qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qg)
+    lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
+    _lib.fa_fwd_window(qg, kg, vg, o, lse, p.causal, wl, wr, g, p.scale)
+    outs = {}
+    prev = _lib.fa_set_bwd_persistent(True)
+    try:
+        for on in (True, False):
+            _lib.fa_set_bwd_persistent(on)
+            dq, dk, dv = (torch.full_like(t, float("nan")) for t in (qg, kg, vg))
+            _lib.fa_bwd_window(qg, kg, vg, o, lse, dog, dq, dk, dv, p.causal, wl, wr, g, p.scale)
+            torch.cuda.synchronize()
+            outs[on] = (dq, dk, dv)
+    finally:
+        _lib.fa_set_bwd_persistent(prev)
+    assert torch.equal(outs[True][1], outs[False][1]), "dK"
+    assert torch.equal(outs[True][2], outs[False][2]), "dV"
+    assert_close("persistent dQ vs one CTA per tile", f64(outs[True][0]), f64(outs[False][0]))
+    if with_oracle:
+        qd, kd, vd, dod = (I.as_f64(t) for t in (q, k, v, do))
+        rdq, rdk, rdv = masked_ref.attention_backward(qd, kd, vd, dod, p.scale, p.causal, wl, wr, g)
+        assert_close("persistent dQ", f64(outs[True][0]), rdq)
+        assert_close("persistent dK", f64(outs[True][1]), rdk)
+        assert_close("persistent dV", f64(outs[True][2]), rdv)

@@ -596,7 +596,7 @@ struct BwdUnit {
   int k0, z, q_tok, k_tok, nq, nk, b, live;
 };
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     bwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -615,6 +615,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   // query steps of a unit: causal ones start at the diagonal; a published unit has one at least
   auto first_step = [&](const BwdUnit& u) { return CAUSAL ? u.k0 / C::BM : 0; };
   auto n_steps = [&](const BwdUnit& u) { return (u.nq + C::BM - 1) / C::BM - first_step(u); };
+  static_assert(!(LOCAL && VARLEN), "the local mask is dense only");
+  // local mask: bwd_kernel's step set of the unit's key tile, the global query steps [a, g)
+  // then the window's steps [L, hi) (every step from the causal start when the tile holds a
+  // global key); step it of the unit is query tile local_steps(u).at(it)
+  auto local_steps = [&](const BwdUnit& u) -> TileSet {
+    const int n_qt = (u.nq + C::BM - 1) / C::BM;
+    const int qlo = CAUSAL ? u.k0 : 0;  // first query that may see key k0
+    TileSet qs = TileSet::make(qlo / C::BM, qlo / C::BM, qlo / C::BM, n_qt);
+    if (u.k0 >= p.lm.n_glob) {
+      const int ke = min(u.k0 + C::BN, u.nk) - 1;
+      const int qmax = min(u.nq - 1, ke + p.lm.win_l);
+      qs = TileSet::make(qlo / C::BM, (p.lm.n_glob + C::BM - 1) / C::BM, max(qlo, u.k0 - p.lm.win_r) / C::BM,
+                         qmax >= 0 ? qmax / C::BM + 1 : 0);
+    }
+    return qs;
+  };
+  auto unit_steps = [&](const BwdUnit& u) -> int {
+    if constexpr (LOCAL) return local_steps(u).count();
+    else return n_steps(u);
+  };
   // first workspace row of the unit's (sequence, head)
   auto wrow0 = [&](const BwdUnit& u) -> long long {
     return VARLEN ? (long long)u.z * p.Nq_pad + 64LL * ((u.q_tok + 63) / 64 + u.b) : (long long)u.z * p.Nq_pad;
@@ -719,7 +739,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         un.nk = sv.Nk;
         un.b = b;
       }
-      if (n_steps(un) > 0) return true;
+      if (unit_steps(un) > 0) return true;
       const int r1 = min(un.k0 + C::BN, un.nk);
       for (int e = lane; e < (r1 - un.k0) * (D / 8); e += 32) {
         const int key = un.k0 + e / (D / 8);
@@ -742,7 +762,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       units[us] = un;  // (every lane holds the same record)
       mbar_arrive_w(&bars[C::B_UF + us]);
       if (!un.live) break;
-      const int k0 = un.k0, i0 = first_step(un), n_it = n_steps(un);
+      const int k0 = un.k0, i0 = first_step(un), n_it = unit_steps(un);
+      TileSet qs{};
+      if constexpr (LOCAL) qs = local_steps(un);
       const long long w0 = wrow0(un);
       // TMA coordinates of row r: dense maps [B*H][N][D] (y = row, z = batch*head), packed
       // maps [total][H][D] (y = head, z = token)
@@ -758,7 +780,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
       kv_units = u + 1;
       for (int it = 0; it < n_it; ++it) {
-        const int g = g0 + it, s = g % C::NS, i = i0 + it;
+        const int g = g0 + it, s = g % C::NS, i = LOCAL ? qs.at(it) : i0 + it;
         if (g >= C::NS && !(ok = mbar_wait_w(&bars[C::B_QE + s], ((g / C::NS) - 1) & 1, wc, 31))) break;
         mbar_arrive_expect_tx_w(&bars[C::B_QF + s], 2 * C::Q_TILE + 2 * C::BM * 4);
         for (int c = 0; c < C::NCHUNK; ++c) {
@@ -821,7 +843,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const BwdUnit un = units[us];
       mbar_arrive_w(&bars[C::B_UE + us]);
       if (!un.live) break;
-      const int n_it = n_steps(un);
+      const int n_it = unit_steps(un);
       if (!(ok = mbar_wait_w(&bars[C::B_KV], u & 1, wc, 32) && s_ready(g0))) break;
       tc_fence_after();
       issue_s(g0);
@@ -858,7 +880,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const BwdUnit un = units[us];
       mbar_arrive_w(&bars[C::B_UE + us]);
       if (!un.live) break;
-      const int n_it = n_steps(un);
+      const int n_it = unit_steps(un);
       // dV and dK start from zero: the previous unit's epilogue must have read them out
       if (u >= 1 && !(ok = mbar_wait_w(&bars[C::B_ACCE], (u - 1) & 1, wc, 56))) break;
       for (int it = 0; ok && it < n_it; ++it) {
@@ -928,10 +950,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
       if (!un.live) break;
-      const int k0 = un.k0, key = k0 + row, i0 = first_step(un), n_it = n_steps(un);
+      const int k0 = un.k0, key = k0 + row, i0 = first_step(un), n_it = unit_steps(un);
+      TileSet qs{};
+      if constexpr (LOCAL) qs = local_steps(un);
       const int nk = VARLEN ? un.nk : p.Nk;  // (dense: the kernel parameter)
       for (int it = 0; it < n_it && ok; ++it) {
-        const int g = g0 + it, s = g % C::NS, i = i0 + it;
+        const int g = g0 + it, s = g % C::NS, i = LOCAL ? qs.at(it) : i0 + it;
         const int b = g % C::NB, ph = (g / C::NB) & 1;
         const uint32_t t_sb = (uint32_t)(b * 64);  // this step's S^T / P^T buffer
         if (!warp_wait(&bars[C::B_QF + s], (g / C::NS) & 1, wc, 38) ||
@@ -946,14 +970,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const float* lse2 = reinterpret_cast<const float*>(smem + C::OFF_LSE + s * C::BM * 4) + col0;
         const float* dlt = reinterpret_cast<const float*>(smem + C::OFF_DLT + s * C::BM * 4) + col0;
         const int qb = i * C::BM + col0;  // query of column 0 of this warpgroup's half
-        const bool need_mask = (k0 + C::BN > nk) || (CAUSAL && (k0 + C::BN - 1 > qb));
+        bool need_mask = (k0 + C::BN > nk) || (CAUSAL && (k0 + C::BN - 1 > qb));
+        if (LOCAL)
+          need_mask = need_mask || !(k0 + C::BN <= p.lm.n_glob || qb + 31 < p.lm.n_glob ||
+                                     (k0 >= qb + 31 - p.lm.win_l && k0 + C::BN - 1 <= qb + p.lm.win_r));
         const int lim = CAUSAL ? key - qb : (1 << 30);  // columns c with q = qb + c < key are masked
         const bool key_valid = key < nk;
+        // local: for a non-global key, columns c >= gq (non-global queries) are visible only
+        // inside the window key - win_r <= q <= key + win_l
+        const bool kglob = !LOCAL || key < p.lm.n_glob;
+        const int gq = p.lm.n_glob - qb, wlo = key - p.lm.win_r - qb, whi = key + p.lm.win_l - qb;
         float pv[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           float x = ex2(fmaf(as_f(sreg[c]), sl2, -lse2[c]));
           if (need_mask && (!key_valid || (CAUSAL && c < lim))) x = 0.f;
+          if (LOCAL && need_mask && !kglob && c >= gq && (c < wlo || c > whi)) x = 0.f;
           pv[c] = x;
         }
         uint32_t pk[16];
@@ -1030,7 +1062,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::B_UE + us]);
       if (!un.live) break;
-      const int i0 = first_step(un), n_it = n_steps(un);
+      const int i0 = first_step(un), n_it = unit_steps(un);
+      TileSet qs{};
+      if constexpr (LOCAL) qs = local_steps(un);
       const long long w0 = wrow0(un);
       // K^T into TMEM for this unit (lane d holds K[key][d] for all 128 keys as bf16 pairs,
       // lanes d >= D zeros) once K has landed and the previous unit's dQ^T MMAs are done
@@ -1076,7 +1110,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         reg_tie(v1);
         tc_fence_before();
         mbar_arrive(&bars[C::B_DQE + b]);
-        float* gdst = p.dq_accum + ((size_t)w0 + (size_t)(i0 + it) * C::BM) * D;
+        float* gdst = p.dq_accum + ((size_t)w0 + (size_t)(LOCAL ? qs.at(it) : i0 + it) * C::BM) * D;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -1246,11 +1280,11 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool VARLEN = false>
+template <int D, bool CAUSAL, bool VARLEN = false, bool LOCAL = false>
 cudaError_t launch_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                              const BwdParams& p, int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = bwd_persist_kernel<D, CAUSAL, VARLEN>;
+  auto kern = bwd_persist_kernel<D, CAUSAL, VARLEN, LOCAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   dim3 grid = VARLEN ? dim3((unsigned)((p.va.total_k >> 7) + p.va.B), (unsigned)p.va.H)
@@ -1289,6 +1323,10 @@ cudaError_t conv_t(const ConvParams& p, cudaStream_t st) {
 
 cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int BH, cudaStream_t st) {
+  if (p.local && p.persist && p.n_gk == 0) {
+    TA11_SWITCH_D(D, (causal ? bwd::launch_persist_t<DD, true, false, true>(tq, tk, tv, tdo, p, BH, st)
+                             : bwd::launch_persist_t<DD, false, false, true>(tq, tk, tv, tdo, p, BH, st)))
+  }
   if (p.local) {
     TA11_SWITCH_D(D, (causal ? bwd::launch_t<DD, true, false, true>(tq, tk, tv, tdo, p, BH, st)
                              : bwd::launch_t<DD, false, false, true>(tq, tk, tv, tdo, p, BH, st)))
