@@ -122,11 +122,13 @@ int fa_set_fwd_persistent(int on);
 /*
  * The same choice for the backward's main kernel when its (key tile, head) units are more
  * than the SMs hold at once: fa_bwd and fa_bwd_varlen with D < 128 or at most 8192 queries
- * per head (where it measured faster), fa_bwd_window unless it splits global key tiles over
- * query chunks (see fa_bwd_window_workspace_size).  1 (default) persistent CTAs whose
+ * per head (where it measured faster), and fa_bwd_window (its split global key tiles'
+ * chunks included, see fa_bwd_window_workspace_size).  1 (default) persistent CTAs whose
  * pipelines run on across units (the next unit's K / V loads and first score GEMMs overlap
  * the current unit's dK / dV epilogue), 0 one CTA per unit.  dK and dV are bitwise the same
- * either way; dQ adds fp32 contributions in no fixed order, as fa_bwd documents.
+ * either way, except the rows of split global key tiles (their chunks' fp32 partial sums
+ * are added in no fixed order); dQ adds fp32 contributions in no fixed order, as fa_bwd
+ * documents.
  * Process-wide; returns the previous value.
  */
 int fa_set_bwd_persistent(int on);

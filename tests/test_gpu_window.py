@@ -326,3 +326,46 @@ def test_window_backward_persistent_equals_one_cta_per_tile(p, wl, wr, g, with_o
         assert_close("persistent dQ", f64(outs[True][0]), rdq)
         assert_close("persistent dK", f64(outs[True][1]), rdk)
         assert_close("persistent dV", f64(outs[True][2]), rdv)
+
+
+# Split global key tiles (global tokens, more than 64 query steps) in the persistent
+# backward: their chunks add partial dK, dV into the fp32 area in no fixed order, so those
+# rows (the first ceil(G/128) key tiles) agree within tolerance; every other row bitwise.
+BWD_PERSIST_SPLIT_CASES = [
+    (I.Problem(1, 8, 4200, 4200, 64, True), 300, -1, 64),
+    (I.Problem(1, 5, 4500, 4500, 128, False), 200, 100, 150),
+]
+
+
+@pytest.mark.parametrize("p,wl,wr,g", BWD_PERSIST_SPLIT_CASES,
+                         ids=[f"{c[0].name()}-wl{c[1]}-wr{c[2]}-g{c[3]}" for c in BWD_PERSIST_SPLIT_CASES])
+def test_window_backward_persistent_with_split_key_tiles(p, wl, wr, g):
+    assert _lib.fa_bwd_window_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D, wl, wr, g) > \
+        _lib.fa_bwd_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D), "the case must split"
+    q, k, v, do = I.draw(p, 9)
+    dev = torch.device("cuda")
+    qg, kg, vg, dog = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qg)
+    lse = torch.empty((p.B, p.H, p.Nq), dtype=torch.float32, device=dev)
+    _lib.fa_fwd_window(qg, kg, vg, o, lse, p.causal, wl, wr, g, p.scale)
+    outs = {}
+    prev = _lib.fa_set_bwd_persistent(True)
+    try:
+        for on in (True, False):
+            _lib.fa_set_bwd_persistent(on)
+            dq, dk, dv = (torch.full_like(t, float("nan")) for t in (qg, kg, vg))
+            _lib.fa_bwd_window(qg, kg, vg, o, lse, dog, dq, dk, dv, p.causal, wl, wr, g, p.scale)
+            torch.cuda.synchronize()
+            outs[on] = (dq, dk, dv)
+    finally:
+        _lib.fa_set_bwd_persistent(prev)
+    ks = (g + 127) // 128 * 128  # rows of the split global key tiles
+    for n, i in (("dK", 1), ("dV", 2)):
+        a, b = outs[True][i], outs[False][i]
+        assert torch.equal(a[:, :, ks:], b[:, :, ks:]), f"{n} outside the split tiles"
+        assert_close(f"{n} of the split tiles", f64(a[:, :, :ks]), f64(b[:, :, :ks]))
+    qd, kd, vd, dod = (I.as_f64(t) for t in (q, k, v, do))
+    rdq, rdk, rdv = masked_ref.attention_backward(qd, kd, vd, dod, p.scale, p.causal, wl, wr, g)
+    assert_close("persistent dQ", f64(outs[True][0]), rdq)
+    assert_close("persistent dK", f64(outs[True][1]), rdk)
+    assert_close("persistent dV", f64(outs[True][2]), rdv)

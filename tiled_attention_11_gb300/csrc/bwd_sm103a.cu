@@ -593,10 +593,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 // z = batch*head, q_tok = k_tok = b = 0, nq = Nq, nk = Nk; packed: z = head, q_tok / k_tok
 // the sequence's first tokens, nq / nk its lengths, b its index.  live = 0 ends the ring.
 struct BwdUnit {
-  int k0, z, q_tok, k_tok, nq, nk, b, live;
+  int k0, z, q_tok, k_tok, nq, nk, b, live;  // b: packed, the sequence; local mask, the query
+                                              // chunk of a split global key tile (-1: none)
 };
 
-template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false>
+// SPLIT (local mask only): the launch also holds the chunks of split global key tiles
+template <int D, bool CAUSAL, bool VARLEN, bool LOCAL = false, bool SPLIT = false>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     bwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -616,6 +618,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   auto first_step = [&](const BwdUnit& u) { return CAUSAL ? u.k0 / C::BM : 0; };
   auto n_steps = [&](const BwdUnit& u) { return (u.nq + C::BM - 1) / C::BM - first_step(u); };
   static_assert(!(LOCAL && VARLEN), "the local mask is dense only");
+  static_assert(LOCAL || !SPLIT, "only the local mask splits key tiles");
   // local mask: bwd_kernel's step set of the unit's key tile, the global query steps [a, g)
   // then the window's steps [L, hi) (every step from the causal start when the tile holds a
   // global key); step it of the unit is query tile local_steps(u).at(it)
@@ -628,6 +631,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       const int qmax = min(u.nq - 1, ke + p.lm.win_l);
       qs = TileSet::make(qlo / C::BM, (p.lm.n_glob + C::BM - 1) / C::BM, max(qlo, u.k0 - p.lm.win_r) / C::BM,
                          qmax >= 0 ? qmax / C::BM + 1 : 0);
+    }
+    if (SPLIT && u.b >= 0) {  // a chunk of a split global key tile: its query steps only
+      const int lo = u.b * p.split_q, hi = lo + p.split_q;
+      qs = TileSet::make(max(qs.a, lo), min(qs.g, hi), max(qs.L, lo), min(qs.hi, hi));
     }
     return qs;
   };
@@ -715,7 +722,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         // lpt: units in longest-first order over all heads (key tile 0 of every head, then
         // key tile 1, ...), for causal launches of a few waves whose tail would otherwise be
         // one head's heaviest key tiles starting last
-        int kt = ux, zz = uy;
+        int kt = ux, zz = uy, chunk = -1;
+        if (SPLIT) {  // bwd_kernel's grid: the split global key tiles' chunks first
+          const int n_split_ctas = p.n_gk * p.n_qsplit;
+          if (kt < n_split_ctas) {
+            chunk = kt % p.n_qsplit;
+            kt = kt / p.n_qsplit;
+          } else {
+            kt = kt - n_split_ctas + p.n_gk;
+          }
+        }
         if (p.lpt) {
           const int lin = uy * (int)gridDim.x + ux;
           kt = lin / (int)gridDim.y;
@@ -723,7 +739,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         }
         un.k0 = kt * C::BN;
         un.z = zz;
-        un.q_tok = un.k_tok = un.b = 0;
+        un.q_tok = un.k_tok = 0;
+        un.b = SPLIT ? chunk : 0;
         un.nq = p.Nq;
         un.nk = p.Nk;
       } else {
@@ -740,6 +757,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         un.b = b;
       }
       if (unit_steps(un) > 0) return true;
+      if (SPLIT && un.b >= 0) return false;  // a chunk with no step adds nothing to dkv_accum
       const int r1 = min(un.k0 + C::BN, un.nk);
       for (int e = lane; e < (r1 - un.k0) * (D / 8); e += 32) {
         const int key = un.k0 + e / (D / 8);
@@ -1034,15 +1052,33 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       g0 += n_it;
       if (!(ok = ok && warp_wait(&bars[C::B_DQF + gl % C::NB], (gl / C::NB) & 1, wc, 45))) break;
       tc_fence_after();
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) +
-                           (VARLEN ? ((size_t)(un.k_tok + key) * p.va.H + un.z) * D : ((size_t)un.z * p.Nk + key) * D);
-      const float mul = (wg == 0) ? p.scale : 1.f;
+      if (SPLIT && un.b >= 0) {
+        // partial sums of a split global key tile: add (unscaled) into dkv_accum, as bwd_kernel
+        float* acc = p.dkv_accum + (((size_t)un.z * (p.n_gk * C::BN) + (size_t)key) * 2 + wg) * D;
 #pragma unroll
-      for (int gg = 0; gg < D / 16; ++gg) {
-        uint32_t v[16];
-        tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + gg * 16, v);
-        tmem_wait_ld(v);
-        if (key < nk) store16_bf16(dst + gg * 16, v, mul);
+        for (int gg = 0; gg < D / 16; ++gg) {
+          uint32_t v[16];
+          tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + gg * 16, v);
+          tmem_wait_ld(v);
+          if (key < nk) {
+#pragma unroll
+            for (int c = 0; c < 16; c += 4)
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(acc + gg * 16 + c), "f"(as_f(v[c])),
+                           "f"(as_f(v[c + 1])), "f"(as_f(v[c + 2])), "f"(as_f(v[c + 3]))
+                           : "memory");
+          }
+        }
+      } else {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dk : p.dv) +
+                             (VARLEN ? ((size_t)(un.k_tok + key) * p.va.H + un.z) * D : ((size_t)un.z * p.Nk + key) * D);
+        const float mul = (wg == 0) ? p.scale : 1.f;
+#pragma unroll
+        for (int gg = 0; gg < D / 16; ++gg) {
+          uint32_t v[16];
+          tmem_ld16(t_lane + (wg == 0 ? C::T_DK : C::T_DV) + gg * 16, v);
+          tmem_wait_ld(v);
+          if (key < nk) store16_bf16(dst + gg * 16, v, mul);
+        }
       }
       tc_fence_before();
       mbar_arrive(&bars[C::B_ACCE]);
@@ -1280,15 +1316,16 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool VARLEN = false, bool LOCAL = false>
+template <int D, bool CAUSAL, bool VARLEN = false, bool LOCAL = false, bool SPLIT = false>
 cudaError_t launch_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                              const BwdParams& p, int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = bwd_persist_kernel<D, CAUSAL, VARLEN, LOCAL>;
+  auto kern = bwd_persist_kernel<D, CAUSAL, VARLEN, LOCAL, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
+  const int gx = SPLIT ? p.n_gk * p.n_qsplit + (p.n_k_tiles - p.n_gk) : p.n_k_tiles;
   dim3 grid = VARLEN ? dim3((unsigned)((p.va.total_k >> 7) + p.va.B), (unsigned)p.va.H)
-                     : dim3((unsigned)p.n_k_tiles, (unsigned)BH);
+                     : dim3((unsigned)gx, (unsigned)BH);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
@@ -1323,7 +1360,11 @@ cudaError_t conv_t(const ConvParams& p, cudaStream_t st) {
 
 cudaError_t launch_bwd(int D, bool causal, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int BH, cudaStream_t st) {
-  if (p.local && p.persist && p.n_gk == 0) {
+  if (p.local && p.persist && p.n_gk > 0) {
+    TA11_SWITCH_D(D, (causal ? bwd::launch_persist_t<DD, true, false, true, true>(tq, tk, tv, tdo, p, BH, st)
+                             : bwd::launch_persist_t<DD, false, false, true, true>(tq, tk, tv, tdo, p, BH, st)))
+  }
+  if (p.local && p.persist) {
     TA11_SWITCH_D(D, (causal ? bwd::launch_persist_t<DD, true, false, true>(tq, tk, tv, tdo, p, BH, st)
                              : bwd::launch_persist_t<DD, false, false, true>(tq, tk, tv, tdo, p, BH, st)))
   }

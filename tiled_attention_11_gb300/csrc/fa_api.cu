@@ -448,8 +448,8 @@ int bwd_dense(const void* q, const void* k, const void* v, const void* o, const 
   // persistent kernel: more CTAs than one wave.  It saves a fixed time per unit; with
   // D = 128 and more than 128 query steps per unit it measured about 1% slower than one CTA
   // per unit, so those keep one CTA per unit.  A window mask keeps units short whatever Nq
-  // is; it goes persistent unless global key tiles are split over query chunks.
-  const bool short_units = lm ? split.n_gk == 0 : (D < 128 || Nq <= 8192);
+  // is (a split global key tile's chunks included).
+  const bool short_units = lm || D < 128 || Nq <= 8192;
   bp.persist = (short_units && (long long)bp.n_k_tiles * BH > current_sms()) ? g_bwd_persist.load() : 0;
   // causal launches of a few waves (persistent or not): longest-first over all heads
   bp.lpt = (!lm && causal && (long long)bp.n_k_tiles * BH <= 8LL * current_sms()) ? g_lpt.load() : 0;
