@@ -106,10 +106,10 @@ int fa_device_status(unsigned* site, int reset);
 void fa_set_wait_limit_ns(unsigned long long ns);
 
 /*
- * Schedule of the forward kernels (fa_fwd, fa_fwd_varlen, fa_fwd_fp8, and fa_fwd_window
- * unless it splits global query rows over key chunks, see fa_fwd_window_workspace_size)
- * when their (query-tile pair, head) units are more than the SMs can hold at once (no
- * counterpart on the pages; a scheduling choice, not a change of the result):
+ * Schedule of the forward kernels (fa_fwd, fa_fwd_varlen, fa_fwd_fp8, fa_fwd_window, the
+ * key chunks of its split global query rows included) when their (query-tile pair, head)
+ * units are more than the SMs can hold at once (no counterpart on the pages; a scheduling
+ * choice, not a change of the result):
  *   1 (default)  persistent CTAs: a CTA that finishes a unit takes over the next CTA of
  *                its grid that has not started, so one CTA's pipelines run on across
  *                units (the next unit's loads and first score GEMMs overlap the current

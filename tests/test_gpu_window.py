@@ -369,3 +369,19 @@ def test_window_backward_persistent_with_split_key_tiles(p, wl, wr, g):
     assert_close("persistent dQ", f64(outs[True][0]), rdq)
     assert_close("persistent dK", f64(outs[True][1]), rdk)
     assert_close("persistent dV", f64(outs[True][2]), rdv)
+
+
+# Split global query rows (non-causal, global tokens, more than 32 key tiles) in the
+# persistent forward: the key chunks' partial records are the one-CTA kernel's and
+# combine_kernel merges them in a fixed order, so O and L agree bit for bit.
+FWD_PERSIST_SPLIT_CASES = [
+    (I.Problem(1, 24, 4500, 4500, 64, False), 200, 200, 128, True),
+    (I.Problem(2, 10, 4200, 4200, 128, False), 300, 100, 300, False),
+]
+
+
+@pytest.mark.parametrize("p,wl,wr,g,with_oracle", FWD_PERSIST_SPLIT_CASES,
+                         ids=[f"{c[0].name()}-wl{c[1]}-wr{c[2]}-g{c[3]}" for c in FWD_PERSIST_SPLIT_CASES])
+def test_window_forward_persistent_with_split_rows(p, wl, wr, g, with_oracle):
+    assert _lib.fa_fwd_window_workspace_size(p.B, p.H, p.Nq, p.Nk, p.D, p.causal, wl, wr, g) > 0, "must split"
+    test_window_forward_persistent_equals_one_cta_per_pair(p, wl, wr, g, with_oracle)

@@ -250,8 +250,7 @@ def fa_set_wait_limit_ns(ns: int) -> None:
 
 def fa_set_fwd_persistent(on: bool) -> bool:
     """C ``fa_set_fwd_persistent``: the forward's schedule beyond one wave of CTAs (dense,
-    packed, FP8 and unsplit window masks; persistent CTAs by default); returns the previous
-    setting."""
+    packed, FP8 and window masks; persistent CTAs by default); returns the previous setting."""
     return bool(lib().fa_set_fwd_persistent(int(bool(on))))
 
 

@@ -333,9 +333,9 @@ int fwd_dense(const void* q, const void* k, const void* v, void* o, float* lse, 
   // (tile t with tile n-1-t) so that every CTA walks about the same number of key tiles.
   const long long n_ctas = (long long)BH * ((p.n_q_tiles + 1) / 2);
   p.fold = (!lm && causal && n_ctas <= current_sms()) ? 1 : 0;
-  // persistent CTAs beyond one wave; with the local mask only when no global query rows are
-  // split over key chunks (their partial records take the one-CTA-per-unit kernel)
-  p.persist = (!p.fold && n_ctas > current_sms() && (!lm || split.n_gp == 0)) ? g_fwd_persist.load() : 0;
+  // persistent CTAs beyond one wave (with the local mask, split global rows' key chunks
+  // included: the split is non-causal only)
+  p.persist = (!p.fold && n_ctas > current_sms()) ? g_fwd_persist.load() : 0;
   // causal launches of up to eight waves: longest-first over all heads, so no head's
   // heaviest pairs start last (the layer's 13 waves keep head-by-head order for L2 locality)
   p.lpt = (!lm && p.persist && causal && n_ctas <= 8LL * current_sms()) ? g_lpt.load() : 0;

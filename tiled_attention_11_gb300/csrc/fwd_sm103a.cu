@@ -1150,7 +1150,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 // unit, also for a tile that sees no key (its rows get O = 0, L = -inf), so the phases stay
 // in step.  Per-row arithmetic and key order are fwd_kernel's.
 // ------------------------------------------------------------------------------------
-template <int D, bool CAUSAL>
+// SPLIT: the launch also holds the key chunks of split global query rows (non-causal mask
+// with global tokens): unit `pad` is the chunk (-1: none) and its rows get partial records
+// for combine_kernel instead of O and L, as in fwd_kernel.
+template <int D, bool CAUSAL, bool SPLIT = false>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     fwd_persist_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -1176,6 +1179,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     const int hi = kmax >= 0 ? kmax / C::BN + 1 : 0;
     if (qa < p.lm.n_glob) return TileSet::make(0, 0, 0, hi);
     return TileSet::make(0, (p.lm.n_glob + C::BN - 1) / C::BN, max(qa - p.lm.win_l, 0) / C::BN, hi);
+  };
+  // the set restricted to a unit's key chunk (split global rows)
+  auto unit_set = [&](int qa, int chunk) -> TileSet {
+    const TileSet ks = key_set(qa);
+    if (!SPLIT || chunk < 0) return ks;
+    const int lo = chunk * p.split_t, hi = lo + p.split_t;
+    return TileSet::make(max(ks.a, lo), min(ks.g, hi), max(ks.L, lo), min(ks.hi, hi));
   };
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
 
@@ -1239,13 +1249,23 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       };
       for (int i = 0;; ++i) {
         FwdUnit un;
+        int pair = ux, chunk = -1;
+        if (SPLIT) {  // fwd_kernel's grid: the split global pairs' key chunks first
+          const int n_split_ctas = p.n_gp * p.n_split;
+          if (pair < n_split_ctas) {
+            chunk = pair % p.n_split;
+            pair = pair / p.n_split;
+          } else {
+            pair = pair - n_split_ctas + p.n_gp;
+          }
+        }
         un.live = ux >= 0 ? 1 : 0;
-        un.q0 = ux * 2 * C::BM;  // pairs in launch order: those holding global rows first
+        un.q0 = pair * 2 * C::BM;  // pairs in launch order: those holding global rows first
         un.z = uy;
         un.q_tok = un.k_tok = 0;
         un.nq = p.Nq;
         un.nk = p.Nk;
-        un.pad = 0;
+        un.pad = chunk;
         bool ok = true;
         const int us = i % C::NU;
         if (i >= C::NU && !mbar_wait_w(&bars[C::B_UE + us], ((i / C::NU) - 1) & 1, wc, 10)) break;
@@ -1253,7 +1273,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mbar_arrive_w(&bars[C::B_UF + us]);
         if (!un.live) break;
         const int q0 = un.q0;
-        const TileSet ks0 = key_set(q0), ks1 = key_set(q0 + C::BM);
+        const TileSet ks0 = unit_set(q0, un.pad), ks1 = unit_set(q0 + C::BM, un.pad);
         for (int t = 0; t < 2 && ok; ++t) {  // Q_t is free once the last S MMA reading it is done
           if (i >= 1 && !(ok = mbar_wait_w(&bars[C::B_QE + t], (i - 1) & 1, wc, 11))) break;
           mbar_arrive_expect_tx_w(&bars[C::B_Q + t], C::TILE_BYTES);
@@ -1327,7 +1347,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         const FwdUnit u = units[us];
         mbar_arrive_w(&bars[C::B_UE + us]);
         if (!u.live) break;
-        const TileSet ks[2] = {key_set(u.q0), key_set(u.q0 + C::BM)};
+        const TileSet ks[2] = {unit_set(u.q0, u.pad), unit_set(u.q0 + C::BM, u.pad)};
         bool qr[2] = {false, false};  // Q_t of this unit waited for
         auto wait_q = [&](int t) {    // (one wait per unit and tile, before its first S)
           if (!qr[t]) {
@@ -1415,10 +1435,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       if (!u.live) break;
       const int qt0 = u.q0 + t * C::BM;
       const int q_idx = qt0 + row;
-      int n_kv_all, kg, kl;  // the set is [0, kg) then [kl, ...): step n visits tile n or kl + n - kg
+      // the set is [ka0, kg) then [kl, ...): step n visits tile ka0 + n or kl + n - (kg - ka0)
+      // (ka0 = 0 unless a key chunk starts later)
+      int n_kv_all, ka0, kg, kl;
       {
-        const TileSet ks = key_set(qt0);
+        const TileSet ks = unit_set(qt0, u.pad);
         n_kv_all = ks.count();
+        ka0 = SPLIT ? ks.a : 0;
         kg = ks.g;
         kl = ks.L;
       }
@@ -1439,7 +1462,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         reg_tie(s[3]);
         // Mask keys past Nk, (causal) keys after this row's query index and keys outside
         // the window that are not global, unless the row is global.
-        const int ka = (n_kv < kg ? n_kv : kl + (n_kv - kg)) * C::BN;
+        const int ka = (n_kv < kg - ka0 ? ka0 + n_kv : kl + (n_kv - (kg - ka0))) * C::BN;
         const bool need_mask = (ka + C::BN > p.Nk) || (CAUSAL && (ka + C::BN - 1 > qt0)) ||
                                !(ka + C::BN <= p.lm.n_glob || qt0 + C::BM - 1 < p.lm.n_glob ||
                                  (ka >= qt0 + C::BM - 1 - p.lm.win_l && ka + C::BN - 1 <= qt0 + p.lm.win_r));
@@ -1523,6 +1546,37 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       if (t == 1) go = warp_wait(&bars[C::B_STG], i & 1, wc, 9) && go;
       else if (i >= 1) go = warp_wait(&bars[C::B_STG1], (i - 1) & 1, wc, 9) && go;
       go = named_bar_and(1 + t, 128, go);
+      if (SPLIT && u.pad >= 0) {
+        // partial record of this key chunk: unnormalised O accumulator, m, l, lr (the
+        // staging tile is not used and is handed on at once)
+        if (go) {
+          const bool rv = q_idx < p.Nq;
+          const size_t rec = ((size_t)u.z * (p.n_gp * 2 * C::BM) + q_idx) * p.n_split + u.pad;
+          float* po = p.part_o + rec * D;
+          if (has_keys) {
+            tc_fence_after();
+#pragma unroll
+            for (int g = 0; g < D / 16; ++g) {
+              uint32_t o[16];
+              tmem_ld16(t_o + g * 16, o);
+              tmem_wait_ld(o);
+#pragma unroll
+              for (int c = 0; c < 16; c += 4)
+                if (rv)
+                  *reinterpret_cast<float4*>(po + g * 16 + c) =
+                      make_float4(as_f(o[c]), as_f(o[c + 1]), as_f(o[c + 2]), as_f(o[c + 3]));
+            }
+          } else if (rv) {
+            for (int d = 0; d < D; d += 4) *reinterpret_cast<float4*>(po + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          if (rv)
+            *reinterpret_cast<float4*>(p.part_ml + rec * 4) =
+                has_keys ? make_float4(m, l, lr, 0.f) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+        }
+        if (row == 0) mbar_arrive(&bars[t == 0 ? C::B_STG : C::B_STG1]);
+        ok = ok && go;
+        continue;
+      }
       if (go && has_keys) {
         tc_fence_after();
         // (a row with no visible key has lr = l = 0 and gets O = 0, L = -inf)
@@ -1951,14 +2005,16 @@ cudaError_t launch_persist_t(const CUtensorMap& tq, const CUtensorMap& tk, const
   return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT = false>
 cudaError_t launch_persist_local_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                    const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t st) {
   using C = Cfg<D>;
-  auto kern = fwd_persist_local_kernel<D, CAUSAL>;
+  auto kern = fwd_persist_local_kernel<D, CAUSAL, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  kern<<<dim3((unsigned)((p.n_q_tiles + 1) / 2), (unsigned)BH), C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, to, p);
+  const int n_pairs = (p.n_q_tiles + 1) / 2;
+  const int gx = SPLIT ? p.n_gp * p.n_split + (n_pairs - p.n_gp) : n_pairs;
+  kern<<<dim3((unsigned)gx, (unsigned)BH), C::THREADS, C::SMEM_ALLOC, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -2000,7 +2056,9 @@ cudaError_t launch_fwd(int D, bool causal, const CUtensorMap& tq, const CUtensor
                        const CUtensorMap& to, const FwdParams& p, int BH, cudaStream_t st) {
 #define TA11_FWD_CASE(DD)                                                                        \
   case DD:                                                                                       \
-    if (p.local && p.persist && p.n_gp == 0)                                                     \
+    if (p.local && p.persist && p.n_gp > 0) /* (split global rows: non-causal only) */            \
+      return fwd::launch_persist_local_t<DD, false, true>(tq, tk, tv, to, p, BH, st);            \
+    if (p.local && p.persist)                                                                    \
       return causal ? fwd::launch_persist_local_t<DD, true>(tq, tk, tv, to, p, BH, st)           \
                     : fwd::launch_persist_local_t<DD, false>(tq, tk, tv, to, p, BH, st);         \
     if (p.local)                                                                                 \
