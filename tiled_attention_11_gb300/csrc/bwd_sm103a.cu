@@ -744,12 +744,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         un.nq = p.Nq;
         un.nk = p.Nk;
       } else {
-        const int b = slot_seq(p.va.cu_k, p.va.B, p.va.total_k, 7, ux);
-        const int kt = ux - slot_base(p.va.cu_k, p.va.total_k, 7, b);
-        const SeqView sv = seq_view<true>(p.va, p.Nq, p.Nk, b * p.va.H + uy);
+        // lpt: slot-major over the heads (slot x of every head, then slot x + 1), so the
+        // heaviest key tiles of a long sequence start while the other heads' work remains
+        int sx = ux, hy = uy;
+        if (p.lpt) {
+          const int lin = uy * (int)gridDim.x + ux;
+          sx = lin / (int)gridDim.y;
+          hy = lin % (int)gridDim.y;
+        }
+        const int b = slot_seq(p.va.cu_k, p.va.B, p.va.total_k, 7, sx);
+        const int kt = sx - slot_base(p.va.cu_k, p.va.total_k, 7, b);
+        const SeqView sv = seq_view<true>(p.va, p.Nq, p.Nk, b * p.va.H + hy);
         if (kt * C::BN >= sv.Nk) return false;
         un.k0 = kt * C::BN;
-        un.z = uy;
+        un.z = hy;
         un.q_tok = sv.q_tok;
         un.k_tok = sv.k_tok;
         un.nq = sv.Nq;

@@ -717,6 +717,9 @@ extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* 
   p.va = ta11::VarlenArgs{cu_seqlens_q, cu_seqlens_k, H, total_q, total_k, B};
   // persistent CTAs beyond one wave (compact slots of 256 queries per head, see slot_seq)
   p.persist = ((long long)((total_q >> 8) + B) * H > current_sms()) ? g_fwd_persist.load() : 0;
+  // causal packed batches: slot-major claim order over the heads, so a long sequence's
+  // heaviest pairs do not start at the end of the launch for the last heads
+  p.lpt = (p.persist && causal) ? g_lpt.load() : 0;
   return ta11::launch_fwd(D, causal != 0, tq, tk, tv, tq, p, B * H, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -782,6 +785,7 @@ extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const 
   // persistent kernel beyond one wave of compact 128-key slots (slot_seq), as for the dense layout
   bp.persist = ((D < 128 || max_seqlen_q <= 8192) && (long long)((total_k >> 7) + B) * H > current_sms())
                    ? g_bwd_persist.load() : 0;
+  bp.lpt = (bp.persist && causal) ? g_lpt.load() : 0;  // (as the forward: slot-major over the heads)
   if (ta11::launch_bwd(D, causal != 0, tq, tk, tv, tdo, bp, B * H, stream) != cudaSuccess) return FA_ERR_LAUNCH;
   ta11::ConvParams cp{dq_accum, dq, B * H, max_seqlen_q, w.Nq_pad, scale, va};
   if (ta11::launch_bwd_convert(D, cp, stream) != cudaSuccess) return FA_ERR_LAUNCH;

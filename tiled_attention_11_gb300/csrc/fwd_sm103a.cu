@@ -815,13 +815,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           un.nk = p.Nk;
           return true;
         }
-        const int b = slot_seq(p.va.cu_q, p.va.B, p.va.total_q, 8, ux);
-        const int j = ux - slot_base(p.va.cu_q, p.va.total_q, 8, b);
-        const SeqView sv = seq_view<true>(p.va, p.Nq, p.Nk, b * p.va.H + uy);
+        // lpt: slot-major over the heads (slot x of every head, then slot x + 1), so the
+        // heaviest pairs of a long sequence start while the other heads' work remains
+        int sx = ux, hy = uy;
+        if (p.lpt) {
+          const int lin = uy * (int)gridDim.x + ux;
+          sx = lin / (int)gridDim.y;
+          hy = lin % (int)gridDim.y;
+        }
+        const int b = slot_seq(p.va.cu_q, p.va.B, p.va.total_q, 8, sx);
+        const int j = sx - slot_base(p.va.cu_q, p.va.total_q, 8, b);
+        const SeqView sv = seq_view<true>(p.va, p.Nq, p.Nk, b * p.va.H + hy);
         const int n_pairs = (sv.Nq + 2 * C::BM - 1) / (2 * C::BM);
         if (j >= n_pairs) return false;
         un.q0 = (n_pairs - 1 - j) * 2 * C::BM;  // heaviest pair of the sequence first
-        un.z = uy;
+        un.z = hy;
         un.q_tok = sv.q_tok;
         un.k_tok = sv.k_tok;
         un.nq = sv.Nq;
@@ -831,9 +839,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         for (int e = lane; e < (r1 - un.q0) * (D / 8); e += 32) {
           const int q = un.q0 + e / (D / 8);
           reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
-                                   ((size_t)(sv.q_tok + q) * p.va.H + uy) * D)[e % (D / 8)] = make_uint4(0, 0, 0, 0);
+                                   ((size_t)(sv.q_tok + q) * p.va.H + hy) * D)[e % (D / 8)] = make_uint4(0, 0, 0, 0);
         }
-        for (int q = un.q0 + lane; q < r1; q += 32) p.lse[(size_t)uy * p.va.total_q + sv.q_tok + q] = -INFINITY;
+        for (int q = un.q0 + lane; q < r1; q += 32) p.lse[(size_t)hy * p.va.total_q + sv.q_tok + q] = -INFINITY;
         return false;
       };
       for (int i = 0;; ++i) {
