@@ -732,10 +732,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             kt = kt - n_split_ctas + p.n_gk;
           }
         }
-        if (p.lpt) {
-          const int lin = uy * (int)gridDim.x + ux;
-          kt = lin / (int)gridDim.y;
-          zz = lin % (int)gridDim.y;
+        if (p.lpt) {  // rank-major within groups of p.lpt heads (all heads when p.lpt >= H)
+          const int gx = (int)gridDim.x, nh = (int)gridDim.y, gs0 = min(p.lpt, nh);
+          const int lin = uy * gx + ux;
+          const int grp = lin / (gs0 * gx), h0 = grp * gs0, gs = min(gs0, nh - h0);
+          const int idx = lin - h0 * gx;
+          kt = idx / gs;
+          zz = h0 + idx % gs;
         }
         un.k0 = kt * C::BN;
         un.z = zz;

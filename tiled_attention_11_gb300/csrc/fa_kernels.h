@@ -135,10 +135,12 @@ struct FwdParams {
   // whose CTA `pair` holds query tiles pair and n_q_tiles-1-pair instead of 2*pair and
   // 2*pair+1, so every CTA walks about the same number of key tiles.
   int fold;
-  // Dense layout, plain masks, more units than one wave: the persistent kernel (a CTA
-  // takes over not-yet-started CTAs of its grid instead of exiting).
+  // More units than one wave: the persistent kernel (a CTA takes over not-yet-started CTAs
+  // of its grid instead of exiting).
   int persist;
-  // persistent, dense: claim units longest-first over all heads instead of head by head
+  // persistent, causal: 0 claim units head by head; n > 0 rank-major (longest first) within
+  // groups of n heads, over all heads when n >= H; packed layout: any n > 0 is slot-major
+  // over all heads
   int lpt;
 };
 
@@ -179,10 +181,12 @@ struct BwdParams {
   // partial dK, dV (fp32, unscaled) into dkv_accum; bwd_kv_convert writes them out.
   int n_gk, n_qsplit, split_q;
   float* dkv_accum;     // [B*H][n_gk*128][2][D] (zeroed before the launch)
-  // Dense layout, plain masks, more units than one wave and at least one query step per
-  // key tile: the persistent kernel (a CTA takes over not-yet-started CTAs of its grid).
+  // More units than one wave: the persistent kernel (a CTA takes over not-yet-started CTAs
+  // of its grid).
   int persist;
-  // persistent, dense: claim units longest-first over all heads instead of head by head
+  // causal: 0 claim units head by head; n > 0 rank-major (longest first) within groups of
+  // n heads, over all heads when n >= H (the one-CTA kernel: any n > 0 is over all heads);
+  // packed layout, persistent: any n > 0 is slot-major over all heads
   int lpt;
 };
 
@@ -226,7 +230,8 @@ struct Fp8FwdParams {
   unsigned* status;
   // more (query-tile pair, head) units than one wave: the persistent kernel
   int persist;
-  // persistent: claim units longest-first over all heads instead of head by head
+  // persistent, causal: 0 claim units head by head; n > 0 rank-major (longest first)
+  // within groups of n heads, over all heads when n >= H
   int lpt;
 };
 

@@ -397,9 +397,22 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   // key tiles of query tile t of pair `pair` (heaviest pairs of a head first: pair =
   // gridDim.x - 1 - x)
   auto n_keys = [&](int pair, int t) { return CAUSAL ? min(nk_tiles, 2 * pair + 1 + t) : nk_tiles; };
-  // a published unit is a CTA index (x, y); lpt maps it to (pair rank, head) rank-major
-  auto unit_rank = [&](int2 u) { return p.lpt ? (u.y * (int)gridDim.x + u.x) / (int)gridDim.y : u.x; };
-  auto unit_head = [&](int2 u) { return p.lpt ? (u.y * (int)gridDim.x + u.x) % (int)gridDim.y : u.y; };
+  // a published unit is a CTA index (x, y); lpt maps it to (pair rank, head), rank-major
+  // within groups of p.lpt heads (all heads when p.lpt >= H)
+  auto unit_map = [&](int2 u, int& rank, int& head) {
+    rank = u.x;
+    head = u.y;
+    if (p.lpt) {
+      const int gx = (int)gridDim.x, nh = (int)gridDim.y, gs0 = min(p.lpt, nh);
+      const int lin = u.y * gx + u.x;
+      const int grp = lin / (gs0 * gx), h0 = grp * gs0, gs = min(gs0, nh - h0);
+      const int idx = lin - h0 * gx;
+      rank = idx / gs;
+      head = h0 + idx % gs;
+    }
+  };
+  auto unit_rank = [&](int2 u) { int r, h; unit_map(u, r, h); return r; };
+  auto unit_head = [&](int2 u) { int r, h; unit_map(u, r, h); return h; };
   const WaitCtx wc{p.wait_limit_ns, p.status, abort_flag};
 
   if (threadIdx.x == 0) {
@@ -451,13 +464,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       units[us] = make_int2(ux, uy);
       mbar_arrive_w(&bars[C::B_UF + us]);
       if (ux < 0) break;
-      // lpt: longest-first over all heads (rank-major), for causal launches of a few waves
-      int pr = ux, bh = uy;
-      if (p.lpt) {
-        const int lin = uy * (int)gridDim.x + ux;
-        pr = lin / (int)gridDim.y;
-        bh = lin % (int)gridDim.y;
-      }
+      // lpt: longest-first (rank-major) over all heads for causal launches of a few waves,
+      // within groups of heads beyond
+      int pr, bh;
+      unit_map(make_int2(ux, uy), pr, bh);
       const int pair = (int)gridDim.x - 1 - pr, q0 = pair * 2 * C::BM;
       const int n_kv = n_keys(pair, 1);  // tile 1's walk contains tile 0's
       bool ok = true;

@@ -803,10 +803,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
           // heaviest pair, then every head's next one), for launches of a few waves whose
           // tail would otherwise be one head's heaviest pairs starting last
           int pr = ux, zz = uy;
-          if (p.lpt) {
-            const int lin = uy * (int)gridDim.x + ux;
-            pr = lin / (int)gridDim.y;
-            zz = lin % (int)gridDim.y;
+          if (p.lpt) {  // rank-major within groups of p.lpt heads (all heads when p.lpt >= H)
+            const int gx = (int)gridDim.x, nh = (int)gridDim.y, gs0 = min(p.lpt, nh);
+            const int lin = uy * gx + ux;
+            const int grp = lin / (gs0 * gx), h0 = grp * gs0, gs = min(gs0, nh - h0);
+            const int idx = lin - h0 * gx;
+            pr = idx / gs;
+            zz = h0 + idx % gs;
           }
           un.q0 = ((int)gridDim.x - 1 - pr) * 2 * C::BM;
           un.z = zz;
