@@ -1203,7 +1203,9 @@ template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   using R = RowCfg<D>;
   constexpr int TPR = R::TPR;
-  const int bh = blockIdx.y;
+  // dense: the last heads first (their O was written last, still in L2), so the first heads'
+  // rows, which the main kernel takes first, are the ones left in L2 at the end
+  const int bh = VARLEN ? (int)blockIdx.y : (int)gridDim.y - 1 - (int)blockIdx.y;
   const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nq, bh);
   const int rows = VARLEN ? (sv.Nq + 63) / 64 * 64 : p.Nq_pad;  // padded rows of this sequence
   const int rb = blockIdx.x * R::ROWS_CTA;                       // first row of this block
@@ -1260,7 +1262,8 @@ template <int D, bool VARLEN>
 __global__ void __launch_bounds__(256) convert_kernel(const ConvParams p) {
   using R = RowCfg<D>;
   constexpr int TPR = R::TPR;
-  const int bh = blockIdx.y;
+  // dense: the last heads first, whose dq_accum the main kernel touched last (still in L2)
+  const int bh = VARLEN ? (int)blockIdx.y : (int)gridDim.y - 1 - (int)blockIdx.y;
   const SeqView sv = seq_view<VARLEN>(p.va, p.Nq, p.Nq, bh);
   const int rb = blockIdx.x * R::ROWS_CTA;
   if (rb >= sv.Nq) return;
