@@ -1270,8 +1270,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
             pair = pair - n_split_ctas + p.n_gp;
           }
         }
+        // causal: the last pairs first (their windows are whole; the first pairs' are cut at the
+        // sequence start), so a head ends on its light pairs; otherwise launch order (pairs
+        // holding global rows first)
+        if (CAUSAL && !SPLIT) pair = (int)gridDim.x - 1 - pair;
         un.live = ux >= 0 ? 1 : 0;
-        un.q0 = pair * 2 * C::BM;  // pairs in launch order: those holding global rows first
+        un.q0 = pair * 2 * C::BM;
         un.z = uy;
         un.q_tok = un.k_tok = 0;
         un.nq = p.Nq;
